@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module only draws random numbers and lays them out as stored operands.
+It holds none of the GEMM arithmetic: both the CUDA path (through the tests
+and the benchmark) and the CPU oracle consume the tensors it returns, so the
+two sides always see identical bits.
+
+Recipe (the same for every workload):
+  * a fresh ``torch.Generator('cpu').manual_seed(seed)`` per workload (and,
+    for the square sweep, per size);
+  * operands are drawn in the order A, then B, then C (when C is pre-filled),
+    each directly in its *stored* shape: A is [M,K], or [K,M] when
+    ``transpose_a``; B is [K,N], or [N,K] when ``transpose_b``; C is [M,N];
+  * values are drawn as fp32 -- ``uniform[-1,1]`` as ``2*rand-1`` and
+    ``normal(0,s)`` as ``s*randn`` -- then converted to the storage dtype with
+    PyTorch's round-to-nearest-even cast.
+
+The workloads follow the tensorcore gemm.md "Measured perf" shapes and the
+tessl architecture.md "Round 2 Evolutions" table (square NN, TN/NT weight
+gradient shapes, split-K and narrow-N).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@dataclass
+class Problem:
+    """One GEMM problem: C[M,N] = alpha*op(A)@op(B) + beta*C (row-major)."""
+
+    M: int
+    N: int
+    K: int
+    ab_dtype: str           # "f16" | "bf16" | "f32" (A and B share it)
+    c_dtype: str            # "f16" | "bf16" | "f32"
+    transpose_a: bool = False
+    transpose_b: bool = False
+    alpha: float = 1.0
+    beta: float = 0.0
+    A: torch.Tensor | None = field(default=None, repr=False)
+    B: torch.Tensor | None = field(default=None, repr=False)
+    C: torch.Tensor | None = field(default=None, repr=False)   # C_old (input)
+
+    @property
+    def layout(self) -> str:
+        return ("T" if self.transpose_a else "N") + ("T" if self.transpose_b else "N")
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def _draw(gen: torch.Generator, shape, dist: str, scale: float) -> torch.Tensor:
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal":
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * scale
+    if dist == "int":
+        # integer-valued entries in [-scale, scale]
+        s = int(scale)
+        return torch.randint(-s, s + 1, shape, generator=gen).to(torch.float32)
+    raise ValueError(dist)
+
+
+def make_problem(M, N, K, ab_dtype, c_dtype, *, transpose_a=False, transpose_b=False,
+                 alpha=1.0, beta=0.0, seed=0, dist="uniform", scale=1.0,
+                 c_fill="zero", gen: torch.Generator | None = None,
+                 lda=0, ldb=0, ldc=0) -> Problem:
+    """Draw one problem's operands.  ``gen`` continues an existing stream
+    (used by the ragged batch); otherwise a fresh generator seeded ``seed``.
+
+    A non-zero ``lda/ldb/ldc`` pads the stored rows to that many elements
+    (the padding holds random values as well, so a kernel that reads past
+    the logical row shows up as a parity failure)."""
+    g = gen if gen is not None else torch.Generator("cpu").manual_seed(seed)
+    dt_ab, dt_c = DTYPES[ab_dtype], DTYPES[c_dtype]
+    a_rows, a_cols = (K, M) if transpose_a else (M, K)
+    b_rows, b_cols = (N, K) if transpose_b else (K, N)
+    A = _draw(g, (a_rows, max(a_cols, lda)), dist, scale).to(dt_ab)
+    B = _draw(g, (b_rows, max(b_cols, ldb)), dist, scale).to(dt_ab)
+    if c_fill == "zero":
+        C = torch.zeros((M, max(N, ldc)), dtype=dt_c)
+    elif c_fill == "uniform":
+        C = _draw(g, (M, max(N, ldc)), "uniform", 1.0).to(dt_c)
+    elif c_fill == "nan":
+        C = torch.full((M, max(N, ldc)), float("nan"), dtype=dt_c)
+    elif c_fill == "int":
+        C = _draw(g, (M, max(N, ldc)), "int", scale).to(dt_c)
+    else:
+        raise ValueError(c_fill)
+    return Problem(M, N, K, ab_dtype, c_dtype, transpose_a, transpose_b, alpha, beta, A, B, C)
+
+
+# --------------------------------------------------------------------------
+# The named workloads.
+# --------------------------------------------------------------------------
+
+def fp32_nn_256() -> Problem:
+    """fp32 NN 256^3, uniform[-1,1] from seed 0, C zero, alpha=1 beta=0."""
+    return make_problem(256, 256, 256, "f32", "f32", seed=0, dist="uniform")
+
+
+def bf16_nn_4096() -> Problem:
+    """bf16 NN 4096^3, bf16 out, normal(0,1) from seed 1, alpha=1 beta=0."""
+    return make_problem(4096, 4096, 4096, "bf16", "bf16", seed=1, dist="normal", scale=1.0)
+
+
+def bf16_tn_nt_4096x8192(layout: str) -> Problem:
+    """bf16 M=N=4096 K=8192, fp32 out, alpha=0.5 beta=1, C uniform[-1,1],
+    inputs normal(0,0.02) from seed 2.  ``layout`` is "TN" (A stored [K,M])
+    or "NT" (B stored [N,K])."""
+    assert layout in ("TN", "NT")
+    return make_problem(4096, 4096, 8192, "bf16", "f32", transpose_a=(layout == "TN"),
+                        transpose_b=(layout == "NT"), alpha=0.5, beta=1.0, seed=2,
+                        dist="normal", scale=0.02, c_fill="uniform")
+
+
+def bf16_tn_splitk_256x16384() -> Problem:
+    """bf16 TN M=N=256 K=16384 (weight-gradient shape), fp32 out, normal(0,1), seed 3."""
+    return make_problem(256, 256, 16384, "bf16", "f32", transpose_a=True, seed=3,
+                        dist="normal", scale=1.0)
+
+
+def fp16_nn_narrow_8192x384x4096() -> Problem:
+    """fp16 NN M=8192 N=384 K=4096, fp16 out, normal(0,1) from a fresh seed-3 generator."""
+    return make_problem(8192, 384, 4096, "f16", "f16", seed=3, dist="normal", scale=1.0)
+
+
+SQUARE_SIZES = (256, 512, 1024, 2048, 4096, 8192)
+
+
+def fp16_nn_square(n: int) -> Problem:
+    """fp16 NN n^3, fp16 out, uniform[-1,1], fresh seed-4 generator per size."""
+    return make_problem(n, n, n, "f16", "f16", seed=4, dist="uniform")
+
+
+def ragged_shapes(count: int = 64, lo: int = 1, hi: int = 3000, seed: int = 4):
+    """The (M,N,K) triples of the ragged batch, drawn first from a fresh generator."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    mnk = torch.randint(lo, hi + 1, (count, 3), generator=g)
+    return g, [tuple(int(v) for v in row) for row in mnk]
+
+
+def fp16_ragged(count: int = 64, lo: int = 1, hi: int = 3000, seed: int = 4):
+    """64 independent fp16 NN problems, M,N,K ~ U[1,3000], contiguous, uniform[-1,1]."""
+    g, shapes = ragged_shapes(count, lo, hi, seed)
+    return [make_problem(M, N, K, "f16", "f16", gen=g, dist="uniform") for (M, N, K) in shapes]

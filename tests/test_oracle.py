@@ -1,0 +1,315 @@
+"""Pins for the CPU oracle (no GPU needed).
+
+The oracle is checked against things other than itself:
+  * exhaustive decoding of every binary16 / bfloat16 bit pattern against
+    PyTorch's casts (an independent implementation of the encodings);
+  * the worked 2x2 input of the Foundry metal.md "Quick Start" and its closed
+    form (tests/golden/foundry_quickstart_2x2.txt);
+  * exact rational arithmetic (``fractions``) on tiny shapes, every layout,
+    padded leading dimensions, alpha/beta;
+  * numpy's float64 matmul on operands decoded by PyTorch;
+  * closed forms: identity, permutation, rank one (K = 1), alpha/beta on
+    integer data, beta = 0 ignoring a NaN-filled C;
+  * mutation tests: plausible mistakes planted in a copy of oracle.c (a
+    swapped index, a dropped term, a wrong sign, a wrong decoder bias, a
+    wrong default leading dimension, a signed T) must each fail a pin.
+"""
+from __future__ import annotations
+
+import itertools
+import os
+import re
+import subprocess
+import tempfile
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LAYOUTS = [(False, False), (True, False), (False, True), (True, True)]
+
+
+def torch_decode(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def op_a(p, Ad):
+    return Ad[: p.K, : p.M].T if p.transpose_a else Ad[: p.M, : p.K]
+
+
+def op_b(p, Bd):
+    return Bd[: p.N, : p.K].T if p.transpose_b else Bd[: p.K, : p.N]
+
+
+# ---------------------------------------------------------------- decoders
+
+@pytest.mark.parametrize("name,tdt", [("f16", torch.float16), ("bf16", torch.bfloat16)])
+def test_decoder_exhaustive(name, tdt):
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16)
+    t = bits.view(tdt)
+    mine = oracle.decode(t)
+    ref = torch_decode(t)
+    nan_m, nan_r = np.isnan(mine), np.isnan(ref)
+    assert (nan_m == nan_r).all()
+    assert (mine[~nan_m] == ref[~nan_r]).all()
+    # signed zeros and infinities keep their sign
+    assert (np.signbit(mine[~nan_m]) == np.signbit(ref[~nan_r])).all()
+
+
+def test_decoder_f32_widening():
+    g = torch.Generator().manual_seed(5)
+    t = torch.randn(10000, generator=g) * 1e30
+    t[:4] = torch.tensor([0.0, -0.0, float("inf"), 1e-45])
+    assert (oracle.decode(t) == t.to(torch.float64).numpy()).all()
+
+
+# ---------------------------------------------------------- worked example
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            vals[k.strip()] = [float(x) for x in v.split()]
+    return vals
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_worked_example_2x2(dt, ta, tb):
+    g = _read_golden("foundry_quickstart_2x2.txt")
+    M, N, K = (int(v) for v in g["M N K"])
+    A = torch.tensor(g["A"]).reshape(M, K)
+    B = torch.tensor(g["B"]).reshape(K, N)
+    want = np.array(g["C"]).reshape(M, N)
+    p = synthetic.Problem(M, N, K, dt, dt, ta, tb, g["alpha beta"][0], g["alpha beta"][1],
+                          (A.T if ta else A).contiguous().to(synthetic.DTYPES[dt]),
+                          (B.T if tb else B).contiguous().to(synthetic.DTYPES[dt]),
+                          torch.zeros(M, N, dtype=synthetic.DTYPES[dt]))
+    R, T = oracle.gemm(p)
+    assert (R == want).all()
+    assert (T == want).all()          # all products positive here
+
+
+# ------------------------------------------------------ exact brute force
+
+def exact_reference(p):
+    """R and T in exact rational arithmetic from PyTorch-decoded operands."""
+    Ad, Bd = torch_decode(p.A), torch_decode(p.B)
+    a, b = op_a(p, Ad), op_b(p, Bd)
+    Cd = torch_decode(p.C)
+    alpha = Fraction(float(np.float32(p.alpha)))
+    beta = Fraction(float(np.float32(p.beta)))
+    R = np.empty((p.M, p.N), dtype=object)
+    T = np.empty((p.M, p.N), dtype=object)
+    for i in range(p.M):
+        for j in range(p.N):
+            s = Fraction(0)
+            t = Fraction(0)
+            for k in range(p.K):
+                prod = Fraction(float(a[i, k])) * Fraction(float(b[k, j]))
+                s += prod
+                t += abs(prod)
+            r = alpha * s
+            if p.beta != 0:
+                r += beta * Fraction(float(Cd[i, j]))
+            R[i, j] = r
+            T[i, j] = t
+    return R, T
+
+
+def tiny_problems():
+    """A fixed family of tiny problems covering every dtype, layout, padded
+    leading dimension, alpha/beta choice and a NaN-filled C with beta = 0."""
+    out = []
+    seed = 100
+    for dt, (ta, tb) in itertools.product(["f16", "bf16", "f32"], LAYOUTS):
+        for (M, N, K, alpha, beta, fill, pad) in [(3, 5, 4, 1.0, 0.0, "nan", 0),
+                                                   (5, 2, 7, -0.75, 1.5, "uniform", 3),
+                                                   (1, 6, 1, 2.0, -1.0, "uniform", 1)]:
+            seed += 1
+            lda = (M if ta else K) + pad if pad else 0
+            ldb = (K if tb else N) + pad if pad else 0
+            ldc = N + pad if pad else 0
+            out.append(synthetic.make_problem(M, N, K, dt, dt, transpose_a=ta, transpose_b=tb,
+                                              alpha=alpha, beta=beta, seed=seed, dist="normal",
+                                              scale=3.0, c_fill=fill, lda=lda, ldb=ldb, ldc=ldc))
+    return out
+
+
+def pins_pass(lib) -> list[str]:
+    """Run the pins against a build of the oracle; return the failures."""
+    fails = []
+    # exact rational brute force
+    for p in tiny_problems():
+        R, T = oracle.gemm(p, lib=lib)
+        Rx, Tx = exact_reference(p)
+        scale = np.array([[float(abs(v)) for v in row] for row in Tx]) + 1.0
+        errR = np.array([[abs(float(Fraction(R[i, j]) - Rx[i, j])) if np.isfinite(R[i, j]) else np.inf
+                          for j in range(p.N)] for i in range(p.M)])
+        errT = np.array([[abs(float(Fraction(T[i, j]) - Tx[i, j])) if np.isfinite(T[i, j]) else np.inf
+                          for j in range(p.N)] for i in range(p.M)])
+        if not (errR <= 1e-13 * scale).all() or not (errT <= 1e-13 * scale).all():
+            fails.append(f"brute force {p.M}x{p.N}x{p.K} {p.ab_dtype} {p.layout}")
+        # the single-element path must agree with the row path bitwise
+        ii, jj = np.meshgrid(np.arange(p.M), np.arange(p.N), indexing="ij")
+        Rp, Tp = oracle.gemm_points(p, ii.ravel(), jj.ravel(), lib=lib)
+        if not (np.array_equal(Rp, R.ravel(), equal_nan=True) and np.array_equal(Tp, T.ravel())):
+            fails.append(f"points != rows {p.layout}")
+    # decoder exhaustive
+    for tdt in (torch.float16, torch.bfloat16):
+        t = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16).view(tdt)
+        mine, ref = oracle.decode(t, lib=lib), torch_decode(t)
+        if not np.array_equal(mine, ref, equal_nan=True):
+            fails.append(f"decode {tdt}")
+    # default (ld = 0) leading dimensions on a non-square problem
+    p = synthetic.make_problem(3, 5, 4, "f32", "f32", transpose_a=True, transpose_b=True,
+                               alpha=1.0, beta=1.0, seed=7, c_fill="uniform")
+    s_rows = oracle.gemm(p, lib=lib)[0]
+    s, keep = oracle._struct(p, lda=0, ldb=0, ldc=0)
+    import ctypes
+    R0 = np.empty((3, 5))
+    T0 = np.empty((3, 5))
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_gemm_rows(ctypes.byref(s), 0, 3, R0.ctypes.data_as(dp), T0.ctypes.data_as(dp))
+    if not np.array_equal(R0, s_rows):
+        fails.append("ld = 0 default")
+    return fails
+
+
+def test_pins_pass_on_oracle():
+    assert pins_pass(oracle.load_library()) == []
+
+
+MUTATIONS = {
+    # (regex on oracle.c, replacement): a plausible mistake each
+    "transpose_a index swapped": (r"\? k \* lda \+ i : i \* lda \+ k", "? i * lda + k : k * lda + i"),
+    "transpose_b ignored": (r"return p->transpose_b \? j \* ldb \+ k : k \* ldb \+ j;",
+                            "return k * ldb + j;"),
+    "beta term dropped": (r"r \+= p->beta \* load\(p->C, p->c_dtype, i \* ldc \+ j\);\n            S\[j\] = r;",
+                          "S[j] = r;"),
+    "alpha sign flipped": (r"double r = p->alpha \* S\[j\];", "double r = -p->alpha * S[j];"),
+    "f16 exponent bias off by one": (r"e - 25\)", "e - 24)"),
+    "bf16 subnormal scale wrong": (r"-133\)", "-126)"),
+    "default ldc uses M": (r"\*ldc = p->ldc \? p->ldc : p->N;", "*ldc = p->ldc ? p->ldc : p->M;"),
+    "T signed": (r"Ta\[j\] \+= fabs\(prod\);", "Ta[j] += prod;"),
+    "last k dropped": (r"for \(int64_t k = 0; k < K; \+\+k\) \{\n            const double a",
+                       "for (int64_t k = 0; k < K - 1; ++k) {\n            const double a"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name):
+    pat, rep = MUTATIONS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    mutated, n = re.subn(pat, rep, src)
+    assert n >= 1, f"mutation {name!r} did not apply"
+    with tempfile.TemporaryDirectory() as d:
+        cpath = os.path.join(d, "mutant.c")
+        with open(cpath, "w") as f:
+            f.write(mutated)
+        so = oracle.build(cpath, os.path.join(d, "libmutant.so"))
+        lib = oracle.load_library(so)
+        assert pins_pass(lib) != [], f"planted mistake {name!r} went unnoticed"
+
+
+# ------------------------------------------------------- library special case
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_vs_numpy_float64(dt, ta, tb):
+    M, N, K = 67, 45, 129
+    p = synthetic.make_problem(M, N, K, dt, "f32", transpose_a=ta, transpose_b=tb, alpha=0.5,
+                               beta=-2.0, seed=11, dist="normal", c_fill="uniform",
+                               lda=(M if ta else K) + 5, ldb=(K if tb else N) + 2, ldc=N + 7)
+    R, T = oracle.gemm(p)
+    a = op_a(p, torch_decode(p.A))
+    b = op_b(p, torch_decode(p.B))
+    ref = float(np.float32(0.5)) * (a @ b) + (-2.0) * torch_decode(p.C)[:, :N]
+    Tref = np.abs(a) @ np.abs(b)
+    assert np.all(np.abs(R - ref) <= 1e-12 * (Tref + 1.0))
+    assert np.all(np.abs(T - Tref) <= 1e-12 * Tref)
+
+
+# -------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_identity(dt):
+    n = 40
+    p = synthetic.make_problem(n, 24, n, dt, "f32", seed=3, dist="normal")
+    p.A = torch.eye(n).to(synthetic.DTYPES[dt])
+    R, _ = oracle.gemm(p)
+    assert (R == torch_decode(p.B)).all()
+
+
+def test_permutation_transposed():
+    n = 33
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(9))
+    P = torch.zeros(n, n)
+    P[torch.arange(n), perm] = 1.0
+    p = synthetic.make_problem(n, 17, n, "bf16", "f32", transpose_a=True, seed=4, dist="normal")
+    p.A = P.T.contiguous().to(torch.bfloat16)        # stored [K,M]: op(A) = P
+    R, _ = oracle.gemm(p)
+    assert (R == torch_decode(p.B)[perm]).all()
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+def test_rank_one(dt):
+    p = synthetic.make_problem(31, 29, 1, dt, "f32", seed=8, dist="normal")
+    R, T = oracle.gemm(p)
+    a = torch_decode(p.A)[:, 0]
+    b = torch_decode(p.B)[0, :]
+    assert (R == np.outer(a, b)).all()
+    assert (T == np.abs(np.outer(a, b))).all()
+
+
+def test_alpha_beta_integer_exact():
+    p = synthetic.make_problem(20, 30, 50, "bf16", "f32", transpose_b=True, alpha=0.5, beta=1.0,
+                               seed=12, dist="int", scale=4, c_fill="int")
+    R, _ = oracle.gemm(p)
+    a = op_a(p, torch_decode(p.A)).astype(np.int64)
+    b = op_b(p, torch_decode(p.B)).astype(np.int64)
+    exact = (a @ b) * 0.5 + torch_decode(p.C)
+    assert (R == exact).all()
+
+
+def test_beta_zero_ignores_nan_c():
+    p = synthetic.make_problem(9, 7, 5, "f16", "f16", seed=2, c_fill="nan")
+    R, _ = oracle.gemm(p)
+    assert np.isfinite(R).all()
+
+
+def test_linearity_in_alpha_and_beta():
+    base = dict(M=12, N=10, K=40, ab_dtype="bf16", c_dtype="f32")
+    p1 = synthetic.make_problem(**base, alpha=1.0, beta=0.0, seed=21, c_fill="uniform")
+    p2 = synthetic.make_problem(**base, alpha=0.25, beta=0.0, seed=21, c_fill="uniform")
+    p3 = synthetic.make_problem(**base, alpha=1.0, beta=2.0, seed=21, c_fill="uniform")
+    R1, _ = oracle.gemm(p1)
+    R2, _ = oracle.gemm(p2)
+    R3, _ = oracle.gemm(p3)
+    assert np.array_equal(R2, 0.25 * R1)                 # power-of-two scaling is exact
+    assert np.allclose(R3 - R1, 2.0 * torch_decode(p1.C), rtol=0, atol=1e-12)
+
+
+def test_sub_block_consistency():
+    p = synthetic.make_problem(40, 36, 64, "f16", "f32", seed=13, dist="normal")
+    R, T = oracle.gemm(p)
+    q = synthetic.Problem(10, 12, 64, "f16", "f32", A=p.A[5:15].contiguous(),
+                          B=p.B[:, 20:32].contiguous(), C=torch.zeros(10, 12))
+    Rq, Tq = oracle.gemm(q)
+    assert np.array_equal(Rq, R[5:15, 20:32]) and np.array_equal(Tq, T[5:15, 20:32])
+
+
+def test_row_band_matches_full():
+    p = synthetic.make_problem(30, 20, 50, "bf16", "bf16", seed=14, dist="normal")
+    R, T = oracle.gemm(p)
+    Rb, Tb = oracle.gemm(p, 7, 19)
+    assert np.array_equal(Rb, R[7:19]) and np.array_equal(Tb, T[7:19])
