@@ -1,0 +1,156 @@
+/*
+ * tcgemm -- GEMM for GB300 (sm_103a): C = alpha * op(A) @ op(B) + beta * C.
+ *
+ * The operation is the one defined on the tensorcore gemm.md page, section
+ * "Surface": BLAS row-major layout, C[M,N] = alpha * A[M,K] @ B[K,N] +
+ * beta * C[M,N], with optional transposes and leading dimensions that
+ * default to row-major contiguous when 0.  The descriptor below keeps that
+ * page's field list.  The async/stream and batched calls follow the same
+ * page's section "Async, batched, and streams"; the validation order (checked
+ * sizes, non-zero dims, finite scalars, no overlap, nothing launched on
+ * error) follows the tessl architecture.md sections "GEMM Pipeline & Kernel
+ * Selection" and "The Kernel Library and the nn Boundary".
+ *
+ * Conventions shared by every call:
+ *   - Matrices are row-major.  op(A) is A stored [M,K] (lda >= K), or, with
+ *     transpose_a, A stored [K,M] (lda >= M).  op(B) is B stored [K,N]
+ *     (ldb >= N), or, with transpose_b, B stored [N,K] (ldb >= K) -- the
+ *     layout of a linear layer's weight (phobos matmul page, "matmul_t").
+ *     C is stored [M,N] (ldc >= N).  Leading dimensions count ELEMENTS;
+ *     0 means contiguous.
+ *   - A, B and C are DEVICE pointers (except tc_gemm_host) owned by the
+ *     caller; they must stay valid until the work completes (tc_stream_sync
+ *     for the async calls).  The library never frees caller memory.
+ *   - Types: a_dtype == b_dtype in {TC_F16, TC_BF16, TC_F32};
+ *     accum_dtype == TC_F32; c_dtype == a_dtype or TC_F32.  f16/bf16 inputs
+ *     run on the tcgen05 tensor cores; f32 inputs run on FFMA CUDA cores in
+ *     exact fp32 (never TF32).
+ *   - beta == 0 means C is not read (NaN/Inf in C do not propagate).
+ *     alpha == 0 is not special-cased.  The output is rounded once,
+ *     round-to-nearest-even, from the fp32 value alpha*acc + beta*C_old.
+ *   - Results are bitwise deterministic run to run for every variant,
+ *     including split-K.
+ *   - Errors: every call returns a tc_status_t and never aborts or traps.
+ *     On any error detected before launch, nothing is enqueued and C is
+ *     untouched.  A raw-pointer ABI cannot check buffer capacity; the
+ *     Python binding checks capacity in elements.  Failures on the device
+ *     surface at tc_stream_sync / the synchronous call.
+ */
+#ifndef TCGEMM_H
+#define TCGEMM_H
+
+#include <stdbool.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TC_F16 = 1, TC_BF16 = 2, TC_F32 = 3 } tc_dtype_t;
+
+typedef enum {
+    TC_OK = 0,
+    TC_ERR_NULL = 1,               /* a required pointer is NULL */
+    TC_ERR_DIM = 2,                /* M, N or K outside [1, 2^31-1]; batch < 1 */
+    TC_ERR_LD = 3,                 /* a leading dimension below its minimum, or negative */
+    TC_ERR_DTYPE = 4,              /* unsupported dtype combination */
+    TC_ERR_SCALAR = 5,             /* alpha or beta not finite */
+    TC_ERR_OVERLAP = 6,            /* C's byte range overlaps A's or B's */
+    TC_ERR_OVERFLOW = 7,           /* an element or byte count overflows int64 */
+    TC_ERR_ALIGN_UNSUPPORTED = 8,  /* reserved: every valid input has a kernel */
+    TC_ERR_CUDA = 9,               /* a CUDA runtime error (launch, copy, no device) */
+    TC_ERR_DEVICE_TIMEOUT = 10,    /* a kernel's bounded wait expired; it stopped early */
+    TC_ERR_STRIDE = 11,            /* batched: negative stride */
+    TC_ERR_VARIANT = 12            /* a forced variant cannot serve this problem */
+} tc_status_t;
+
+/* tensorcore gemm.md, "Surface": the GEMM descriptor, field for field. */
+typedef struct {
+    int32_t M, N, K;
+    tc_dtype_t a_dtype, b_dtype, c_dtype, accum_dtype;
+    bool transpose_a, transpose_b;
+    float alpha, beta;
+    int32_t lda, ldb, ldc;
+} tc_gemm_desc;
+
+/* tensorcore gemm.md, "Async, batched, and streams": same-shape batch with
+ * element strides between consecutive matrices (stride 0 = the same matrix
+ * for every batch entry, allowed for A and B only). */
+typedef struct {
+    tc_gemm_desc base;
+    int32_t batch;
+    int64_t stride_a, stride_b, stride_c;
+} tc_gemm_batched_desc;
+
+typedef struct tc_ctx tc_ctx;
+typedef struct tc_stream tc_stream;
+
+/* Create a context on CUDA device `device` (it becomes current for the
+ * calling thread).  The context owns the TMA descriptor encoder, a default
+ * stream and a device status word.  Returns TC_ERR_CUDA when no usable
+ * device exists.  *out is NULL on error. */
+tc_status_t tc_ctx_create(tc_ctx **out, int device);
+void tc_ctx_destroy(tc_ctx *ctx);
+
+/* tensorcore gemm.md, "Async, batched, and streams": a stream on which
+ * tc_gemm_async enqueues work; only tc_stream_sync waits for it.  Each
+ * stream owns its own workspace (split-K partials, repacked operands), so
+ * work on different streams never shares scratch memory. */
+tc_status_t tc_stream_create(tc_ctx *ctx, tc_stream **out);
+/* Wrap an existing cudaStream_t (e.g. PyTorch's current stream); the
+ * library does not destroy the wrapped stream. */
+tc_status_t tc_stream_wrap(tc_ctx *ctx, void *cuda_stream, tc_stream **out);
+/* Wait for the stream's work; returns TC_ERR_DEVICE_TIMEOUT if a kernel
+ * reported an expired wait, TC_ERR_CUDA on a CUDA error. */
+tc_status_t tc_stream_sync(tc_stream *s);
+/* The cudaStream_t behind the stream (for event timing by the caller). */
+void *tc_stream_handle(tc_stream *s);
+void tc_stream_destroy(tc_stream *s);
+
+/* Synchronous GEMM on the context's default stream (returns when C is
+ * written). */
+tc_status_t tc_gemm(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B, void *C);
+/* Enqueue the GEMM on stream s and return. */
+tc_status_t tc_gemm_async(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B,
+                          void *C, tc_stream *s);
+/* Same-shape batch: matrix i is at A + i*stride_a (elements), etc.  One
+ * launch covers every batch entry. */
+tc_status_t tc_gemm_batched(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A,
+                            const void *B, void *C);
+tc_status_t tc_gemm_batched_async(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A,
+                                  const void *B, void *C, tc_stream *s);
+/* n independent problems (each with its own descriptor and pointers),
+ * enqueued on s.  All descriptors are validated before anything is
+ * enqueued. */
+tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d,
+                                  const void *const *A, const void *const *B, void *const *C,
+                                  tc_stream *s);
+/* Same GEMM with HOST operands: copies A and B (and C when beta != 0) to the
+ * device, runs, copies C back and waits.  Device buffers are cached in the
+ * context.  Pinned host memory gives full copy bandwidth. */
+tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
+                         const void *B_host, void *C_host);
+
+/* Host-only checks, no device needed: the same validation every call runs
+ * first.  A, B, C are only compared as addresses (overlap), never read. */
+tc_status_t tc_gemm_validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C);
+tc_status_t tc_gemm_batched_validate(const tc_gemm_batched_desc *bd, const void *A,
+                                     const void *B, const void *C);
+/* Host-only: the kernel variant the dispatcher would pick for this problem
+ * on a GPU with num_sms SMs, written into buf (NUL-terminated, truncated to
+ * len).  A, B, C are inspected for 16-byte alignment only. */
+tc_status_t tc_gemm_plan(const tc_gemm_desc *d, const void *A, const void *B, const void *C,
+                         int num_sms, char *buf, size_t len);
+
+/* The variant and configuration of the last kernel this context launched
+ * (tensorcore gemm.md "Fallback ladder": which path served the call). */
+const char *tc_last_kernel(tc_ctx *ctx);
+/* Number of kernels this context has launched (0 after any refused call). */
+uint64_t tc_launch_count(tc_ctx *ctx);
+const char *tc_status_string(tc_status_t st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TCGEMM_H */

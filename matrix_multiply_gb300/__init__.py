@@ -1,0 +1,342 @@
+"""Python binding of tcgemm, the GB300 (sm_103a) GEMM library.
+
+C = alpha * op(A) @ op(B) + beta * C, row-major, NN/TN/NT/TT, leading
+dimensions, f16/bf16 (tcgen05 tensor cores) or f32 (exact FFMA) inputs with
+fp32 accumulation -- the operation of the tensorcore gemm.md page, section
+"Surface".
+
+This module only marshals arguments: every step of the computation runs in
+the CUDA kernels of ``_lib/libtcgemm.so``.  The functions keep the C names
+(``tc_gemm``, ``tc_gemm_async``, ``tc_gemm_batched``, ...) and take either raw
+device addresses or torch tensors (PyTorch provides device memory and
+streams only).  Where a tensor is given, its capacity is checked in
+elements before the call (the tessl architecture.md "nn Boundary" rule: a
+view of too few elements is refused, nothing is launched).
+
+There is no fallback: if the library is missing, importing this package
+raises.  Build it with ``python -c "import __graft_entry__ as g; g.build()"``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtcgemm.so")
+
+# ------------------------------------------------------------------ enums
+
+TC_F16, TC_BF16, TC_F32 = 1, 2, 3
+STATUS = {
+    0: "TC_OK", 1: "TC_ERR_NULL", 2: "TC_ERR_DIM", 3: "TC_ERR_LD", 4: "TC_ERR_DTYPE",
+    5: "TC_ERR_SCALAR", 6: "TC_ERR_OVERLAP", 7: "TC_ERR_OVERFLOW", 8: "TC_ERR_ALIGN_UNSUPPORTED",
+    9: "TC_ERR_CUDA", 10: "TC_ERR_DEVICE_TIMEOUT", 11: "TC_ERR_STRIDE", 12: "TC_ERR_VARIANT",
+}
+for _code, _name in STATUS.items():
+    globals()[_name] = _code
+
+
+class tc_gemm_desc(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("a_dtype", ctypes.c_int), ("b_dtype", ctypes.c_int), ("c_dtype", ctypes.c_int),
+        ("accum_dtype", ctypes.c_int),
+        ("transpose_a", ctypes.c_bool), ("transpose_b", ctypes.c_bool),
+        ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+        ("lda", ctypes.c_int32), ("ldb", ctypes.c_int32), ("ldc", ctypes.c_int32),
+    ]
+
+
+class tc_gemm_batched_desc(ctypes.Structure):
+    _fields_ = [("base", tc_gemm_desc), ("batch", ctypes.c_int32),
+                ("stride_a", ctypes.c_int64), ("stride_b", ctypes.c_int64),
+                ("stride_c", ctypes.c_int64)]
+
+
+class TcError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_lib.tc_status_string(status).decode()})")
+
+
+# ------------------------------------------------------------------ loading
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"tcgemm CUDA library not built ({LIB_PATH} missing); run "
+            "python -c \"import __graft_entry__ as g; g.build()\"")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, st = ctypes.c_void_p, ctypes.c_int
+    D = ctypes.POINTER(tc_gemm_desc)
+    BD = ctypes.POINTER(tc_gemm_batched_desc)
+    sig = {
+        "tc_ctx_create": (st, [ctypes.POINTER(vp), ctypes.c_int]),
+        "tc_ctx_destroy": (None, [vp]),
+        "tc_stream_create": (st, [vp, ctypes.POINTER(vp)]),
+        "tc_stream_wrap": (st, [vp, vp, ctypes.POINTER(vp)]),
+        "tc_stream_sync": (st, [vp]),
+        "tc_stream_handle": (vp, [vp]),
+        "tc_stream_destroy": (None, [vp]),
+        "tc_gemm": (st, [vp, D, vp, vp, vp]),
+        "tc_gemm_async": (st, [vp, D, vp, vp, vp, vp]),
+        "tc_gemm_batched": (st, [vp, BD, vp, vp, vp]),
+        "tc_gemm_batched_async": (st, [vp, BD, vp, vp, vp, vp]),
+        "tc_gemm_grouped_async": (st, [vp, ctypes.c_int, D, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                       ctypes.POINTER(vp), vp]),
+        "tc_gemm_host": (st, [vp, D, vp, vp, vp]),
+        "tc_gemm_validate": (st, [D, vp, vp, vp]),
+        "tc_gemm_batched_validate": (st, [BD, vp, vp, vp]),
+        "tc_gemm_plan": (st, [D, vp, vp, vp, ctypes.c_int, ctypes.c_char_p, ctypes.c_size_t]),
+        "tc_last_kernel": (ctypes.c_char_p, [vp]),
+        "tc_launch_count": (ctypes.c_uint64, [vp]),
+        "tc_status_string": (ctypes.c_char_p, [st]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+EXPORTED = (
+    "tc_ctx_create", "tc_ctx_destroy", "tc_stream_create", "tc_stream_wrap", "tc_stream_sync",
+    "tc_stream_handle", "tc_stream_destroy", "tc_gemm", "tc_gemm_async", "tc_gemm_batched",
+    "tc_gemm_batched_async", "tc_gemm_grouped_async", "tc_gemm_host", "tc_gemm_validate",
+    "tc_gemm_batched_validate", "tc_gemm_plan", "tc_last_kernel", "tc_launch_count",
+    "tc_status_string",
+)
+
+
+def library():
+    """The loaded ctypes library (for tests that call the ABI directly)."""
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise TcError(status, what)
+
+
+# ------------------------------------------------------------------ helpers
+
+_DT_NAMES = {"f16": TC_F16, "bf16": TC_BF16, "f32": TC_F32}
+
+
+def _torch_dtype_code(t) -> int:
+    import torch
+    return {torch.float16: TC_F16, torch.bfloat16: TC_BF16, torch.float32: TC_F32}[t.dtype]
+
+
+def _addr(x) -> int:
+    """A device address from a torch tensor or an int."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def make_desc(M, N, K, a_dtype, c_dtype=None, *, transpose_a=False, transpose_b=False,
+              alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0) -> tc_gemm_desc:
+    a = _DT_NAMES.get(a_dtype, a_dtype)
+    c = _DT_NAMES.get(c_dtype, c_dtype) if c_dtype is not None else a
+    return tc_gemm_desc(M, N, K, a, a, c, TC_F32, bool(transpose_a), bool(transpose_b),
+                        float(alpha), float(beta), lda, ldb, ldc)
+
+
+def _require(t, n_elems: int, what: str):
+    """Capacity check in elements (tessl architecture.md, 'nn Boundary')."""
+    if t is None or isinstance(t, int):
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
+    if n_elems > avail:
+        raise ValueError(f"{what} holds {avail} elements, the descriptor needs {n_elems}")
+
+
+def _extent(rows, cols, ld):
+    return (rows - 1) * ld + cols
+
+
+def _check_capacity(d: tc_gemm_desc, A, B, C, batch=1, sa=0, sb=0, sc=0):
+    lda = d.lda or (d.M if d.transpose_a else d.K)
+    ldb = d.ldb or (d.K if d.transpose_b else d.N)
+    ldc = d.ldc or d.N
+    ar, ac = (d.K, d.M) if d.transpose_a else (d.M, d.K)
+    br, bc = (d.N, d.K) if d.transpose_b else (d.K, d.N)
+    if min(d.M, d.N, d.K, batch) < 1 or lda < ac or ldb < bc or ldc < d.N:
+        return   # the library reports the precise error
+    _require(A, (batch - 1) * sa + _extent(ar, ac, lda), "A")
+    _require(B, (batch - 1) * sb + _extent(br, bc, ldb), "B")
+    _require(C, (batch - 1) * sc + _extent(d.M, d.N, ldc), "C")
+
+
+# ------------------------------------------------------------------ objects
+
+class Context:
+    """A tc_ctx on one CUDA device."""
+
+    def __init__(self, device: int = 0):
+        p = ctypes.c_void_p()
+        _check(_lib.tc_ctx_create(ctypes.byref(p), device), "tc_ctx_create")
+        self.ptr = p.value
+        self.device = device
+
+    def close(self):
+        if self.ptr:
+            _lib.tc_ctx_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def last_kernel(self) -> str:
+        return _lib.tc_last_kernel(self.ptr).decode()
+
+    @property
+    def launch_count(self) -> int:
+        return int(_lib.tc_launch_count(self.ptr))
+
+
+class Stream:
+    """A tc_stream: owned (created by the library) or wrapping a torch stream."""
+
+    def __init__(self, ctx: Context, torch_stream=None):
+        p = ctypes.c_void_p()
+        if torch_stream is None:
+            _check(_lib.tc_stream_create(ctx.ptr, ctypes.byref(p)), "tc_stream_create")
+        else:
+            _check(_lib.tc_stream_wrap(ctx.ptr, ctypes.c_void_p(torch_stream.cuda_stream),
+                                       ctypes.byref(p)), "tc_stream_wrap")
+        self.ptr = p.value
+        self.ctx = ctx
+
+    @property
+    def handle(self) -> int:
+        return _lib.tc_stream_handle(self.ptr) or 0
+
+    def sync(self):
+        _check(_lib.tc_stream_sync(self.ptr), "tc_stream_sync")
+
+    def close(self):
+        if self.ptr:
+            _lib.tc_stream_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------ C names
+
+def tc_gemm(ctx: Context, d: tc_gemm_desc, A, B, C):
+    _check_capacity(d, A, B, C)
+    _check(_lib.tc_gemm(ctx.ptr, ctypes.byref(d), _addr(A), _addr(B), _addr(C)), "tc_gemm")
+
+
+def tc_gemm_async(ctx: Context, d: tc_gemm_desc, A, B, C, stream: Stream):
+    _check_capacity(d, A, B, C)
+    _check(_lib.tc_gemm_async(ctx.ptr, ctypes.byref(d), _addr(A), _addr(B), _addr(C), stream.ptr),
+           "tc_gemm_async")
+
+
+def tc_gemm_batched(ctx: Context, bd: tc_gemm_batched_desc, A, B, C):
+    _check_capacity(bd.base, A, B, C, bd.batch, bd.stride_a, bd.stride_b, bd.stride_c)
+    _check(_lib.tc_gemm_batched(ctx.ptr, ctypes.byref(bd), _addr(A), _addr(B), _addr(C)),
+           "tc_gemm_batched")
+
+
+def tc_gemm_batched_async(ctx: Context, bd: tc_gemm_batched_desc, A, B, C, stream: Stream):
+    _check_capacity(bd.base, A, B, C, bd.batch, bd.stride_a, bd.stride_b, bd.stride_c)
+    _check(_lib.tc_gemm_batched_async(ctx.ptr, ctypes.byref(bd), _addr(A), _addr(B), _addr(C),
+                                      stream.ptr), "tc_gemm_batched_async")
+
+
+def tc_gemm_grouped_async(ctx: Context, descs, As, Bs, Cs, stream: Stream):
+    n = len(descs)
+    for d, a, b, c in zip(descs, As, Bs, Cs):
+        _check_capacity(d, a, b, c)
+    arr = (tc_gemm_desc * n)(*descs)
+    pa = (ctypes.c_void_p * n)(*[_addr(x) for x in As])
+    pb = (ctypes.c_void_p * n)(*[_addr(x) for x in Bs])
+    pc = (ctypes.c_void_p * n)(*[_addr(x) for x in Cs])
+    _check(_lib.tc_gemm_grouped_async(ctx.ptr, n, arr, pa, pb, pc, stream.ptr), "tc_gemm_grouped_async")
+
+
+def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):
+    """Host operands (CPU tensors, ideally pinned): copy in, run, copy out."""
+    for t in (A_host, B_host, C_host):
+        if not isinstance(t, int) and t.is_cuda:
+            raise ValueError("tc_gemm_host takes host tensors")
+    _check(_lib.tc_gemm_host(ctx.ptr, ctypes.byref(d), _addr(A_host), _addr(B_host), _addr(C_host)),
+           "tc_gemm_host")
+
+
+def tc_gemm_validate(d: tc_gemm_desc, A=1 << 20, B=2 << 40, C=3 << 40) -> int:
+    """Host-only validation status (no device needed)."""
+    return int(_lib.tc_gemm_validate(ctypes.byref(d) if d is not None else None,
+                                     _addr(A), _addr(B), _addr(C)))
+
+
+def tc_gemm_batched_validate(bd: tc_gemm_batched_desc, A=1 << 20, B=2 << 40, C=3 << 40) -> int:
+    return int(_lib.tc_gemm_batched_validate(ctypes.byref(bd), _addr(A), _addr(B), _addr(C)))
+
+
+def tc_gemm_plan(d: tc_gemm_desc, A=1 << 20, B=2 << 40, C=3 << 40, num_sms: int = 152) -> str:
+    """The variant the dispatcher picks (host-only)."""
+    buf = ctypes.create_string_buffer(256)
+    _check(_lib.tc_gemm_plan(ctypes.byref(d), _addr(A), _addr(B), _addr(C), num_sms, buf, 256),
+           "tc_gemm_plan")
+    return buf.value.decode()
+
+
+def tc_last_kernel(ctx: Context) -> str:
+    return ctx.last_kernel
+
+
+def tc_launch_count(ctx: Context) -> int:
+    return ctx.launch_count
+
+
+def tc_status_string(status: int) -> str:
+    return _lib.tc_status_string(status).decode()
+
+
+# ------------------------------------------------------------------ tensor API
+
+@dataclass
+class _Shapes:
+    M: int
+    N: int
+    K: int
+
+
+def gemm(ctx: Context, A, B, C, *, transpose_a=False, transpose_b=False, alpha=1.0, beta=0.0,
+         stream: Stream | None = None):
+    """C = alpha*op(A)@op(B) + beta*C on torch CUDA tensors (2-D, row-major,
+    unit column stride; row strides become leading dimensions)."""
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be 2-D with unit column stride")
+    M = A.shape[1] if transpose_a else A.shape[0]
+    K = A.shape[0] if transpose_a else A.shape[1]
+    N = B.shape[0] if transpose_b else B.shape[1]
+    d = tc_gemm_desc(M, N, K, _torch_dtype_code(A), _torch_dtype_code(B), _torch_dtype_code(C), TC_F32,
+                     bool(transpose_a), bool(transpose_b), float(alpha), float(beta),
+                     A.stride(0), B.stride(0), C.stride(0))
+    if stream is None:
+        tc_gemm(ctx, d, A, B, C)
+    else:
+        tc_gemm_async(ctx, d, A, B, C, stream)
+    return C

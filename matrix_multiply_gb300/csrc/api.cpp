@@ -1,0 +1,716 @@
+// The C ABI of tcgemm: validation, normalisation, dispatch and launch.
+//
+// Call path of every GEMM (tessl architecture.md, "GEMM Pipeline & Kernel
+// Selection" and "The Kernel Library and the nn Boundary"):
+//   validate (checked sizes, dims, dtypes, leading dims, finite scalars,
+//   overlap) -> normalise ld = 0 to contiguous (tensorcore gemm.md,
+//   "Surface") -> plan (variant, tile, split, grid) -> repack operands TMA
+//   cannot read -> encode TMA descriptors -> launch -> record the variant
+//   (tensorcore gemm.md, "Fallback ladder": tc_last_backend).
+// Nothing is enqueued unless every check passed.
+#include "../../include/tcgemm.h"
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+using namespace tc;
+
+struct tc_stream {
+    tc_ctx *ctx = nullptr;
+    cudaStream_t st = nullptr;
+    bool owned = false;
+    void *ws = nullptr;              // repacked operands + split-K partials
+    size_t ws_cap = 0;
+    unsigned *tickets = nullptr;     // split-K arrival counters, kept at zero
+    size_t tickets_cap = 0;
+    unsigned *status_host = nullptr; // mapped, pinned: kernels report timeouts here
+    unsigned *status_dev = nullptr;
+};
+
+struct tc_ctx {
+    int device = 0;
+    int num_sms = 0;
+    tc_stream *def = nullptr;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::string last = "none";
+    uint64_t launches = 0;
+    void *dbuf[3] = {nullptr, nullptr, nullptr};  // device copies for tc_gemm_host
+    size_t dcap[3] = {0, 0, 0};
+    std::mutex mu;
+};
+
+namespace {
+
+size_t elem_size(tc_dtype_t t) { return t == TC_F32 ? 4 : 2; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_add_overflow(a, b, out); }
+
+// A problem after validation: normalised leading dimensions and extents.
+struct Norm {
+    int64_t lda, ldb, ldc;
+    int64_t a_rows, a_cols, b_rows, b_cols;   // stored shapes
+    int64_t batch, sa, sb, sc;                // batch and element strides
+    int64_t a_bytes, b_bytes, c_bytes;        // byte extents touched (all batch entries)
+};
+
+// Extent in elements of a stored rows x cols matrix with leading dim ld,
+// repeated `batch` times at `stride`.
+bool extent(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_t stride, int64_t esz,
+            int64_t *bytes)
+{
+    int64_t e, t;
+    if (!mul_ok(rows - 1, ld, &e) || !add_ok(e, cols, &e)) return false;
+    if (batch > 1) {
+        if (!mul_ok(batch - 1, stride, &t) || !add_ok(e, t, &e)) return false;
+    }
+    return mul_ok(e, esz, bytes);
+}
+
+bool ranges_overlap(const void *p, int64_t pb, const void *q, int64_t qb)
+{
+    const uintptr_t a0 = (uintptr_t)p, a1 = a0 + (uintptr_t)pb;
+    const uintptr_t b0 = (uintptr_t)q, b1 = b0 + (uintptr_t)qb;
+    return a0 < b1 && b0 < a1;
+}
+
+tc_status_t validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C, int64_t batch,
+                     int64_t sa, int64_t sb, int64_t sc, Norm *n)
+{
+    if (!d || !A || !B || !C) return TC_ERR_NULL;
+    if (d->M < 1 || d->N < 1 || d->K < 1 || batch < 1) return TC_ERR_DIM;
+    const bool ab_ok = d->a_dtype == TC_F16 || d->a_dtype == TC_BF16 || d->a_dtype == TC_F32;
+    if (!ab_ok || d->b_dtype != d->a_dtype || d->accum_dtype != TC_F32 ||
+        (d->c_dtype != d->a_dtype && d->c_dtype != TC_F32))
+        return TC_ERR_DTYPE;
+    if (d->lda < 0 || d->ldb < 0 || d->ldc < 0) return TC_ERR_LD;
+    if (sa < 0 || sb < 0 || sc < 0) return TC_ERR_STRIDE;
+
+    Norm r;
+    r.a_rows = d->transpose_a ? d->K : d->M;
+    r.a_cols = d->transpose_a ? d->M : d->K;
+    r.b_rows = d->transpose_b ? d->N : d->K;
+    r.b_cols = d->transpose_b ? d->K : d->N;
+    r.lda = d->lda ? d->lda : r.a_cols;
+    r.ldb = d->ldb ? d->ldb : r.b_cols;
+    r.ldc = d->ldc ? d->ldc : d->N;
+    if (r.lda < r.a_cols || r.ldb < r.b_cols || r.ldc < d->N) return TC_ERR_LD;
+    r.batch = batch;
+    r.sa = sa;
+    r.sb = sb;
+    r.sc = sc;
+    const int64_t ea = (int64_t)elem_size(d->a_dtype), ec = (int64_t)elem_size(d->c_dtype);
+    if (!extent(r.a_rows, r.a_cols, r.lda, batch, sa, ea, &r.a_bytes) ||
+        !extent(r.b_rows, r.b_cols, r.ldb, batch, sb, ea, &r.b_bytes) ||
+        !extent(d->M, d->N, r.ldc, batch, sc, ec, &r.c_bytes))
+        return TC_ERR_OVERFLOW;
+    if (batch > 1) {
+        // distinct batch entries must not write the same C elements
+        int64_t c_one;
+        if (!extent(d->M, d->N, r.ldc, 1, 0, 1, &c_one)) return TC_ERR_OVERFLOW;
+        if (sc < c_one) return TC_ERR_STRIDE;
+    }
+    if (!std::isfinite(d->alpha) || !std::isfinite(d->beta)) return TC_ERR_SCALAR;
+    if (ranges_overlap(C, r.c_bytes, A, r.a_bytes) || ranges_overlap(C, r.c_bytes, B, r.b_bytes))
+        return TC_ERR_OVERLAP;
+    *n = r;
+    return TC_OK;
+}
+
+// --------------------------------------------------------------- dispatch
+
+struct Plan {
+    bool ffma = false;
+    int ffma_tile = FFMA_SMALL;
+    int bn = 256, split = 1, grid = 1, group_m = 8;
+    bool pack_a = false, pack_b = false;
+    int64_t tiles = 0, units = 0;
+    std::string name;
+};
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Environment override for tests and sweeps: TC_FORCE_VARIANT holds
+// space/comma separated tokens: bn=<64|128|192|256> split=<S> grid=<G>
+// group_m=<G> ffma=<small|large> pack=<1>.
+struct Force {
+    int bn = 0, split = 0, grid = 0, group_m = 0, ffma = -1, pack = 0;
+};
+
+Force read_force()
+{
+    Force f;
+    const char *e = std::getenv("TC_FORCE_VARIANT");
+    if (!e) return f;
+    std::string s(e);
+    for (auto &ch : s)
+        if (ch == ',') ch = ' ';
+    size_t pos = 0;
+    while (pos < s.size()) {
+        size_t end = s.find(' ', pos);
+        if (end == std::string::npos) end = s.size();
+        std::string tok = s.substr(pos, end - pos);
+        pos = end + 1;
+        const size_t eq = tok.find('=');
+        if (eq == std::string::npos) continue;
+        const std::string k = tok.substr(0, eq), v = tok.substr(eq + 1);
+        if (k == "bn") f.bn = std::atoi(v.c_str());
+        else if (k == "split") f.split = std::atoi(v.c_str());
+        else if (k == "grid") f.grid = std::atoi(v.c_str());
+        else if (k == "group_m") f.group_m = std::atoi(v.c_str());
+        else if (k == "ffma") f.ffma = (v == "large") ? FFMA_LARGE : FFMA_SMALL;
+        else if (k == "pack") f.pack = std::atoi(v.c_str());
+    }
+    return f;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Relative per-tile throughput of the tensor-core main loop by tile width:
+// narrower tiles read more shared memory per MMA flop.
+double bn_rate(int bn) { return bn == 256 ? 1.0 : bn == 192 ? 0.97 : bn == 128 ? 0.90 : 0.70; }
+
+tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const void *B, int num_sms,
+                      Plan *out)
+{
+    Plan p;
+    const Force f = read_force();
+    if (num_sms < 1) num_sms = 1;
+    const char *lay = d->transpose_a ? (d->transpose_b ? "tt" : "tn") : (d->transpose_b ? "nt" : "nn");
+    const char *dt = d->a_dtype == TC_F32 ? "f32" : d->a_dtype == TC_BF16 ? "bf16" : "f16";
+    const char *ct = d->c_dtype == TC_F32 ? "f32" : d->c_dtype == TC_BF16 ? "bf16" : "f16";
+    char buf[160];
+
+    if (d->a_dtype == TC_F32) {
+        // fp32-exact path on CUDA cores
+        p.ffma = true;
+        const int64_t big_tiles = cdiv(d->M, 128) * cdiv(d->N, 128) * n.batch;
+        p.ffma_tile = (big_tiles >= num_sms) ? FFMA_LARGE : FFMA_SMALL;
+        if (f.ffma >= 0) p.ffma_tile = f.ffma;
+        std::snprintf(buf, sizeof buf, "ffma_f32_%s_%s", lay, p.ffma_tile == FFMA_LARGE ? "128x128" : "32x32");
+        p.name = buf;
+        *out = p;
+        return TC_OK;
+    }
+
+    // TMA reads an operand in place only with a 16-byte aligned base and
+    // 16-byte multiple row (and batch) strides; otherwise it is repacked.
+    const bool a3 = n.batch > 1 && n.sa != 0, b3 = n.batch > 1 && n.sb != 0;
+    p.pack_a = !aligned16(A) || (n.lda % 8) != 0 || (a3 && (n.sa % 8) != 0);
+    p.pack_b = !aligned16(B) || (n.ldb % 8) != 0 || (b3 && (n.sb % 8) != 0);
+    if (f.pack) p.pack_a = p.pack_b = true;
+
+    const int64_t num_kb = cdiv(d->K, BK);
+    const int64_t tm = cdiv(d->M, BM);
+
+    // Split-K: too few output tiles to occupy the SMs and a long K loop.
+    const int64_t tiles128 = tm * cdiv(d->N, 128) * n.batch;
+    int bn = 0, split = 1;
+    if (tiles128 * 2 <= num_sms && num_kb >= 16) {
+        bn = 128;
+        split = (int)std::min<int64_t>(num_sms / tiles128, num_kb / 4);
+        if (split < 2) split = 1;
+    } else {
+        // pick the tile width that minimises (tiles per CTA) x (time per tile)
+        double best = 1e300;
+        for (int cand : {256, 192, 128}) {
+            const int64_t tiles = tm * cdiv(d->N, cand) * n.batch;
+            const int64_t per_cta = cdiv(tiles, num_sms);
+            const double t = (double)per_cta * cand / bn_rate(cand);
+            if (t < best - 1e-9) {
+                best = t;
+                bn = cand;
+            }
+        }
+    }
+    if (f.bn == 64 || f.bn == 128 || f.bn == 192 || f.bn == 256) bn = f.bn;
+    if (f.split > 0) split = (int)std::min<int64_t>(f.split, num_kb);
+    p.bn = bn;
+    p.split = split;
+    p.tiles = tm * cdiv(d->N, bn) * n.batch;
+    p.units = p.tiles * split;
+    if (p.units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
+    p.grid = (int)std::min<int64_t>(p.units, num_sms);
+    if (f.grid > 0) p.grid = (int)std::min<int64_t>(f.grid, p.units);
+    p.group_m = f.group_m > 0 ? f.group_m : 8;
+    std::snprintf(buf, sizeof buf, "tcgen05_%s_%s_%s_128x%d%s%s%s", lay, dt, ct, bn,
+                  split > 1 ? "_splitk" : "", p.pack_a ? "_packA" : "", p.pack_b ? "_packB" : "");
+    p.name = buf;
+    if (split > 1) {
+        std::snprintf(buf, sizeof buf, "_s%d", split);
+        p.name += buf;
+    }
+    *out = p;
+    return TC_OK;
+}
+
+// --------------------------------------------------------------- resources
+
+tc_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? TC_OK : TC_ERR_CUDA; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+tc_status_t ensure_ws(tc_stream *s, size_t bytes)
+{
+    if (bytes <= s->ws_cap) return TC_OK;
+    size_t cap = round_up(bytes + bytes / 4, (size_t)1 << 20);
+    if (s->ws) {
+        cudaError_t e = cudaFreeAsync(s->ws, s->st);
+        s->ws = nullptr;
+        s->ws_cap = 0;
+        if (e != cudaSuccess) return TC_ERR_CUDA;
+    }
+    if (cudaMallocAsync(&s->ws, cap, s->st) != cudaSuccess) {
+        s->ws = nullptr;
+        return TC_ERR_CUDA;
+    }
+    s->ws_cap = cap;
+    return TC_OK;
+}
+
+tc_status_t ensure_tickets(tc_stream *s, size_t count)
+{
+    if (count <= s->tickets_cap) return TC_OK;
+    size_t cap = round_up(count, 4096);
+    if (s->tickets) {
+        if (cudaFreeAsync(s->tickets, s->st) != cudaSuccess) return TC_ERR_CUDA;
+        s->tickets = nullptr;
+        s->tickets_cap = 0;
+    }
+    if (cudaMallocAsync(reinterpret_cast<void **>(&s->tickets), cap * sizeof(unsigned), s->st) != cudaSuccess) {
+        s->tickets = nullptr;
+        return TC_ERR_CUDA;
+    }
+    if (cudaMemsetAsync(s->tickets, 0, cap * sizeof(unsigned), s->st) != cudaSuccess) return TC_ERR_CUDA;
+    s->tickets_cap = cap;
+    return TC_OK;
+}
+
+bool encode_map(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, int64_t inner, int64_t outer,
+                int64_t ld_elems, bool three_d, int64_t batch, int64_t bstride_elems, uint32_t box_inner,
+                uint32_t box_outer)
+{
+    const CUtensorMapDataType t = dt == TC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)ld_elems * 2, (cuuint64_t)bstride_elems * 2};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = ctx->encode(m, t, three_d ? 3 : 2, const_cast<void *>(base), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+tc_status_t read_status(tc_stream *s)
+{
+    volatile unsigned *st = s->status_host;
+    if (st && *st != 0u) {
+        *st = 0u;
+        return TC_ERR_DEVICE_TIMEOUT;
+    }
+    return TC_OK;
+}
+
+// Enqueue one validated, planned problem on stream s.
+tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Plan &p, const void *A,
+                    const void *B, void *C, tc_stream *s)
+{
+    cudaError_t e;
+    if (p.ffma) {
+        FfmaArgs a{};
+        a.M = d->M;
+        a.N = d->N;
+        a.K = d->K;
+        a.batch = (int)n.batch;
+        a.ta = d->transpose_a;
+        a.tb = d->transpose_b;
+        a.A = static_cast<const float *>(A);
+        a.B = static_cast<const float *>(B);
+        a.C = static_cast<float *>(C);
+        a.lda = n.lda;
+        a.ldb = n.ldb;
+        a.ldc = n.ldc;
+        a.stride_a = n.sa;
+        a.stride_b = n.sb;
+        a.stride_c = n.sc;
+        a.alpha = d->alpha;
+        a.beta = d->beta;
+        e = launch_ffma(a, p.ffma_tile, s->st);
+        if (e != cudaSuccess) return TC_ERR_CUDA;
+        ctx->launches += 1;
+        ctx->last = p.name;
+        return TC_OK;
+    }
+
+    // ---- workspace: [packed A | packed B | split-K partials]
+    const int64_t a_batch = (n.batch > 1 && n.sa != 0) ? n.batch : 1;
+    const int64_t b_batch = (n.batch > 1 && n.sb != 0) ? n.batch : 1;
+    const int64_t lda_p = p.pack_a ? (int64_t)round_up((size_t)n.a_cols, 8) : n.lda;
+    const int64_t ldb_p = p.pack_b ? (int64_t)round_up((size_t)n.b_cols, 8) : n.ldb;
+    const size_t a_pack_bytes = p.pack_a ? round_up((size_t)(n.a_rows * lda_p * a_batch * 2), 256) : 0;
+    const size_t b_pack_bytes = p.pack_b ? round_up((size_t)(n.b_rows * ldb_p * b_batch * 2), 256) : 0;
+    const size_t part_bytes = p.split > 1 ? (size_t)p.units * BM * p.bn * sizeof(float) : 0;
+    tc_status_t st = ensure_ws(s, a_pack_bytes + b_pack_bytes + part_bytes + 256);
+    if (st != TC_OK) return st;
+    if (p.split > 1 && (st = ensure_tickets(s, (size_t)p.tiles * 4)) != TC_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(s->ws);
+    const void *Ause = A, *Buse = B;
+    int64_t sa = n.sa, sb = n.sb;
+    uint64_t launches = 0;
+    if (p.pack_a) {
+        PackArgs pk{static_cast<const uint16_t *>(A), reinterpret_cast<uint16_t *>(ws), n.a_rows, n.a_cols,
+                    n.lda, lda_p, a_batch > 1 ? n.sa : 0, n.a_rows * lda_p, (int)a_batch};
+        if ((e = launch_pack(pk, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        Ause = ws;
+        sa = a_batch > 1 ? n.a_rows * lda_p : 0;
+        ++launches;
+    }
+    if (p.pack_b) {
+        uint8_t *dst = ws + a_pack_bytes;
+        PackArgs pk{static_cast<const uint16_t *>(B), reinterpret_cast<uint16_t *>(dst), n.b_rows, n.b_cols,
+                    n.ldb, ldb_p, b_batch > 1 ? n.sb : 0, n.b_rows * ldb_p, (int)b_batch};
+        if ((e = launch_pack(pk, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        Buse = dst;
+        sb = b_batch > 1 ? n.b_rows * ldb_p : 0;
+        ++launches;
+    }
+
+    MmaLaunch L{};
+    L.bn = p.bn;
+    L.grid = p.grid;
+    MmaArgs &a = L.args;
+    a.M = d->M;
+    a.N = d->N;
+    a.K = d->K;
+    a.num_kb = (int)cdiv(d->K, BK);
+    a.tiles_m = (int)cdiv(d->M, BM);
+    a.tiles_n = (int)cdiv(d->N, p.bn);
+    a.tiles_per_batch = a.tiles_m * a.tiles_n;
+    a.batch = (int)n.batch;
+    a.split_k = p.split;
+    a.total_units = (int)p.units;
+    a.group_m = p.group_m;
+    a.a_kmajor = !d->transpose_a;
+    a.b_kmajor = d->transpose_b;
+    a.a_3d = a_batch > 1;
+    a.b_3d = b_batch > 1;
+    // instruction descriptor (kind::f16): D f32 (bit 4), A/B format
+    // (bits 7-9 / 10-12: 0 = f16, 1 = bf16), A/B MN-major (bits 15 / 16),
+    // N >> 3 (bits 17-22), M >> 4 (bits 24-28)
+    const uint32_t fmt = d->a_dtype == TC_BF16 ? 1u : 0u;
+    a.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(!a.a_kmajor) << 15) |
+              ((uint32_t)(!a.b_kmajor) << 16) | ((uint32_t)(p.bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    a.alpha = d->alpha;
+    a.beta = d->beta;
+    a.C = C;
+    a.ldc = n.ldc;
+    a.stride_c = n.batch > 1 ? n.sc : 0;
+    a.c_dtype = d->c_dtype;
+    const int64_t ec = (int64_t)elem_size(d->c_dtype);
+    a.c_vec_ok = aligned16(C) && (n.ldc * ec) % 16 == 0 && (a.stride_c * ec) % 16 == 0;
+    a.ws = p.split > 1 ? reinterpret_cast<float *>(ws + a_pack_bytes + b_pack_bytes) : nullptr;
+    a.tickets = p.split > 1 ? s->tickets : nullptr;
+    a.status = s->status_dev;
+    const int64_t kb_per_unit = cdiv(a.num_kb, p.split);
+    a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
+
+    const int64_t lda_use = p.pack_a ? lda_p : n.lda;
+    const int64_t ldb_use = p.pack_b ? ldb_p : n.ldb;
+    bool ok;
+    if (a.a_kmajor)
+        ok = encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->K, d->M, lda_use, a.a_3d, n.batch, sa, 64, BM);
+    else
+        ok = encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->M, d->K, lda_use, a.a_3d, n.batch, sa, 64, 64);
+    if (ok) {
+        if (a.b_kmajor)
+            ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->K, d->N, ldb_use, a.b_3d, n.batch, sb, 64,
+                            (uint32_t)p.bn);
+        else
+            ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, a.b_3d, n.batch, sb, 64, 64);
+    }
+    if (!ok) return TC_ERR_CUDA;
+    if ((e = launch_mma(L, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+    ++launches;
+    ctx->launches += launches;
+    ctx->last = p.name;
+    return TC_OK;
+}
+
+tc_status_t run(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B, void *C, int64_t batch,
+                int64_t sa, int64_t sb, int64_t sc, tc_stream *s)
+{
+    if (!ctx || !s) return TC_ERR_NULL;
+    Norm n;
+    tc_status_t st = validate(d, A, B, C, batch, sa, sb, sc, &n);
+    if (st != TC_OK) return st;
+    Plan p;
+    if ((st = make_plan(d, n, A, B, ctx->num_sms, &p)) != TC_OK) return st;
+    std::lock_guard<std::mutex> g(ctx->mu);
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    return enqueue(ctx, d, n, p, A, B, C, s);
+}
+
+tc_status_t stream_init(tc_ctx *ctx, tc_stream *s)
+{
+    s->ctx = ctx;
+    if (cudaHostAlloc(reinterpret_cast<void **>(&s->status_host), sizeof(unsigned), cudaHostAllocMapped) !=
+        cudaSuccess)
+        return TC_ERR_CUDA;
+    *s->status_host = 0u;
+    if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&s->status_dev), s->status_host, 0) != cudaSuccess)
+        return TC_ERR_CUDA;
+    return TC_OK;
+}
+
+void stream_free(tc_stream *s)
+{
+    if (!s) return;
+    if (s->st) cudaStreamSynchronize(s->st);
+    if (s->ws) cudaFree(s->ws);
+    if (s->tickets) cudaFree(s->tickets);
+    if (s->status_host) cudaFreeHost(s->status_host);
+    if (s->owned && s->st) cudaStreamDestroy(s->st);
+    delete s;
+}
+
+}  // namespace
+
+// =============================================================== C ABI
+
+extern "C" {
+
+const char *tc_status_string(tc_status_t st)
+{
+    switch (st) {
+    case TC_OK: return "ok";
+    case TC_ERR_NULL: return "null pointer";
+    case TC_ERR_DIM: return "dimension out of range (M, N, K, batch must be >= 1)";
+    case TC_ERR_LD: return "leading dimension below its minimum or negative";
+    case TC_ERR_DTYPE: return "unsupported dtype combination";
+    case TC_ERR_SCALAR: return "alpha or beta is not finite";
+    case TC_ERR_OVERLAP: return "C overlaps A or B";
+    case TC_ERR_OVERFLOW: return "size computation overflows";
+    case TC_ERR_ALIGN_UNSUPPORTED: return "alignment unsupported";
+    case TC_ERR_CUDA: return "CUDA error";
+    case TC_ERR_DEVICE_TIMEOUT: return "device wait timed out; the kernel stopped early";
+    case TC_ERR_STRIDE: return "invalid batch stride";
+    case TC_ERR_VARIANT: return "forced variant cannot serve this problem";
+    }
+    return "unknown status";
+}
+
+tc_status_t tc_ctx_create(tc_ctx **out, int device)
+{
+    if (!out) return TC_ERR_NULL;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+        cudaGetLastError();
+        return TC_ERR_CUDA;
+    }
+    if (cudaSetDevice(device) != cudaSuccess) return TC_ERR_CUDA;
+    tc_ctx *ctx = new tc_ctx();
+    ctx->device = device;
+    if (cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        delete ctx;
+        return TC_ERR_CUDA;
+    }
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        delete ctx;
+        return TC_ERR_CUDA;
+    }
+    ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    tc_stream *s = new tc_stream();
+    tc_status_t st = stream_init(ctx, s);
+    if (st == TC_OK && cudaStreamCreateWithFlags(&s->st, cudaStreamNonBlocking) != cudaSuccess) st = TC_ERR_CUDA;
+    if (st != TC_OK) {
+        stream_free(s);
+        delete ctx;
+        return st;
+    }
+    s->owned = true;
+    ctx->def = s;
+    *out = ctx;
+    return TC_OK;
+}
+
+void tc_ctx_destroy(tc_ctx *ctx)
+{
+    if (!ctx) return;
+    cudaSetDevice(ctx->device);
+    stream_free(ctx->def);
+    for (int i = 0; i < 3; ++i)
+        if (ctx->dbuf[i]) cudaFree(ctx->dbuf[i]);
+    delete ctx;
+}
+
+tc_status_t tc_stream_create(tc_ctx *ctx, tc_stream **out)
+{
+    if (!ctx || !out) return TC_ERR_NULL;
+    *out = nullptr;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    tc_stream *s = new tc_stream();
+    tc_status_t st = stream_init(ctx, s);
+    if (st == TC_OK && cudaStreamCreateWithFlags(&s->st, cudaStreamNonBlocking) != cudaSuccess) st = TC_ERR_CUDA;
+    if (st != TC_OK) {
+        stream_free(s);
+        return st;
+    }
+    s->owned = true;
+    *out = s;
+    return TC_OK;
+}
+
+tc_status_t tc_stream_wrap(tc_ctx *ctx, void *cuda_stream, tc_stream **out)
+{
+    if (!ctx || !out) return TC_ERR_NULL;
+    *out = nullptr;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    tc_stream *s = new tc_stream();
+    tc_status_t st = stream_init(ctx, s);
+    if (st != TC_OK) {
+        stream_free(s);
+        return st;
+    }
+    s->st = static_cast<cudaStream_t>(cuda_stream);
+    s->owned = false;
+    *out = s;
+    return TC_OK;
+}
+
+tc_status_t tc_stream_sync(tc_stream *s)
+{
+    if (!s) return TC_ERR_NULL;
+    if (cudaStreamSynchronize(s->st) != cudaSuccess) return TC_ERR_CUDA;
+    return read_status(s);
+}
+
+void *tc_stream_handle(tc_stream *s) { return s ? static_cast<void *>(s->st) : nullptr; }
+
+void tc_stream_destroy(tc_stream *s) { stream_free(s); }
+
+tc_status_t tc_gemm_async(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B, void *C,
+                          tc_stream *s)
+{
+    return run(ctx, d, A, B, C, 1, 0, 0, 0, s);
+}
+
+tc_status_t tc_gemm(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B, void *C)
+{
+    if (!ctx) return TC_ERR_NULL;
+    tc_status_t st = run(ctx, d, A, B, C, 1, 0, 0, 0, ctx->def);
+    if (st != TC_OK) return st;
+    return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_batched_async(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A, const void *B,
+                                  void *C, tc_stream *s)
+{
+    if (!bd) return TC_ERR_NULL;
+    return run(ctx, &bd->base, A, B, C, bd->batch, bd->stride_a, bd->stride_b, bd->stride_c, s);
+}
+
+tc_status_t tc_gemm_batched(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A, const void *B, void *C)
+{
+    if (!ctx) return TC_ERR_NULL;
+    tc_status_t st = tc_gemm_batched_async(ctx, bd, A, B, C, ctx->def);
+    if (st != TC_OK) return st;
+    return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d, const void *const *A,
+                                  const void *const *B, void *const *C, tc_stream *s)
+{
+    if (!ctx || !s || !d || !A || !B || !C) return TC_ERR_NULL;
+    if (n < 0) return TC_ERR_DIM;
+    // validate everything before enqueueing anything
+    for (int i = 0; i < n; ++i) {
+        Norm nn;
+        tc_status_t st = validate(&d[i], A[i], B[i], C[i], 1, 0, 0, 0, &nn);
+        if (st != TC_OK) return st;
+    }
+    for (int i = 0; i < n; ++i) {
+        tc_status_t st = run(ctx, &d[i], A[i], B[i], C[i], 1, 0, 0, 0, s);
+        if (st != TC_OK) return st;
+    }
+    return TC_OK;
+}
+
+tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host, const void *B_host, void *C_host)
+{
+    if (!ctx) return TC_ERR_NULL;
+    Norm n;
+    // validate on the host buffers (overlap between host ranges, dims, ...)
+    tc_status_t st = validate(d, A_host, B_host, C_host, 1, 0, 0, 0, &n);
+    if (st != TC_OK) return st;
+    const size_t bytes[3] = {(size_t)n.a_bytes, (size_t)n.b_bytes, (size_t)n.c_bytes};
+    {
+        std::lock_guard<std::mutex> g(ctx->mu);
+        if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+        for (int i = 0; i < 3; ++i) {
+            if (bytes[i] > ctx->dcap[i]) {
+                if (ctx->dbuf[i]) cudaFree(ctx->dbuf[i]);
+                ctx->dbuf[i] = nullptr;
+                ctx->dcap[i] = 0;
+                if (cudaMalloc(&ctx->dbuf[i], bytes[i]) != cudaSuccess) return TC_ERR_CUDA;
+                ctx->dcap[i] = bytes[i];
+            }
+        }
+    }
+    cudaStream_t st0 = ctx->def->st;
+    if (cudaMemcpyAsync(ctx->dbuf[0], A_host, bytes[0], cudaMemcpyHostToDevice, st0) != cudaSuccess ||
+        cudaMemcpyAsync(ctx->dbuf[1], B_host, bytes[1], cudaMemcpyHostToDevice, st0) != cudaSuccess)
+        return TC_ERR_CUDA;
+    if (d->beta != 0.0f &&
+        cudaMemcpyAsync(ctx->dbuf[2], C_host, bytes[2], cudaMemcpyHostToDevice, st0) != cudaSuccess)
+        return TC_ERR_CUDA;
+    st = run(ctx, d, ctx->dbuf[0], ctx->dbuf[1], ctx->dbuf[2], 1, 0, 0, 0, ctx->def);
+    if (st != TC_OK) return st;
+    if (cudaMemcpyAsync(C_host, ctx->dbuf[2], bytes[2], cudaMemcpyDeviceToHost, st0) != cudaSuccess)
+        return TC_ERR_CUDA;
+    return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C)
+{
+    Norm n;
+    return validate(d, A, B, C, 1, 0, 0, 0, &n);
+}
+
+tc_status_t tc_gemm_batched_validate(const tc_gemm_batched_desc *bd, const void *A, const void *B, const void *C)
+{
+    if (!bd) return TC_ERR_NULL;
+    Norm n;
+    return validate(&bd->base, A, B, C, bd->batch, bd->stride_a, bd->stride_b, bd->stride_c, &n);
+}
+
+tc_status_t tc_gemm_plan(const tc_gemm_desc *d, const void *A, const void *B, const void *C, int num_sms, char *buf,
+                         size_t len)
+{
+    if (!buf || len == 0) return TC_ERR_NULL;
+    buf[0] = '\0';
+    Norm n;
+    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n);
+    if (st != TC_OK) return st;
+    Plan p;
+    if ((st = make_plan(d, n, A, B, num_sms, &p)) != TC_OK) return st;
+    std::snprintf(buf, len, "%s", p.name.c_str());
+    return TC_OK;
+}
+
+const char *tc_last_kernel(tc_ctx *ctx) { return ctx ? ctx->last.c_str() : ""; }
+
+uint64_t tc_launch_count(tc_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+// fp32-exact GEMM on the FFMA CUDA cores (no TF32, no tensor cores).
+//
+// The tessl architecture.md "GEMM Pipeline & Kernel Selection" chart routes
+// "f32 exact" NN work to its own small-tile kernel, and the phobos matmul
+// page's "sgemm" kernel is the fp32 loop with the alpha/beta epilogue.  Here
+// every output element is one fused multiply-add chain over k in ascending
+// order, acc = fma(a_ik, b_kj, acc), followed by alpha*acc + beta*C_old:
+// deterministic and never reassociated.
+//
+// Tiles are staged through shared memory (A transposed to [k][m], B as
+// [k][n]) with register double buffering of the next K block; each thread
+// owns a TM x TN register block with a strided row/column assignment so
+// shared-memory reads are conflict-free.  Every layout (NN/TN/NT/TT), any
+// leading dimension and ragged edges go through bounds-checked loads.
+#include "internal.h"
+
+namespace tc {
+namespace {
+
+template <int BM, int BN, int BK, int TM, int TN>
+__global__ void __launch_bounds__(256) ffma_kernel(const FfmaArgs a)
+{
+    static_assert((BM / TM) * (BN / TN) == 256, "256 threads");
+    static_assert((BM * BK) % 256 == 0 && (BN * BK) % 256 == 0, "tile loads");
+    constexpr int LA = BM * BK / 256;   // A elements loaded per thread per K block
+    constexpr int LB = BN * BK / 256;
+    __shared__ float As[2][BK][BM + 4];
+    __shared__ float Bs[2][BK][BN + 4];
+
+    const int tid = threadIdx.x;
+    const int tx = tid % (BN / TN);     // column group
+    const int ty = tid / (BN / TN);     // row group
+    const long long n0 = (long long)blockIdx.x * BN;
+    const long long tiles_m = ((long long)a.M + BM - 1) / BM;
+
+    for (int b = blockIdx.z; b < a.batch; b += gridDim.z)
+    for (long long mt = blockIdx.y; mt < tiles_m; mt += gridDim.y) {
+        const long long m0 = mt * BM;
+        const float *A = a.A + (long long)b * a.stride_a;
+        const float *B = a.B + (long long)b * a.stride_b;
+        float *C = a.C + (long long)b * a.stride_c;
+
+        // element e of the A tile: (m, k).  Consecutive threads walk the
+        // stored-contiguous dimension so global loads coalesce.
+        auto a_coord = [&](int e, int &m, int &k) {
+            if (a.ta) { m = e % BM; k = e / BM; }      // stored [K,M]: m contiguous
+            else      { k = e % BK; m = e / BK; }      // stored [M,K]: k contiguous
+        };
+        auto b_coord = [&](int e, int &k, int &n) {
+            if (a.tb) { k = e % BK; n = e / BK; }      // stored [N,K]: k contiguous
+            else      { n = e % BN; k = e / BN; }      // stored [K,N]: n contiguous
+        };
+        auto load_a = [&](long long kb, float (&ra)[LA]) {
+#pragma unroll
+            for (int i = 0; i < LA; ++i) {
+                int m, k;
+                a_coord(tid + i * 256, m, k);
+                const long long gm = m0 + m, gk = kb + k;
+                ra[i] = (gm < a.M && gk < a.K)
+                            ? (a.ta ? A[gk * a.lda + gm] : A[gm * a.lda + gk])
+                            : 0.0f;
+            }
+        };
+        auto load_b = [&](long long kb, float (&rb)[LB]) {
+#pragma unroll
+            for (int i = 0; i < LB; ++i) {
+                int k, n;
+                b_coord(tid + i * 256, k, n);
+                const long long gk = kb + k, gn = n0 + n;
+                rb[i] = (gk < a.K && gn < a.N)
+                            ? (a.tb ? B[gn * a.ldb + gk] : B[gk * a.ldb + gn])
+                            : 0.0f;
+            }
+        };
+        auto store_tiles = [&](int buf, const float (&ra)[LA], const float (&rb)[LB]) {
+#pragma unroll
+            for (int i = 0; i < LA; ++i) {
+                int m, k;
+                a_coord(tid + i * 256, m, k);
+                As[buf][k][m] = ra[i];
+            }
+#pragma unroll
+            for (int i = 0; i < LB; ++i) {
+                int k, n;
+                b_coord(tid + i * 256, k, n);
+                Bs[buf][k][n] = rb[i];
+            }
+        };
+
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+        float ra[LA], rb[LB];
+        load_a(0, ra);
+        load_b(0, rb);
+        store_tiles(0, ra, rb);
+        __syncthreads();
+
+        int buf = 0;
+        for (long long kb = 0; kb < a.K; kb += BK) {
+            const bool more = kb + BK < a.K;
+            if (more) {
+                load_a(kb + BK, ra);
+                load_b(kb + BK, rb);
+            }
+            const int kend = (int)min((long long)BK, a.K - kb);   // zero-padded beyond K, but stop the chain at K
+            for (int kk = 0; kk < kend; ++kk) {
+                float av[TM], bv[TN];
+#pragma unroll
+                for (int i = 0; i < TM; ++i) av[i] = As[buf][kk][ty + i * (BM / TM)];
+#pragma unroll
+                for (int j = 0; j < TN; ++j) bv[j] = Bs[buf][kk][tx + j * (BN / TN)];
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            }
+            if (more) {
+                store_tiles(buf ^ 1, ra, rb);
+                __syncthreads();
+                buf ^= 1;
+            }
+        }
+
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const long long gm = m0 + ty + i * (BM / TM);
+            if (gm >= a.M) continue;
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const long long gn = n0 + tx + j * (BN / TN);
+                if (gn >= a.N) continue;
+                float *c = C + gm * a.ldc + gn;
+                const float r = a.alpha * acc[i][j];
+                *c = (a.beta != 0.0f) ? fmaf(a.beta, *c, r) : r;
+            }
+        }
+        __syncthreads();   // shared tiles are reused by the next tile
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st)
+{
+    const int zb = a.batch < 65535 ? a.batch : 65535;
+    if (tile == FFMA_LARGE) {
+        const long long ty = ((long long)a.M + 127) / 128;
+        dim3 grid((unsigned)(((long long)a.N + 127) / 128), (unsigned)(ty < 65535 ? ty : 65535), zb);
+        ffma_kernel<128, 128, 8, 8, 8><<<grid, 256, 0, st>>>(a);
+    } else {
+        const long long ty = ((long long)a.M + 31) / 32;
+        dim3 grid((unsigned)(((long long)a.N + 31) / 32), (unsigned)(ty < 65535 ? ty : 65535), zb);
+        ffma_kernel<32, 32, 32, 2, 2><<<grid, 256, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tc

@@ -1,0 +1,171 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every
+symbol the header declares, refuses bad descriptors with the right status
+before touching a device, and routes each workload to the intended variant.
+
+Validation order and refusal-without-launch follow the tessl
+architecture.md sections "GEMM Pipeline & Kernel Selection" (validate_gemm)
+and "The Kernel Library and the nn Boundary" (checked multiply, capacity in
+elements, non-zero dims, finite scalars, nothing encoded on error).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+import torch
+
+import matrix_multiply_gb300 as tg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tcgemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tc_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_surface():
+    assert set(declared_functions()) == set(tg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(tg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_ctx_create_without_device_reports_cuda_error():
+    p = ctypes.c_void_p(12345)
+    st = tg.library().tc_ctx_create(ctypes.byref(p), 0)
+    assert st == tg.TC_ERR_CUDA
+    assert p.value is None
+
+
+def test_status_strings():
+    for code in tg.STATUS:
+        assert tg.tc_status_string(code) not in ("", "unknown status")
+    assert tg.tc_status_string(999) == "unknown status"
+
+
+def desc(**kw):
+    base = dict(M=64, N=48, K=32, a_dtype="bf16", c_dtype="bf16")
+    base.update(kw)
+    M, N, K = base.pop("M"), base.pop("N"), base.pop("K")
+    return tg.make_desc(M, N, K, base.pop("a_dtype"), base.pop("c_dtype"), **base)
+
+
+def test_valid_descriptor_passes():
+    assert tg.tc_gemm_validate(desc()) == tg.TC_OK
+    for ta in (False, True):
+        for tb in (False, True):
+            assert tg.tc_gemm_validate(desc(transpose_a=ta, transpose_b=tb)) == tg.TC_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=0), tg.TC_ERR_DIM), (dict(N=-3), tg.TC_ERR_DIM), (dict(K=0), tg.TC_ERR_DIM),
+    (dict(lda=31), tg.TC_ERR_LD), (dict(ldb=47), tg.TC_ERR_LD), (dict(ldc=47), tg.TC_ERR_LD),
+    (dict(lda=-1), tg.TC_ERR_LD),
+    (dict(transpose_a=True, lda=63), tg.TC_ERR_LD),        # A stored [K,M]: lda >= M
+    (dict(transpose_b=True, ldb=31), tg.TC_ERR_LD),        # B stored [N,K]: ldb >= K
+    (dict(alpha=math.inf), tg.TC_ERR_SCALAR), (dict(beta=math.nan), tg.TC_ERR_SCALAR),
+    (dict(c_dtype="f16"), tg.TC_ERR_DTYPE),                # bf16 in, f16 out
+    (dict(a_dtype="f32", c_dtype="bf16"), tg.TC_ERR_DTYPE),
+])
+def test_refusals(kw, status):
+    assert tg.tc_gemm_validate(desc(**kw)) == status
+
+
+def test_dtype_rules():
+    d = desc()
+    d.b_dtype = tg.TC_F16
+    assert tg.tc_gemm_validate(d) == tg.TC_ERR_DTYPE      # A and B must match
+    d = desc()
+    d.accum_dtype = tg.TC_F16
+    assert tg.tc_gemm_validate(d) == tg.TC_ERR_DTYPE      # fp32 accumulation only
+    d = desc()
+    d.a_dtype = d.b_dtype = 7
+    assert tg.tc_gemm_validate(d) == tg.TC_ERR_DTYPE
+    for ab, c in [("f16", "f16"), ("f16", "f32"), ("bf16", "f32"), ("f32", "f32")]:
+        assert tg.tc_gemm_validate(desc(a_dtype=ab, c_dtype=c)) == tg.TC_OK
+
+
+def test_null_pointers():
+    assert tg.tc_gemm_validate(None) == tg.TC_ERR_NULL
+    assert tg.tc_gemm_validate(desc(), A=0) == tg.TC_ERR_NULL
+    assert tg.tc_gemm_validate(desc(), C=0) == tg.TC_ERR_NULL
+
+
+def test_overlap():
+    d = desc(M=64, N=64, K=64)             # A: 64*64*2 = 8192 bytes
+    base = 1 << 30
+    assert tg.tc_gemm_validate(d, A=base, B=base + (1 << 20), C=base + 8192) == tg.TC_OK
+    assert tg.tc_gemm_validate(d, A=base, B=base + (1 << 20), C=base + 8190) == tg.TC_ERR_OVERLAP
+    assert tg.tc_gemm_validate(d, A=base, B=base + (1 << 20), C=base + (1 << 20) - 100) == tg.TC_ERR_OVERLAP
+    assert tg.tc_gemm_validate(d, A=base + (1 << 20), B=base + (2 << 20), C=base) == tg.TC_OK
+
+
+def test_overflow_is_refused():
+    # (rows-1)*ld + cols elements times the element size overflows int64
+    d = desc(M=2**31 - 1, N=2**31 - 1, K=2**31 - 1, a_dtype="f32", c_dtype="f32")
+    d.lda = 2**31 - 1
+    st = tg.tc_gemm_validate(d, A=1 << 12, B=1 << 62, C=(1 << 62) + (1 << 61))
+    assert st in (tg.TC_ERR_OVERFLOW, tg.TC_ERR_OVERLAP)
+    bd = tg.tc_gemm_batched_desc(desc(M=1 << 30, N=1 << 30, K=8), 2**31 - 1, 1 << 60, 0, 1 << 61)
+    assert tg.tc_gemm_batched_validate(bd) == tg.TC_ERR_OVERFLOW
+
+
+def test_batched_strides():
+    d = desc(M=16, N=16, K=16)
+    ok = tg.tc_gemm_batched_desc(d, 4, 256, 256, 256)
+    assert tg.tc_gemm_batched_validate(ok) == tg.TC_OK
+    shared_b = tg.tc_gemm_batched_desc(d, 4, 256, 0, 256)     # one B for every entry
+    assert tg.tc_gemm_batched_validate(shared_b) == tg.TC_OK
+    clash = tg.tc_gemm_batched_desc(d, 4, 256, 256, 100)      # outputs overlap
+    assert tg.tc_gemm_batched_validate(clash) == tg.TC_ERR_STRIDE
+    neg = tg.tc_gemm_batched_desc(d, 4, -256, 256, 256)
+    assert tg.tc_gemm_batched_validate(neg) == tg.TC_ERR_STRIDE
+    zero = tg.tc_gemm_batched_desc(d, 0, 256, 256, 256)
+    assert tg.tc_gemm_batched_validate(zero) == tg.TC_ERR_DIM
+
+
+# ---------------------------------------------------------------- dispatcher
+
+def plan(M, N, K, ab, c, ta=False, tb=False, A=1 << 20, B=1 << 40, C=1 << 41, **kw):
+    return tg.tc_gemm_plan(tg.make_desc(M, N, K, ab, c, transpose_a=ta, transpose_b=tb, **kw),
+                           A=A, B=B, C=C, num_sms=152)
+
+
+def test_plan_fp32_goes_to_ffma():
+    assert plan(256, 256, 256, "f32", "f32").startswith("ffma_f32_nn")
+    assert plan(4096, 4096, 4096, "f32", "f32", tb=True) == "ffma_f32_nt_128x128"
+
+
+def test_plan_tensor_core_shapes():
+    p = plan(4096, 4096, 4096, "bf16", "bf16")
+    assert p.startswith("tcgen05_nn_bf16_bf16_128x") and "split" not in p and "pack" not in p
+    assert plan(4096, 4096, 8192, "bf16", "f32", ta=True).startswith("tcgen05_tn_bf16_f32")
+    assert plan(4096, 4096, 8192, "bf16", "f32", tb=True).startswith("tcgen05_nt_bf16_f32")
+
+
+def test_plan_split_k_for_tall_k():
+    p = plan(256, 256, 16384, "bf16", "f32", ta=True)
+    assert "_splitk" in p and p.startswith("tcgen05_tn_bf16_f32_128x128")
+    s = int(p.rsplit("_s", 1)[1])
+    assert 2 <= s <= 152 // 4
+
+
+def test_plan_narrow_n():
+    assert plan(8192, 384, 4096, "f16", "f16") == "tcgen05_nn_f16_f16_128x192"
+
+
+def test_plan_repacks_unaligned_operands():
+    assert plan(100, 64, 33, "f16", "f16").endswith("_packA")          # lda = 33 elements
+    assert plan(100, 63, 64, "f16", "f16").endswith("_packB")          # ldb = 63
+    assert "pack" not in plan(100, 64, 64, "f16", "f16")
+    assert plan(100, 64, 64, "f16", "f16", A=(1 << 20) + 2).endswith("_packA")   # misaligned base

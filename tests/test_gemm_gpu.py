@@ -1,0 +1,352 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI (GB300).
+
+Every case draws seeded inputs (synthetic.py), runs the library and compares
+each output element (or, at full size, sampled elements plus the ragged
+edges) with the oracle's fp64 value under the bound of tests/parity.py:
+|C - R| <= 1e-4 * sum_k|a b| (+ one output ulp for f16/bf16 output), and
+1e-5 * sum_k|a b| on the fp32-exact path.  Integer-valued inputs are
+compared bitwise.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import matrix_multiply_gb300 as tg
+else:  # collected on CPU only to be deselected
+    tg = None
+
+LAYOUTS = [(False, False), (True, False), (False, True), (True, True)]
+DT_PAIRS = [("bf16", "bf16"), ("bf16", "f32"), ("f16", "f16"), ("f16", "f32")]
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    c = tg.Context(0)
+    yield c
+    c.close()
+
+
+@pytest.fixture
+def force(monkeypatch):
+    def set_(spec):
+        if spec:
+            monkeypatch.setenv("TC_FORCE_VARIANT", spec)
+        else:
+            monkeypatch.delenv("TC_FORCE_VARIANT", raising=False)
+    return set_
+
+
+def run_problem(ctx, p, *, lda=0, ldb=0, ldc=0, stream=None):
+    A, B, C = p.A.cuda(), p.B.cuda(), p.C.cuda()
+    d = tg.make_desc(p.M, p.N, p.K, p.ab_dtype, p.c_dtype, transpose_a=p.transpose_a,
+                     transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta,
+                     lda=lda or A.shape[1], ldb=ldb or B.shape[1], ldc=ldc or C.shape[1])
+    if stream is None:
+        tg.tc_gemm(ctx, d, A, B, C)
+    else:
+        tg.tc_gemm_async(ctx, d, A, B, C, stream)
+        stream.sync()
+    return C.cpu()
+
+
+def check_full(ctx, p, what="", **kw):
+    out = run_problem(ctx, p, **kw)
+    R, T = oracle.gemm(p)
+    got = oracle.decode(out)[:, : p.N]
+    return parity.check(got, R, T, p.c_dtype, exact_f32=(p.ab_dtype == "f32"),
+                        what=f"{what} {ctx.last_kernel}")
+
+
+def check_sampled(ctx, p, n=2000, seed=0, what=""):
+    out = run_problem(ctx, p)
+    rows, cols = parity.sample_points(p.M, p.N, n, np.random.default_rng(seed))
+    R, T = oracle.gemm_points(p, rows, cols)
+    got = oracle.decode(out)[rows, cols]
+    return parity.check(got, R, T, p.c_dtype, exact_f32=(p.ab_dtype == "f32"),
+                        what=f"{what} {ctx.last_kernel}")
+
+
+# ------------------------------------------------------------ small shapes
+
+SHAPES = [(1, 1, 1), (5, 7, 3), (128, 256, 64), (300, 200, 333), (257, 385, 130), (640, 520, 1000)]
+
+
+@pytest.mark.parametrize("ab,c", DT_PAIRS)
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_tensor_core_parity(ctx, ab, c, ta, tb, shape):
+    M, N, K = shape
+    p = synthetic.make_problem(M, N, K, ab, c, transpose_a=ta, transpose_b=tb, seed=M * 7 + K,
+                               dist="normal")
+    check_full(ctx, p, f"{ab}->{c} {p.layout} {shape}")
+    assert ctx.last_kernel.startswith("tcgen05_" + p.layout.lower())
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (256, 256, 256), (300, 200, 333), (130, 70, 90)])
+def test_ffma_parity(ctx, ta, tb, shape):
+    M, N, K = shape
+    p = synthetic.make_problem(M, N, K, "f32", "f32", transpose_a=ta, transpose_b=tb,
+                               alpha=-1.25, beta=0.5, seed=3 + K, dist="uniform", c_fill="uniform")
+    check_full(ctx, p, f"f32 {p.layout} {shape}")
+    assert ctx.last_kernel.startswith("ffma_f32_" + p.layout.lower())
+
+
+@pytest.mark.parametrize("spec", ["ffma=small", "ffma=large"])
+def test_ffma_tiles(ctx, force, spec):
+    force(spec)
+    p = synthetic.make_problem(333, 290, 517, "f32", "f32", transpose_b=True, seed=5)
+    check_full(ctx, p, spec)
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, 1.0), (-2.0, -0.75), (0.0, 1.0)])
+@pytest.mark.parametrize("c", ["bf16", "f32"])
+def test_alpha_beta(ctx, alpha, beta, c):
+    p = synthetic.make_problem(200, 300, 250, "bf16", c, transpose_a=True, alpha=alpha, beta=beta,
+                               seed=17, dist="normal", c_fill="uniform")
+    check_full(ctx, p, f"alpha={alpha} beta={beta}")
+
+
+@pytest.mark.parametrize("spec", ["bn=64", "bn=128", "bn=192", "bn=256", "bn=128 split=3",
+                                  "bn=256 split=7", "bn=64 split=16", "pack=1", "pack=1 split=5",
+                                  "grid=3", "group_m=1", "group_m=3 bn=64"])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_forced_variants(ctx, force, spec, ta, tb):
+    force(spec)
+    p = synthetic.make_problem(333, 470, 1100, "f16", "f32", transpose_a=ta, transpose_b=tb,
+                               alpha=0.75, beta=-1.0, seed=23, dist="normal", c_fill="uniform")
+    check_full(ctx, p, spec)
+
+
+def test_padded_leading_dimensions(ctx):
+    for ta, tb in LAYOUTS:
+        M, N, K = 150, 170, 190
+        p = synthetic.make_problem(M, N, K, "bf16", "f32", transpose_a=ta, transpose_b=tb, seed=31,
+                                   dist="normal", beta=1.0, c_fill="uniform",
+                                   lda=(M if ta else K) + 24, ldb=(K if tb else N) + 8, ldc=N + 40)
+        check_full(ctx, p, f"padded {p.layout}")
+        assert "pack" not in ctx.last_kernel
+        q = synthetic.make_problem(M, N, K, "bf16", "f32", transpose_a=ta, transpose_b=tb, seed=32,
+                                   dist="normal", lda=(M if ta else K) + 3, ldb=(K if tb else N) + 5,
+                                   ldc=N + 1)
+        check_full(ctx, q, f"odd-padded {q.layout}")
+
+
+# ----------------------------------------------------- exactness and edges
+
+@pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "pack=1 bn=256 split=2"])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
+    """Integer entries in [-4,4], K=2048: every partial sum is an integer
+    below 2^24, so fp32 accumulation is exact in any order."""
+    force(spec)
+    p = synthetic.make_problem(300, 260, 2048, "bf16", "f32", transpose_a=ta, transpose_b=tb,
+                               alpha=0.5, beta=1.0, seed=41, dist="int", scale=4, c_fill="int")
+    out = run_problem(ctx, p)
+    R, _ = oracle.gemm(p)
+    assert np.array_equal(oracle.decode(out), R), ctx.last_kernel
+
+
+def test_rank_one_exact(ctx):
+    for dt in ("f16", "bf16"):
+        p = synthetic.make_problem(190, 170, 1, dt, "f32", seed=43, dist="normal")
+        out = run_problem(ctx, p)
+        R, _ = oracle.gemm(p)
+        assert np.array_equal(oracle.decode(out), R)
+
+
+def test_beta_zero_ignores_nan_c(ctx):
+    for ab, c in DT_PAIRS:
+        p = synthetic.make_problem(200, 130, 70, ab, c, seed=47, dist="normal", c_fill="nan")
+        out = run_problem(ctx, p)
+        assert torch.isfinite(out.float()).all(), ctx.last_kernel
+    p = synthetic.make_problem(64, 64, 64, "f32", "f32", seed=48, c_fill="nan")
+    assert torch.isfinite(run_problem(ctx, p)).all()
+
+
+def test_worked_example_2x2(ctx):
+    """Foundry metal.md "Quick Start": A = {1,2,3,4}, B = {5,6,7,8} -> {19,22,43,50}."""
+    for dt in ("f16", "bf16", "f32"):
+        for ta, tb in LAYOUTS:
+            A = torch.tensor([[1.0, 2.0], [3.0, 4.0]])
+            B = torch.tensor([[5.0, 6.0], [7.0, 8.0]])
+            p = synthetic.Problem(2, 2, 2, dt, dt, ta, tb, 1.0, 0.0,
+                                  (A.T if ta else A).contiguous().to(synthetic.DTYPES[dt]),
+                                  (B.T if tb else B).contiguous().to(synthetic.DTYPES[dt]),
+                                  torch.zeros(2, 2, dtype=synthetic.DTYPES[dt]))
+            out = run_problem(ctx, p)
+            assert out.double().flatten().tolist() == [19, 22, 43, 50]
+
+
+def test_identity_and_permutation(ctx):
+    n = 300
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(3))
+    P = torch.zeros(n, n)
+    P[torch.arange(n), perm] = 1.0
+    p = synthetic.make_problem(n, 200, n, "bf16", "f32", seed=5, dist="normal")
+    p.A = P.to(torch.bfloat16)
+    out = run_problem(ctx, p)
+    assert torch.equal(out, p.B.float()[perm])
+
+
+@pytest.mark.parametrize("spec", ["", "bn=128 split=6"])
+def test_determinism(ctx, force, spec):
+    force(spec)
+    p = synthetic.make_problem(384, 512, 4096, "bf16", "f32", transpose_a=True, seed=53, dist="normal")
+    outs = [run_problem(ctx, p) for _ in range(5 if not spec else 10)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_transpose_flags_match_explicit_copies(ctx):
+    """op() through the flags equals the product of explicitly transposed
+    copies, bitwise."""
+    base = synthetic.make_problem(300, 260, 520, "f16", "f32", seed=59, dist="normal")
+    ref = run_problem(ctx, base)
+    for ta, tb in LAYOUTS[1:]:
+        q = synthetic.Problem(300, 260, 520, "f16", "f32", ta, tb, 1.0, 0.0,
+                              base.A.T.contiguous() if ta else base.A,
+                              base.B.T.contiguous() if tb else base.B, torch.zeros(300, 260))
+        assert torch.equal(run_problem(ctx, q), ref), (ta, tb)
+
+
+def test_refused_call_launches_nothing(ctx):
+    before = ctx.launch_count
+    A = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    d = tg.make_desc(64, 64, 64, "bf16", "bf16", alpha=float("nan"))
+    with pytest.raises(tg.TcError):
+        tg.tc_gemm(ctx, d, A, A, C)
+    d = tg.make_desc(64, 64, 64, "bf16", "bf16")
+    with pytest.raises(tg.TcError):
+        tg.tc_gemm(ctx, d, A, A, A)          # C overlaps A
+    with pytest.raises(ValueError):
+        tg.tc_gemm(ctx, tg.make_desc(65, 64, 64, "bf16", "bf16"), A, A, C)   # capacity
+    assert ctx.launch_count == before
+
+
+# ----------------------------------------------------- batched / grouped / streams
+
+@pytest.mark.parametrize("spec", ["", "pack=1", "bn=128 split=3"])
+def test_batched(ctx, force, spec):
+    force(spec)
+    M, N, K, batch = 200, 136, 264, 3
+    g = torch.Generator().manual_seed(61)
+    A = (torch.randn(batch, M, K, generator=g)).to(torch.bfloat16)
+    B = (torch.randn(batch, K, N, generator=g)).to(torch.bfloat16)
+    C = torch.zeros(batch, M, N)
+    Ad, Bd, Cd = A.cuda(), B.cuda(), C.cuda()
+    bd = tg.tc_gemm_batched_desc(tg.make_desc(M, N, K, "bf16", "f32"), batch, M * K, K * N, M * N)
+    tg.tc_gemm_batched(ctx, bd, Ad, Bd, Cd)
+    out = Cd.cpu()
+    for i in range(batch):
+        p = synthetic.Problem(M, N, K, "bf16", "f32", A=A[i], B=B[i], C=C[i])
+        R, T = oracle.gemm(p)
+        parity.check(out[i].numpy(), R, T, "f32", what=f"batch {i} {ctx.last_kernel}")
+    # one B shared by every entry (stride 0) and a K shorter than lda
+    bd = tg.tc_gemm_batched_desc(tg.make_desc(M, N, K - 1, "bf16", "f32", lda=K), batch, M * K, 0, M * N)
+    tg.tc_gemm_batched(ctx, bd, Ad, Bd, Cd)
+    out = Cd.cpu()
+    for i in range(batch):
+        R, T = oracle.gemm(synthetic.Problem(M, N, K - 1, "bf16", "f32", A=A[i][:, : K - 1].contiguous(),
+                                             B=B[0][: K - 1].contiguous(), C=C[i]))
+        parity.check(out[i].numpy(), R, T, "f32", what=f"shared-B batch {i} {ctx.last_kernel}")
+
+
+def test_grouped_ragged(ctx):
+    probs = synthetic.fp16_ragged(count=8, hi=700, seed=71)
+    s = tg.Stream(ctx)
+    As = [p.A.cuda() for p in probs]
+    Bs = [p.B.cuda() for p in probs]
+    Cs = [p.C.cuda() for p in probs]
+    descs = [tg.make_desc(p.M, p.N, p.K, "f16", "f16") for p in probs]
+    tg.tc_gemm_grouped_async(ctx, descs, As, Bs, Cs, s)
+    s.sync()
+    for p, C in zip(probs, Cs):
+        R, T = oracle.gemm(p)
+        parity.check(oracle.decode(C.cpu()), R, T, "f16", what=f"ragged {p.M}x{p.N}x{p.K}")
+    s.close()
+
+
+def test_torch_stream_wrap(ctx):
+    ts = torch.cuda.Stream()
+    s = tg.Stream(ctx, torch_stream=ts)
+    p = synthetic.make_problem(256, 256, 512, "bf16", "bf16", seed=73, dist="normal")
+    out = run_problem(ctx, p, stream=s)
+    R, T = oracle.gemm(p)
+    parity.check(oracle.decode(out), R, T, "bf16", what="wrapped stream")
+    s.close()
+
+
+def test_host_buffers(ctx):
+    p = synthetic.make_problem(300, 200, 256, "bf16", "f32", beta=1.0, seed=79, dist="normal",
+                               c_fill="uniform")
+    A, B, C = p.A.pin_memory(), p.B.pin_memory(), p.C.clone().pin_memory()
+    d = tg.make_desc(p.M, p.N, p.K, "bf16", "f32", beta=1.0)
+    tg.tc_gemm_host(ctx, d, A, B, C)
+    R, T = oracle.gemm(p)
+    parity.check(C.numpy(), R, T, "f32", what="host buffers")
+
+
+# ----------------------------------------------------- the named workloads
+
+def test_fp32_nn_256(ctx):
+    stats = check_full(ctx, synthetic.fp32_nn_256(), "fp32 NN 256^3")
+    assert ctx.last_kernel.startswith("ffma_f32_nn")
+    assert stats["max_err_over_T"] < 1e-5
+
+
+def test_bf16_nn_4096(ctx):
+    check_sampled(ctx, synthetic.bf16_nn_4096(), what="bf16 NN 4096^3")
+    assert "split" not in ctx.last_kernel
+
+
+@pytest.mark.parametrize("layout", ["TN", "NT"])
+def test_bf16_tn_nt_4096x8192(ctx, layout):
+    check_sampled(ctx, synthetic.bf16_tn_nt_4096x8192(layout), what=f"bf16 {layout} 4096x4096x8192")
+
+
+def test_bf16_tn_splitk_256x16384(ctx):
+    check_full(ctx, synthetic.bf16_tn_splitk_256x16384(), "bf16 TN split-K 256x256x16384")
+    assert "splitk" in ctx.last_kernel
+
+
+def test_fp16_nn_narrow_8192x384(ctx):
+    check_sampled(ctx, synthetic.fp16_nn_narrow_8192x384x4096(), what="fp16 NN 8192x384x4096")
+    assert ctx.last_kernel.endswith("128x192")
+
+
+@pytest.mark.parametrize("n", synthetic.SQUARE_SIZES)
+def test_fp16_square_sweep(ctx, n):
+    p = synthetic.fp16_nn_square(n)
+    if n <= 512:
+        check_full(ctx, p, f"fp16 {n}^3")
+    else:
+        check_sampled(ctx, p, n=1500, what=f"fp16 {n}^3")
+
+
+def test_fp16_ragged_64(ctx):
+    probs = synthetic.fp16_ragged()
+    s = tg.Stream(ctx)
+    As = [p.A.cuda() for p in probs]
+    Bs = [p.B.cuda() for p in probs]
+    Cs = [p.C.cuda() for p in probs]
+    tg.tc_gemm_grouped_async(ctx, [tg.make_desc(p.M, p.N, p.K, "f16", "f16") for p in probs],
+                             As, Bs, Cs, s)
+    s.sync()
+    rng = np.random.default_rng(4)
+    for p, C in zip(probs, Cs):
+        rows, cols = parity.sample_points(p.M, p.N, 200, rng)
+        R, T = oracle.gemm_points(p, rows, cols)
+        parity.check(oracle.decode(C.cpu())[rows, cols], R, T, "f16",
+                     what=f"ragged {p.M}x{p.N}x{p.K}")
+    s.close()
