@@ -1,0 +1,323 @@
+"""Benchmark: GEMM TFLOP/s (2MNK/t) of bf16 NN 4096^3 on GB300, through the C ABI.
+
+One step = one GEMM C = A @ B, M = N = K = 4096, bf16 in / bf16 out, fp32
+accumulation, alpha = 1, beta = 0, inputs normal(0,1) rounded to bf16 from
+seed 1 (the tensorcore gemm.md "Measured perf" 4096^3 shape; the tessl
+architecture.md "Column-Panel Grid Swizzling" bf16 4096^3 figure).
+
+Timing: inputs resident in HBM; before every step the L2 is flushed by
+writing a buffer twice the L2 size; each step's GEMM is bracketed by CUDA
+events on the stream it is launched on (the flush is outside the events);
+W warm-up steps, then exactly K timed steps, with a barrier and a device
+synchronize on both sides.  Under torchrun every rank runs an independent
+replica on its own GPU (the path does not shard), the time is the max over
+ranks and the value is the total over ranks.
+
+Also reported: the roofline of the dominant kernel against the measured
+peak, the end-to-end figure through the host-buffer ABI call (copies
+included), SM clocks sampled during the timed region, and the CPU oracle
+timed on a bounded row band as a baseline.  ``--impl reference`` times the
+CPU oracle (the reference arm of this benchmark) instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M = N = K = 4096
+WORKLOAD = "bf16 NN GEMM M=N=K=4096, bf16 out, fp32 accumulate, alpha=1 beta=0, normal(0,1) from seed 1"
+METRIC = "GEMM TFLOP/s (2MNK/t) bf16 4096^3 NN"
+PAGES_BASELINE = 29.0     # TFLOP/s, bf16 4096^3 NN, Apple M5 Pro (tessl architecture.md, column-panel swizzle)
+FLOPS = 2.0 * M * N * K
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained"), d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def profile_traffic(src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    if it was taken on the current source; else None."""
+    path = os.path.join(ROOT, "profiles", "tcgen05_nn_bf16_4096.md")
+    try:
+        vals = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    vals[k.strip()] = v.strip().strip("`")
+        if vals.get("source_sha256") != src_hash:
+            return None
+        return int(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("tc_mma.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "matrix_multiply_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_baseline(target_s: float = 12.0):
+    """The CPU oracle, as it stands, on a band of output rows of the same
+    workload (bounded to ~target_s seconds)."""
+    import oracle
+    import synthetic
+    p = synthetic.bf16_nn_4096()
+    lib = oracle.load_library()
+    t0 = time.perf_counter()
+    rows = 4
+    oracle.gemm(p, 0, rows, lib=lib)
+    dt = time.perf_counter() - t0
+    rows = int(max(4, min(M, rows * target_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.gemm(p, 0, rows, lib=lib)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(lib),
+            "kind": "oracle", "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} problem ({dt:.1f} s)",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import synthetic
+    p = synthetic.bf16_nn_4096()
+    lib = oracle.load_library()
+    rows = 8
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(p, 0, rows, lib=lib)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = 2.0 * rows * N * K * len(times) / tot / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"each step computes rows 0..{rows - 1} of C"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(lib),
+                         "kind": "oracle", "sample": f"rows 0..{rows - 1} of the {M}^3 problem per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import matrix_multiply_gb300 as tg
+    import synthetic
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ctx = tg.Context(local)
+    tstream = torch.cuda.current_stream()
+    stream = tg.Stream(ctx, torch_stream=tstream)
+    p = synthetic.bf16_nn_4096()
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    d = tg.make_desc(M, N, K, "bf16", "bf16")
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        tg.tc_gemm_async(ctx, d, A, B, C, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = ctx.launch_count
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(tstream)
+            step()
+            ends[i].record(tstream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    torch.cuda.synchronize()
+    stream.sync()
+    launches = ctx.launch_count - launches0
+    kernel = ctx.last_kernel
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * FLOPS * args.steps / (total_ms / 1e3) / 1e12
+
+    # end to end through the host-buffer ABI call (copies inside the timed region)
+    Ah, Bh = p.A.pin_memory(), p.B.pin_memory()
+    Ch = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        tg.tc_gemm_host(ctx, d, Ah, Bh, Ch)
+    e2e_steps = max(5, min(args.steps, 30))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        tg.tc_gemm_host(ctx, d, Ah, Bh, Ch)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_ms = e2e_s * 1e3
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * FLOPS / (e2e_ms / 1e3) / 1e12
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    burst, sustained, hbm, src = peaks()
+    achieved = FLOPS / (statistics.mean(ms) / 1e3) / 1e12
+    traffic = profile_traffic(kernel_source_hash())
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / (world * PAGES_BASELINE), "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "layout": "NN",
+                   "global_batch": 1, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "variant": kernel,
+                   "l2": "flushed before every step (write of >= 2x L2); flush outside the timed events",
+                   "vs_baseline_ref": "29.0 TFLOP/s bf16 4096^3 NN on Apple M5 Pro (tessl architecture.md)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                     "frac": achieved / burst, "traffic": traffic,
+                     "peak_source": f"{src} bf16 dense burst (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback 1.9 PFLOP/s"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * (M * K + K * N),
+                "d2h_bytes_per_step": 2 * M * N, "ms_per_step": e2e_ms,
+                "call": "tc_gemm_host (pinned host A, B, C)"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    stream.close()
+    ctx.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

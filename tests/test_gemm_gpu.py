@@ -130,9 +130,10 @@ def test_forced_variants(ctx, force, spec, ta, tb):
 def test_padded_leading_dimensions(ctx):
     for ta, tb in LAYOUTS:
         M, N, K = 150, 170, 190
+        r8 = lambda x: (x + 7) // 8 * 8      # noqa: E731  (16-byte multiple rows: no repacking)
         p = synthetic.make_problem(M, N, K, "bf16", "f32", transpose_a=ta, transpose_b=tb, seed=31,
                                    dist="normal", beta=1.0, c_fill="uniform",
-                                   lda=(M if ta else K) + 24, ldb=(K if tb else N) + 8, ldc=N + 40)
+                                   lda=r8(M if ta else K) + 24, ldb=r8(K if tb else N) + 8, ldc=N + 40)
         check_full(ctx, p, f"padded {p.layout}")
         assert "pack" not in ctx.last_kernel
         q = synthetic.make_problem(M, N, K, "bf16", "f32", transpose_a=ta, transpose_b=tb, seed=32,
