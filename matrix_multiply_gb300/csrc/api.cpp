@@ -43,6 +43,7 @@ struct tc_ctx {
     uint64_t launches = 0;
     void *dbuf[3] = {nullptr, nullptr, nullptr};  // device copies for tc_gemm_host
     size_t dcap[3] = {0, 0, 0};
+    int max_pairs[2] = {-1, -1};                   // resident CTA pairs (BN 128, 256), queried once
     std::mutex mu;
 };
 
@@ -129,7 +130,10 @@ tc_status_t validate(const tc_gemm_desc *d, const void *A, const void *B, const 
 struct Plan {
     bool ffma = false;
     int ffma_tile = FFMA_SMALL;
-    int bn = 256, split = 1, grid = 1, group_m = 8;
+    int bn = 256, cg = 1, split = 1, grid = 1, group_m = 8;
+    int64_t seg0_tiles = 0, split_base = 0;
+    int seg0_split = 1, seg1_split = 1;
+    bool tma_store = true;
     bool pack_a = false, pack_b = false;
     int64_t tiles = 0, units = 0;
     std::string name;
@@ -139,9 +143,12 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Environment override for tests and sweeps: TC_FORCE_VARIANT holds
 // space/comma separated tokens: bn=<64|128|192|256> split=<S> grid=<G>
-// group_m=<G> ffma=<small|large> pack=<1>.
+// group_m=<G> ffma=<small|large> pack=<1> tail=<S> (K slices of the
+// last-wave tiles; 0 or 1 disables) sms=<N> (plan for N SMs) cg=<1|2>
+// (CTAs per tile) store=direct (plain stores of C instead of TMA stores).
 struct Force {
-    int bn = 0, split = 0, grid = 0, group_m = 0, ffma = -1, pack = 0;
+    int bn = 0, split = 0, grid = 0, group_m = 0, ffma = -1, pack = 0, tail = -1, sms = 0, cg = 0;
+    bool direct_store = false;
 };
 
 Force read_force()
@@ -167,23 +174,60 @@ Force read_force()
         else if (k == "group_m") f.group_m = std::atoi(v.c_str());
         else if (k == "ffma") f.ffma = (v == "large") ? FFMA_LARGE : FFMA_SMALL;
         else if (k == "pack") f.pack = std::atoi(v.c_str());
+        else if (k == "tail") f.tail = std::atoi(v.c_str());
+        else if (k == "sms") f.sms = std::atoi(v.c_str());
+        else if (k == "cg") f.cg = std::atoi(v.c_str());
+        else if (k == "store") f.direct_store = (v == "direct");
     }
     return f;
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Relative per-tile throughput of the tensor-core main loop by tile width
-// (narrower tiles read more shared memory per MMA flop), measured on GB300
-// at 4096^3 bf16: 128x192 tiles run 0.87x and 128x128 tiles 0.63x the
-// flop rate of 128x256 tiles.
-double bn_rate(int bn) { return bn == 256 ? 1.0 : bn == 192 ? 0.87 : bn == 128 ? 0.63 : 0.45; }
+// Relative main-loop throughput per SM of each kernel shape (CTAs per tile,
+// tile width), measured on GB300 with bf16 at M = N = 4096 and long K:
+// narrower tiles read more shared memory per MMA flop, and a CTA pair
+// (tcgen05.mma.cta_group::2) loads half of B per SM.
+double tile_rate(int cg, int bn)
+{
+    if (cg == 2) return bn == 256 ? 1.15 : 0.72;
+    return bn == 256 ? 1.0 : bn == 192 ? 0.87 : bn == 128 ? 0.63 : 0.45;
+}
+
+// Persistent schedule of `tiles` output tiles on num_sms CTAs: whole waves
+// of tiles, then the partial last wave.  When the last wave leaves at least
+// half of the SMs idle, its tiles are cut into K slices (reduced in fixed
+// order) so that every SM gets work.
+struct Sched {
+    int64_t tiles, seg0_tiles;
+    int seg0_split, seg1_split;
+    double t;   // modelled time, in units of one BN=256 tile
+};
+
+Sched schedule(int64_t tiles, int64_t num_kb, int num_sms, int cg, int bn, int force_tail)
+{
+    const int64_t G = std::min<int64_t>(tiles, num_sms);
+    const int64_t full = tiles / G, L = tiles % G;
+    Sched s{tiles, tiles, 1, 1, 0.0};
+    if (L > 0 && full >= 1) {
+        int64_t S2 = std::min<int64_t>(std::min<int64_t>(G / L, num_kb / 4), 4);
+        if (force_tail >= 0) S2 = force_tail;
+        if (S2 >= 2) {
+            s.seg0_tiles = tiles - L;
+            s.seg1_split = (int)S2;
+        }
+    }
+    const double tail = L == 0 ? 0.0 : (s.seg1_split > 1 ? 1.0 / s.seg1_split + 0.05 : 1.0);
+    s.t = ((double)full + tail) * bn / tile_rate(cg, bn);
+    return s;
+}
 
 tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const void *B, int num_sms,
                       Plan *out)
 {
     Plan p;
     const Force f = read_force();
+    if (f.sms > 0) num_sms = f.sms;
     if (num_sms < 1) num_sms = 1;
     const char *lay = d->transpose_a ? (d->transpose_b ? "tt" : "tn") : (d->transpose_b ? "nt" : "nn");
     const char *dt = d->a_dtype == TC_F32 ? "f32" : d->a_dtype == TC_BF16 ? "bf16" : "f16";
@@ -210,43 +254,61 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     if (f.pack) p.pack_a = p.pack_b = true;
 
     const int64_t num_kb = cdiv(d->K, BK);
-    const int64_t tm = cdiv(d->M, BM);
-
-    // Split-K: too few output tiles to occupy the SMs and a long K loop.
-    const int64_t tiles128 = tm * cdiv(d->N, 128) * n.batch;
-    int bn = 0, split = 1;
-    if (tiles128 * 2 <= num_sms && num_kb >= 16) {
-        bn = 128;
-        split = (int)std::min<int64_t>(num_sms / tiles128, num_kb / 4);
-        if (split < 2) split = 1;
+    const int64_t tiles128 = cdiv(d->M, BM) * cdiv(d->N, 128) * n.batch;
+    int bn = 0, cg = 1;
+    Sched sc{};
+    if ((f.split == 0 && f.cg != 2 && tiles128 * 2 <= num_sms && num_kb >= 16) || f.split > 0) {
+        // split-K: too few output tiles to occupy the SMs and a long K loop
+        bn = f.bn ? f.bn : 128;
+        const int64_t tiles = cdiv(d->M, BM) * cdiv(d->N, bn) * n.batch;
+        int split = f.split > 0 ? f.split
+                                : (int)std::min<int64_t>(std::max<int64_t>(num_sms / tiles, 1), num_kb / 4);
+        split = (int)std::min<int64_t>(std::max(split, 1), num_kb);
+        sc = {tiles, tiles, split, 1, 0.0};
     } else {
-        // pick the tile width that minimises (tiles per CTA) x (time per tile)
+        // the kernel shape (CTAs per tile, tile width) with the least modelled time
+        static const int shapes[][2] = {{2, 256}, {1, 256}, {1, 192}, {2, 128}, {1, 128}, {1, 64}};
         double best = 1e300;
-        for (int cand : {256, 192, 128}) {
-            const int64_t tiles = tm * cdiv(d->N, cand) * n.batch;
-            const int64_t per_cta = cdiv(tiles, num_sms);
-            const double t = (double)per_cta * cand / bn_rate(cand);
-            if (t < best - 1e-9) {
-                best = t;
-                bn = cand;
+        for (const auto &sh : shapes) {
+            const int c = sh[0], b = sh[1];
+            if (f.cg && c != f.cg) continue;
+            if (f.bn ? b != f.bn : b == 64) continue;      // 64-wide tiles only on request
+            const int workers = c == 2 ? std::max(num_sms / 2, 1) : num_sms;
+            const Sched t = schedule(cdiv(d->M, BM * c) * cdiv(d->N, b) * n.batch, num_kb, workers, c, b, f.tail);
+            if (t.t < best - 1e-9) {
+                best = t.t;
+                bn = b;
+                cg = c;
+                sc = t;
             }
         }
     }
-    if (f.bn == 64 || f.bn == 128 || f.bn == 192 || f.bn == 256) bn = f.bn;
-    if (f.split > 0) split = (int)std::min<int64_t>(f.split, num_kb);
+    const int workers = cg == 2 ? std::max(num_sms / 2, 1) : num_sms;   // tiles in flight
+    if (bn == 0) return TC_ERR_VARIANT;
     p.bn = bn;
-    p.split = split;
-    p.tiles = tm * cdiv(d->N, bn) * n.batch;
-    p.units = p.tiles * split;
+    p.cg = cg;
+    p.tiles = sc.tiles;
+    p.seg0_tiles = sc.seg0_tiles;
+    p.seg0_split = sc.seg0_split;
+    p.seg1_split = sc.seg1_split;
+    p.units = sc.seg0_tiles * sc.seg0_split + (sc.tiles - sc.seg0_tiles) * sc.seg1_split;
+    p.split_base = sc.seg0_split > 1 ? 0 : sc.seg0_tiles;
+    p.split = (sc.seg0_split > 1 || (sc.tiles > sc.seg0_tiles && sc.seg1_split > 1)) ? 2 : 1;
     if (p.units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
-    p.grid = (int)std::min<int64_t>(p.units, num_sms);
+    p.grid = (int)std::min<int64_t>(p.units, workers);
     if (f.grid > 0) p.grid = (int)std::min<int64_t>(f.grid, p.units);
-    p.group_m = f.group_m > 0 ? f.group_m : 8;
-    std::snprintf(buf, sizeof buf, "tcgen05_%s_%s_%s_128x%d%s%s%s", lay, dt, ct, bn,
-                  split > 1 ? "_splitk" : "", p.pack_a ? "_packA" : "", p.pack_b ? "_packB" : "");
+    p.grid *= cg;                                  // CTAs
+    p.group_m = f.group_m > 0 ? f.group_m : 4;
+    p.tma_store = !f.direct_store;
+    std::snprintf(buf, sizeof buf, "tcgen05_%s_%s_%s_%dx%d%s%s%s%s", lay, dt, ct, BM * cg, bn,
+                  cg == 2 ? "_pair" : "", sc.seg0_split > 1 ? "_splitk" : "", p.pack_a ? "_packA" : "",
+                  p.pack_b ? "_packB" : "");
     p.name = buf;
-    if (split > 1) {
-        std::snprintf(buf, sizeof buf, "_s%d", split);
+    if (sc.seg0_split > 1) {
+        std::snprintf(buf, sizeof buf, "_s%d", sc.seg0_split);
+        p.name += buf;
+    } else if (sc.tiles > sc.seg0_tiles) {
+        std::snprintf(buf, sizeof buf, "_tail%dx%d", (int)(sc.tiles - sc.seg0_tiles), sc.seg1_split);
         p.name += buf;
     }
     *out = p;
@@ -297,16 +359,19 @@ tc_status_t ensure_tickets(tc_stream *s, size_t count)
 
 bool encode_map(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, int64_t inner, int64_t outer,
                 int64_t ld_elems, bool three_d, int64_t batch, int64_t bstride_elems, uint32_t box_inner,
-                uint32_t box_outer)
+                uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
-    const CUtensorMapDataType t = dt == TC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType t = dt == TC_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : dt == TC_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int64_t es = (int64_t)elem_size(dt);
     cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
-    cuuint64_t strides[2] = {(cuuint64_t)ld_elems * 2, (cuuint64_t)bstride_elems * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld_elems * es), (cuuint64_t)(bstride_elems * es)};
     cuuint32_t box[3] = {box_inner, box_outer, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = ctx->encode(m, t, three_d ? 3 : 2, const_cast<void *>(base), dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -358,10 +423,11 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     const int64_t ldb_p = p.pack_b ? (int64_t)round_up((size_t)n.b_cols, 8) : n.ldb;
     const size_t a_pack_bytes = p.pack_a ? round_up((size_t)(n.a_rows * lda_p * a_batch * 2), 256) : 0;
     const size_t b_pack_bytes = p.pack_b ? round_up((size_t)(n.b_rows * ldb_p * b_batch * 2), 256) : 0;
-    const size_t part_bytes = p.split > 1 ? (size_t)p.units * BM * p.bn * sizeof(float) : 0;
+    const size_t part_bytes =
+        p.split > 1 ? (size_t)(p.units - p.split_base) * BM * p.cg * p.bn * sizeof(float) : 0;
     tc_status_t st = ensure_ws(s, a_pack_bytes + b_pack_bytes + part_bytes + 256);
     if (st != TC_OK) return st;
-    if (p.split > 1 && (st = ensure_tickets(s, (size_t)p.tiles * 4)) != TC_OK) return st;
+    if (p.split > 1 && (st = ensure_tickets(s, (size_t)p.tiles * p.cg * 4)) != TC_OK) return st;
     uint8_t *ws = static_cast<uint8_t *>(s->ws);
     const void *Ause = A, *Buse = B;
     int64_t sa = n.sa, sb = n.sb;
@@ -386,17 +452,28 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
 
     MmaLaunch L{};
     L.bn = p.bn;
+    L.cg = p.cg;
     L.grid = p.grid;
+    if (p.cg == 2) {
+        // no more pairs than can be resident at once (a persistent grid)
+        int &pairs = ctx->max_pairs[p.bn == 256 ? 1 : 0];
+        if (pairs < 0) pairs = max_active_pairs(p.bn);
+        if (pairs < 1) return TC_ERR_VARIANT;
+        L.grid = std::min(L.grid, 2 * pairs);
+    }
     MmaArgs &a = L.args;
     a.M = d->M;
     a.N = d->N;
     a.K = d->K;
     a.num_kb = (int)cdiv(d->K, BK);
-    a.tiles_m = (int)cdiv(d->M, BM);
+    a.tiles_m = (int)cdiv(d->M, BM * p.cg);
     a.tiles_n = (int)cdiv(d->N, p.bn);
     a.tiles_per_batch = a.tiles_m * a.tiles_n;
     a.batch = (int)n.batch;
-    a.split_k = p.split;
+    a.seg0_tiles = (int)p.seg0_tiles;
+    a.seg0_split = p.seg0_split;
+    a.seg1_split = p.seg1_split;
+    a.split_base = (int)p.split_base;
     a.total_units = (int)p.units;
     a.group_m = p.group_m;
     a.a_kmajor = !d->transpose_a;
@@ -408,7 +485,8 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     // N >> 3 (bits 17-22), M >> 4 (bits 24-28)
     const uint32_t fmt = d->a_dtype == TC_BF16 ? 1u : 0u;
     a.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(!a.a_kmajor) << 15) |
-              ((uint32_t)(!a.b_kmajor) << 16) | ((uint32_t)(p.bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+              ((uint32_t)(!a.b_kmajor) << 16) | ((uint32_t)(p.bn >> 3) << 17) |
+              ((uint32_t)((BM * p.cg) >> 4) << 24);
     a.alpha = d->alpha;
     a.beta = d->beta;
     a.C = C;
@@ -417,10 +495,13 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.c_dtype = d->c_dtype;
     const int64_t ec = (int64_t)elem_size(d->c_dtype);
     a.c_vec_ok = aligned16(C) && (n.ldc * ec) % 16 == 0 && (a.stride_c * ec) % 16 == 0;
+    // C written through TMA stores of 32 x 32 chunks when its layout allows
+    a.c_tma = a.c_vec_ok && p.tma_store;
+    a.c_3d = n.batch > 1;
     a.ws = p.split > 1 ? reinterpret_cast<float *>(ws + a_pack_bytes + b_pack_bytes) : nullptr;
     a.tickets = p.split > 1 ? s->tickets : nullptr;
     a.status = s->status_dev;
-    const int64_t kb_per_unit = cdiv(a.num_kb, p.split);
+    const int64_t kb_per_unit = a.num_kb;
     a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
 
     const int64_t lda_use = p.pack_a ? lda_p : n.lda;
@@ -433,10 +514,13 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     if (ok) {
         if (a.b_kmajor)
             ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->K, d->N, ldb_use, a.b_3d, n.batch, sb, 64,
-                            (uint32_t)p.bn);
+                            (uint32_t)(p.bn / p.cg));
         else
             ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, a.b_3d, n.batch, sb, 64, 64);
     }
+    if (ok && a.c_tma)
+        ok = encode_map(ctx, &L.tmC, d->c_dtype, C, d->N, d->M, n.ldc, a.c_3d, n.batch, a.stride_c, 32, 32,
+                        d->c_dtype == TC_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return TC_ERR_CUDA;
     if ((e = launch_mma(L, s->st)) != cudaSuccess) return TC_ERR_CUDA;
     ++launches;

@@ -15,22 +15,27 @@ constexpr int BK = 64;
 constexpr int MMA_K = 16;                       // K of one kind::f16 tcgen05.mma
 constexpr int MMA_THREADS = 192;                // 4 epilogue warps, TMA warp, MMA warp
 constexpr int SMEM_LIMIT = 232448;              // max dynamic shared memory per block
-constexpr int SMEM_RESERVE = 1024 + 256;        // alignment slack + barriers
+constexpr int EPI_STAGE_BYTES = 4096;           // one 32 x 32 output chunk (fp32 worst case)
+constexpr int EPI_SMEM = 4 * 2 * EPI_STAGE_BYTES;  // 4 epilogue warps, double buffered
+constexpr int SMEM_RESERVE = 1024 + 256 + EPI_SMEM;  // alignment slack + barriers + epilogue staging
 
-__host__ __device__ constexpr int stage_bytes(int bn) { return (BM + bn) * BK * 2; }
+// One pipeline stage of a CTA: its 128 rows of A and its share of B (all BN
+// columns for a single CTA; BN/2 for each CTA of a pair running
+// tcgen05.mma.cta_group::2 on a 256 x BN tile).
+__host__ __device__ constexpr int stage_bytes(int bn, int cg) { return (BM + bn / cg) * BK * 2; }
 __host__ __device__ constexpr int tmem_cols(int bn)
 {
     return (2 * bn <= 128) ? 128 : (2 * bn <= 256) ? 256 : 512;
 }
-__host__ __device__ constexpr int mma_stages(int bn)
+__host__ __device__ constexpr int mma_stages(int bn, int cg)
 {
-    return ((SMEM_LIMIT - SMEM_RESERVE) / stage_bytes(bn)) > 8
+    return ((SMEM_LIMIT - SMEM_RESERVE) / stage_bytes(bn, cg)) > 8
                ? 8
-               : ((SMEM_LIMIT - SMEM_RESERVE) / stage_bytes(bn));
+               : ((SMEM_LIMIT - SMEM_RESERVE) / stage_bytes(bn, cg));
 }
-__host__ __device__ constexpr int mma_smem_bytes(int bn)
+__host__ __device__ constexpr int mma_smem_bytes(int bn, int cg)
 {
-    return mma_stages(bn) * stage_bytes(bn) + SMEM_RESERVE;
+    return mma_stages(bn, cg) * stage_bytes(bn, cg) + SMEM_RESERVE;
 }
 
 // Device-side arguments of the tensor-core kernel (the two TMA descriptors
@@ -41,8 +46,15 @@ struct MmaArgs {
     int tiles_m, tiles_n;  // per batch entry
     int tiles_per_batch;
     int batch;
-    int split_k;           // K slices per output tile (1 = no split)
-    int total_units;       // batch * tiles_per_batch * split_k
+    // Work units: output tiles in the linear (band-swizzled) order, each cut
+    // into K slices.  Tiles [0, seg0_tiles) have seg0_split slices each, the
+    // remaining tiles seg1_split slices each; unit u enumerates (tile, slice)
+    // pairs in that order.  A tile with more than one slice parks its
+    // partial sums in ws slot (u - split_base) and the last slice to finish
+    // reduces them in slice order.
+    int seg0_tiles, seg0_split, seg1_split;
+    int split_base;
+    int total_units;
     int group_m;           // rasterisation band height, in tile rows
     int a_kmajor, b_kmajor;
     int a_3d, b_3d;        // 3-D descriptors: the batch index is the third coordinate
@@ -51,7 +63,9 @@ struct MmaArgs {
     void *C;
     long long ldc, stride_c;
     int c_dtype;           // TC_F16 / TC_BF16 / TC_F32
-    int c_vec_ok;          // 16-byte vector stores allowed on C
+    int c_vec_ok;          // 16-byte vector loads/stores allowed on C
+    int c_tma;             // C is written by TMA stores through the third descriptor
+    int c_3d;              // that descriptor is 3-D (batch index third)
     float *ws;             // split-K partial tiles
     unsigned *tickets;     // split-K arrival counters (zero between launches)
     unsigned *status;      // device status word (0 = fine)
@@ -60,12 +74,16 @@ struct MmaArgs {
 
 struct MmaLaunch {
     int bn;
-    int grid;
-    CUtensorMap tmA, tmB;
+    int cg;      // CTAs per tile: 1, or 2 for a CTA pair (cluster of two)
+    int grid;    // CTAs (a multiple of cg)
+    CUtensorMap tmA, tmB, tmC;
     MmaArgs args;
 };
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st);
+// Largest number of CTA pairs of the BN-wide pair kernel that can be
+// resident at once on the current device (0 if the pair kernel cannot run).
+int max_active_pairs(int bn);
 
 // fp32 FFMA kernel (exact fp32, ascending-k fused multiply-add chain)
 struct FfmaArgs {

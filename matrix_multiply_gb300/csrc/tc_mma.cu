@@ -87,17 +87,31 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity)
 }
 
 struct Unit {
-    int b, tm, tn, s, kb0, kb1, tile;
+    int b, tm, tn;       // batch entry and tile coordinates
+    int tile;            // linear tile id over every batch entry
+    int s, S;            // K slice of this unit and the tile's slice count
+    int kb0, kb1;        // K-block range [kb0, kb1)
+    int ufirst;          // unit of slice 0 of this tile
 };
 
 __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
 {
     Unit r;
-    r.s = u % a.split_k;
-    const int rest = u / a.split_k;
-    r.b = rest / a.tiles_per_batch;
-    const int t = rest - r.b * a.tiles_per_batch;
-    r.tile = t;
+    const int seg0_units = a.seg0_tiles * a.seg0_split;
+    if (u < seg0_units) {
+        r.tile = u / a.seg0_split;
+        r.s = u - r.tile * a.seg0_split;
+        r.S = a.seg0_split;
+    } else {
+        const int v = u - seg0_units;
+        const int q = v / a.seg1_split;
+        r.tile = a.seg0_tiles + q;
+        r.s = v - q * a.seg1_split;
+        r.S = a.seg1_split;
+    }
+    r.ufirst = u - r.s;
+    r.b = r.tile / a.tiles_per_batch;
+    const int t = r.tile - r.b * a.tiles_per_batch;
     // bands of group_m tile rows, column-major inside a band
     const int band = a.group_m * a.tiles_n;
     const int g = t / band;
@@ -106,8 +120,8 @@ __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
     const int in_band = t - g * band;
     r.tm = first_m + in_band % rows_in_band;
     r.tn = in_band / rows_in_band;
-    r.kb0 = (int)(((long long)r.s * a.num_kb) / a.split_k);
-    r.kb1 = (int)(((long long)(r.s + 1) * a.num_kb) / a.split_k);
+    r.kb0 = (int)(((long long)r.s * a.num_kb) / r.S);
+    r.kb1 = (int)(((long long)(r.s + 1) * a.num_kb) / r.S);
     return r;
 }
 
@@ -151,38 +165,44 @@ __device__ __forceinline__ void store_c1(void *C, long long off, float v, int c_
     }
 }
 
-// out[row, col0 .. col0+31] = alpha * v + beta * C_old  (masked to M, N)
-__device__ __forceinline__ void store_row_chunk(const MmaArgs &a, int b, long long row, long long col0,
-                                                float (&v)[32])
+// v <- alpha * v + beta * C_old[row, col0 .. col0+31]; C_old is read only
+// when beta != 0 (masked to M, N)
+__device__ __forceinline__ void apply_alpha_beta(const MmaArgs &a, int b, long long row, long long col0,
+                                                 float (&v)[32])
 {
-    if (row >= a.M) return;
+    if (a.beta == 0.0f || row >= a.M) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = a.alpha * v[j];
+        return;
+    }
     const long long base = (long long)b * a.stride_c + row * a.ldc + col0;
-    const bool full = (col0 + 32 <= a.N);
-    const bool vec = full && a.c_vec_ok;
-    if (a.beta != 0.0f) {
-        if (vec && a.c_dtype == TC_F32) {
-            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.C) + base);
+    const bool vec = (col0 + 32 <= a.N) && a.c_vec_ok;
+    if (vec && a.c_dtype == TC_F32) {
+        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.C) + base);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 c = src[q];
-                v[4 * q + 0] = fmaf(a.beta, c.x, a.alpha * v[4 * q + 0]);
-                v[4 * q + 1] = fmaf(a.beta, c.y, a.alpha * v[4 * q + 1]);
-                v[4 * q + 2] = fmaf(a.beta, c.z, a.alpha * v[4 * q + 2]);
-                v[4 * q + 3] = fmaf(a.beta, c.w, a.alpha * v[4 * q + 3]);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float c = (col0 + j < a.N) ? load_c(a.C, base + j, a.c_dtype) : 0.0f;
-                v[j] = fmaf(a.beta, c, a.alpha * v[j]);
-            }
+        for (int q = 0; q < 8; ++q) {
+            const float4 c = src[q];
+            v[4 * q + 0] = fmaf(a.beta, c.x, a.alpha * v[4 * q + 0]);
+            v[4 * q + 1] = fmaf(a.beta, c.y, a.alpha * v[4 * q + 1]);
+            v[4 * q + 2] = fmaf(a.beta, c.z, a.alpha * v[4 * q + 2]);
+            v[4 * q + 3] = fmaf(a.beta, c.w, a.alpha * v[4 * q + 3]);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = a.alpha * v[j];
+        for (int j = 0; j < 32; ++j) {
+            const float c = (col0 + j < a.N) ? load_c(a.C, base + j, a.c_dtype) : 0.0f;
+            v[j] = fmaf(a.beta, c, a.alpha * v[j]);
+        }
     }
+}
 
-    if (vec) {
+// C[row, col0 .. col0+31] = v with plain stores (C not readable by TMA)
+__device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long row, long long col0,
+                                             const float (&v)[32])
+{
+    if (row >= a.M) return;
+    const long long base = (long long)b * a.stride_c + row * a.ldc + col0;
+    if ((col0 + 32 <= a.N) && a.c_vec_ok) {
         if (a.c_dtype == TC_F32) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.C) + base);
 #pragma unroll
@@ -207,26 +227,74 @@ __device__ __forceinline__ void store_row_chunk(const MmaArgs &a, int b, long lo
     }
 }
 
+// The warp's 32 x 32 chunk (lane = row) goes through a swizzled shared
+// buffer and one TMA store, which also clips rows >= M and columns >= N.
+// fp32 rows are 128 bytes (128-byte swizzle: 16-byte unit q of row r sits at
+// q ^ (r % 8)); 16-bit rows are 64 bytes (64-byte swizzle: q ^ ((r / 2) % 4)).
+// Either way each group of 8 lanes covers all 32 banks.
+__device__ __forceinline__ void store_tma(const MmaArgs &a, const CUtensorMap *tmC, uint8_t *buf, int lane,
+                                          int b, long long row0, long long col0, const float (&v)[32])
+{
+    if (lane == 0) bulk_wait_read<1>();      // this buffer's previous store has read it
+    __syncwarp();
+    if (a.c_dtype == TC_F32) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(buf + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2(v[8 * q + 0], v[8 * q + 1], a.c_dtype);
+            w.y = pack2(v[8 * q + 2], v[8 * q + 3], a.c_dtype);
+            w.z = pack2(v[8 * q + 4], v[8 * q + 5], a.c_dtype);
+            w.w = pack2(v[8 * q + 6], v[8 * q + 7], a.c_dtype);
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
+        }
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (a.c_3d)
+            tma_store_3d(tmC, smem_u32(buf), (int)col0, (int)row0, b);
+        else
+            tma_store_2d(tmC, smem_u32(buf), (int)col0, (int)row0);
+        bulk_commit();
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <int BN>
+// CG = 1: one CTA computes a 128 x BN tile with tcgen05.mma.cta_group::1.
+// CG = 2: a cluster of two CTAs computes a 256 x BN tile with
+//   tcgen05.mma.cta_group::2 issued by the even CTA; each CTA loads its own
+//   128 rows of A and its own BN/2 columns of B, and each CTA's TMEM holds
+//   its 128 rows of the accumulator.  Both CTAs' copies complete on the even
+//   CTA's "full" barriers; its MMA commits arrive on both CTAs' "empty" and
+//   "tmem full" barriers; both CTAs' epilogues release the accumulator on
+//   the even CTA's "tmem empty" barrier.
+template <int BN, int CG>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const MmaArgs args)
+               const __grid_constant__ CUtensorMap tmC, const MmaArgs args)
 {
-    constexpr int STAGE = stage_bytes(BN);
+    constexpr int BNL = BN / CG;                   // B columns loaded by this CTA
+    constexpr int STAGE = stage_bytes(BN, CG);
     constexpr int A_BYTES = BM * BK * 2;
-    constexpr int S = mma_stages(BN);
+    constexpr int S = mma_stages(BN, CG);
     constexpr int TCOLS = tmem_cols(BN);
-    constexpr int ACC_STRIDE = TCOLS / 2;      // TMEM columns between the two accumulators
+    constexpr int ACC_STRIDE = TCOLS / 2;          // TMEM columns between the two accumulators
     constexpr int CHUNKS = BN / 32;
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+    static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
+    static_assert(BNL % 64 == 0 && BN <= 256, "each CTA's B share must be whole 64-column boxes");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * STAGE);
+    uint8_t *cstage = smem + S * STAGE;            // epilogue staging, 2 x 4 KB per warp
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + EPI_SMEM);
     uint64_t *full_bar = bars;
     uint64_t *empty_bar = bars + S;
     uint64_t *tfull_bar = bars + 2 * S;
@@ -237,6 +305,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int cluster = blockIdx.x / CG;
+    const int nclusters = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -245,7 +316,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull_bar[i]), 1);
-            mbar_init(smem_u32(&tempty_bar[i]), 128);
+            mbar_init(smem_u32(&tempty_bar[i]), 4 * CG);    // one arrival per epilogue warp
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0u;
@@ -254,11 +325,18 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (args.c_tma) prefetch_tmap(&tmC);
     }
     __syncwarp();
-    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TCOLS);
+    if (warp == 0) {
+        if (CG == 1)
+            tmem_alloc(smem_u32(tmem_slot), TCOLS);
+        else
+            tmem_alloc_pair(smem_u32(tmem_slot), TCOLS);
+    }
     tc_fence_before();
     __syncthreads();
+    if (CG == 2) cluster_sync();     // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -269,37 +347,53 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < args.total_units; u += gridDim.x) {
+            for (int u = cluster; ok && u < args.total_units; u += nclusters) {
                 const Unit w = decode_unit(args, u);
-                const int m0 = w.tm * BM, n0 = w.tn * BN;
+                const int m0 = w.tm * (BM * CG) + (int)rank * BM;
+                const int n0 = w.tn * BN + (int)rank * BNL;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     const uint32_t stage = it % S, ph = (it / S) & 1u;
                     if (!wait_bar(smem_u32(&empty_bar[stage]), ph ^ 1u, watch, W_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, STAGE);
+                    const uint32_t fb_local = smem_u32(&full_bar[stage]);
+                    uint32_t fb = fb_local;
+                    if (CG == 1) {
+                        mbar_arrive_expect_tx(fb_local, STAGE);
+                    } else {
+                        // the even CTA's barrier counts both CTAs' bytes
+                        fb = mapa_shared(fb_local, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * STAGE);
+                    }
                     const uint32_t sa = smem_u32(smem + stage * STAGE);
                     const uint32_t sb = sa + A_BYTES;
                     const int k0 = kb * BK;
+                    auto load = [&](const CUtensorMap *tm, bool is3d, uint32_t dst, int c0, int c1) {
+                        if (CG == 1) {
+                            tma_load(tm, is3d, dst, fb, c0, c1, w.b);
+                        } else if (is3d) {
+                            tma_load_3d_pair(dst, tm, fb, c0, c1, w.b);
+                        } else {
+                            tma_load_2d_pair(dst, tm, fb, c0, c1);
+                        }
+                    };
                     if (args.a_kmajor) {
-                        tma_load(&tmA, args.a_3d, sa, fb, k0, m0, w.b);
+                        load(&tmA, args.a_3d, sa, k0, m0);
                     } else {
-                        tma_load(&tmA, args.a_3d, sa, fb, m0, k0, w.b);
-                        tma_load(&tmA, args.a_3d, sa + 8192, fb, m0 + 64, k0, w.b);
+                        load(&tmA, args.a_3d, sa, m0, k0);
+                        load(&tmA, args.a_3d, sa + 8192, m0 + 64, k0);
                     }
                     if (args.b_kmajor) {
-                        tma_load(&tmB, args.b_3d, sb, fb, k0, n0, w.b);
+                        load(&tmB, args.b_3d, sb, k0, n0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load(&tmB, args.b_3d, sb + j * 8192, fb, n0 + 64 * j, k0, w.b);
+                        for (int j = 0; j < BNL / 64; ++j) load(&tmB, args.b_3d, sb + j * 8192, n0 + 64 * j, k0);
                     }
                     ++it;
                 }
             }
-            if (!ok) {
+            if (!ok && rank == 0) {
                 // let the copies already issued land before shared memory is released
                 for (uint32_t i = (it > (uint32_t)S ? it - S : 0u); i < it; ++i)
                     drain_wait(smem_u32(&full_bar[i % S]), (i / S) & 1u);
@@ -307,11 +401,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 5) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (even CTA of a pair)
+        if (lane == 0 && rank == 0) {
             uint32_t it = 0, local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < args.total_units; u += gridDim.x, ++local) {
+            for (int u = cluster; ok && u < args.total_units; u += nclusters, ++local) {
                 const Unit w = decode_unit(args, u);
                 const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
                 if (!wait_bar(smem_u32(&tempty_bar[acc]), aph ^ 1u, watch, W_TMEM_EMPTY)) {
@@ -337,25 +431,56 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                                                           : smem_desc_sw128(sa + 2048 * k, 8192, 1024);
                         const uint64_t bd = args.b_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
                                                           : smem_desc_sw128(sb + 2048 * k, 8192, 1024);
-                        mma_f16_ss(d_tmem, ad, bd, args.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
+                        if (CG == 1)
+                            mma_f16_ss(d_tmem, ad, bd, args.idesc, accum);
+                        else
+                            mma_f16_ss_pair(d_tmem, ad, bd, args.idesc, accum);
                     }
-                    mma_commit(smem_u32(&empty_bar[stage]));
+                    if (CG == 1)
+                        mma_commit(smem_u32(&empty_bar[stage]));
+                    else
+                        mma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
                     ++it;
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&tfull_bar[acc]));
+                if (CG == 1)
+                    mma_commit(smem_u32(&tfull_bar[acc]));
+                else
+                    mma_commit_pair(smem_u32(&tfull_bar[acc]), (uint16_t)0x3);
             }
             if (!ok) {
-                mma_commit(smem_u32(drain_bar));
+                if (CG == 1)
+                    mma_commit(smem_u32(drain_bar));
+                else
+                    mma_commit_pair(smem_u32(drain_bar), (uint16_t)0x1);
                 drain_wait(smem_u32(drain_bar), 0);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue warps 0-3
-        uint32_t local = 0;
-        const int row_in_tile = warp * 32 + lane;
-        for (int u = blockIdx.x; u < args.total_units; u += gridDim.x, ++local) {
+        uint32_t local = 0, ebuf = 0;
+        const int row_in_tile = (int)rank * BM + warp * 32 + lane;
+        uint8_t *my_stage = cstage + warp * 2 * EPI_STAGE_BYTES;
+        // alpha/beta, then the chunk to C (TMA store when C allows it)
+        auto emit = [&](int b, long long row, long long col0, float (&v)[32]) {
+            apply_alpha_beta(args, b, row, col0, v);
+            if (args.c_tma) {
+                // buffers alternate over the stores actually issued, so a
+                // buffer is reused only after one newer store was committed
+                const long long row0 = row - lane;
+                if (row0 < args.M && col0 < args.N) {
+                    store_tma(args, &tmC, my_stage + ebuf * EPI_STAGE_BYTES, lane, b, row0, col0, v);
+                    ebuf ^= 1u;
+                }
+            } else {
+                store_direct(args, b, row, col0, v);
+            }
+        };
+        const uint32_t tempty_leader0 = CG == 2 ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
+        const uint32_t tempty_leader1 = CG == 2 ? mapa_shared(smem_u32(&tempty_bar[1]), 0) : 0u;
+        for (int u = cluster; u < args.total_units; u += nclusters, ++local) {
             const Unit w = decode_unit(args, u);
             const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
             bool ok = wait_bar(smem_u32(&tfull_bar[acc]), aph, watch, W_TMEM_FULL);
@@ -363,107 +488,180 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * ACC_STRIDE;
-            const long long row = (long long)w.tm * BM + row_in_tile;
+            const long long row = (long long)w.tm * (BM * CG) + row_in_tile;
+            // accumulator fully read: hand it back to the MMA warp
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 1)
+                        mbar_arrive(smem_u32(&tempty_bar[acc]));
+                    else
+                        mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+                }
+            };
 
-            if (args.split_k == 1) {
+            if (w.S == 1) {
 #pragma unroll 1
                 for (int c = 0; c < CHUNKS; ++c) {
                     uint32_t r[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(taddr + c * 32, r);
                     tmem_ld_wait();
-                    if (c == CHUNKS - 1) {
-                        // accumulator fully read: hand it back to the MMA warp
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&tempty_bar[acc]));
-                    }
+                    if (c == CHUNKS - 1) release();
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    store_row_chunk(args, w.b, row, (long long)w.tn * BN + c * 32, v);
+                    emit(w.b, row, (long long)w.tn * BN + c * 32, v);
                 }
             } else {
-                // split-K: park this slice's partial tile (this warp's 32 rows),
-                // column-interleaved so each store instruction is coalesced
-                const long long tile_id = (long long)w.b * args.tiles_per_batch + w.tile;
+                // K slices: park this slice's partial tile (this warp's 32
+                // rows), column-interleaved so each store instruction is
+                // coalesced; the last slice to arrive sums them in slice order
                 const size_t slab = (size_t)BN * 32;          // floats per warp quarter
-                float *mine = args.ws + ((size_t)(tile_id * args.split_k + w.s) * 4 + warp) * slab;
+                auto slot = [&](int unit) {
+                    return args.ws + (((size_t)(unit - args.split_base) * CG + rank) * 4 + warp) * slab;
+                };
+                float *mine = slot(w.ufirst + w.s);
 #pragma unroll 1
                 for (int c = 0; c < CHUNKS; ++c) {
                     uint32_t r[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(taddr + c * 32, r);
                     tmem_ld_wait();
-                    if (c == CHUNKS - 1) {
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&tempty_bar[acc]));
-                    }
+                    if (c == CHUNKS - 1) release();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(c * 32 + j) * 32 + lane, __uint_as_float(r[j]));
                 }
                 __threadfence();
                 __syncwarp();
                 unsigned old = 0;
-                unsigned *ticket = args.tickets + tile_id * 4 + warp;
+                unsigned *ticket = args.tickets + ((size_t)w.tile * CG + rank) * 4 + warp;
                 if (lane == 0) old = atomicAdd(ticket, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (unsigned)(args.split_k - 1)) {
-                    // last slice to arrive: sum the slices in the fixed order 0..S-1
+                if (old == (unsigned)(w.S - 1)) {
                     __threadfence();
-                    const float *first = args.ws + ((size_t)(tile_id * args.split_k) * 4 + warp) * slab;
-                    const size_t sstride = (size_t)4 * slab;
 #pragma unroll 1
                     for (int c = 0; c < CHUNKS; ++c) {
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                        for (int s = 0; s < args.split_k; ++s) {
-                            const float *p = first + s * sstride + (size_t)(c * 32) * 32 + lane;
+                        for (int s = 0; s < w.S; ++s) {
+                            const float *p = slot(w.ufirst + s) + (size_t)(c * 32) * 32 + lane;
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] += __ldcg(p + j * 32);
                         }
-                        store_row_chunk(args, w.b, row, (long long)w.tn * BN + c * 32, v);
+                        emit(w.b, row, (long long)w.tn * BN + c * 32, v);
                     }
                     if (lane == 0) *ticket = 0u;       // ready for the next launch
                 }
             }
         }
+        // every TMA store has finished before shared memory is released
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (CG == 2) cluster_sync();     // no CTA leaves while its peer may still signal it
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem_base, TCOLS);
+    if (warp == 0) {
+        if (CG == 1)
+            tmem_dealloc(tmem_base, TCOLS);
+        else
+            tmem_dealloc_pair(tmem_base, TCOLS);
+    }
 }
 
-template <int BN>
-cudaError_t launch_bn(const MmaLaunch &L, cudaStream_t st)
+template <int BN, int CG>
+cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st)
 {
-    constexpr int smem = mma_smem_bytes(BN);
+    constexpr int smem = mma_smem_bytes(BN, CG);
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(mma_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(mma_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
+        if (CG == 2) {
+            e = cudaFuncSetAttribute(mma_kernel<BN, CG>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            if (e != cudaSuccess) return e;
+        }
         configured[dev] = true;
     }
-    mma_kernel<BN><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.args);
-    return cudaGetLastError();
+    if (CG == 1) {
+        mma_kernel<BN, CG><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.args);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid, 1, 1);
+    cfg.blockDim = dim3(MMA_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG>, L.tmA, L.tmB, L.tmC, L.args);
+}
+
+template <int BN>
+int pairs_for()
+{
+    constexpr int smem = mma_smem_bytes(BN, 2);
+    if (cudaFuncSetAttribute(mma_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(MMA_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<BN, 2>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
+    if (L.cg == 2) {
+        switch (L.bn) {
+        case 128: return launch_kernel<128, 2>(L, st);
+        case 256: return launch_kernel<256, 2>(L, st);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (L.bn) {
-    case 64: return launch_bn<64>(L, st);
-    case 128: return launch_bn<128>(L, st);
-    case 192: return launch_bn<192>(L, st);
-    case 256: return launch_bn<256>(L, st);
+    case 64: return launch_kernel<64, 1>(L, st);
+    case 128: return launch_kernel<128, 1>(L, st);
+    case 192: return launch_kernel<192, 1>(L, st);
+    case 256: return launch_kernel<256, 1>(L, st);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_active_pairs(int bn)
+{
+    switch (bn) {
+    case 128: return pairs_for<128>();
+    case 256: return pairs_for<256>();
+    default: return 0;
     }
 }
 

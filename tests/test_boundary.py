@@ -148,7 +148,7 @@ def test_plan_fp32_goes_to_ffma():
 
 def test_plan_tensor_core_shapes():
     p = plan(4096, 4096, 4096, "bf16", "bf16")
-    assert p.startswith("tcgen05_nn_bf16_bf16_128x") and "split" not in p and "pack" not in p
+    assert p.startswith("tcgen05_nn_bf16_bf16_256x256_pair") and "split" not in p and "pack" not in p
     assert plan(4096, 4096, 8192, "bf16", "f32", ta=True).startswith("tcgen05_tn_bf16_f32")
     assert plan(4096, 4096, 8192, "bf16", "f32", tb=True).startswith("tcgen05_nt_bf16_f32")
 
@@ -158,6 +158,12 @@ def test_plan_split_k_for_tall_k():
     assert "_splitk" in p and p.startswith("tcgen05_tn_bf16_f32_128x128")
     s = int(p.rsplit("_s", 1)[1])
     assert 2 <= s <= 152 // 4
+
+
+def test_plan_tail_split():
+    # 256 tiles of 256x256 on 76 CTA pairs: 3 whole waves, the last 28 tiles in 2 K slices
+    assert plan(4096, 4096, 4096, "bf16", "bf16") == "tcgen05_nn_bf16_bf16_256x256_pair_tail28x2"
+    assert "tail" not in plan(2048, 2048, 2048, "bf16", "bf16")       # one wave
 
 
 def test_plan_narrow_n():

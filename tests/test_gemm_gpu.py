@@ -118,7 +118,10 @@ def test_alpha_beta(ctx, alpha, beta, c):
 
 @pytest.mark.parametrize("spec", ["bn=64", "bn=128", "bn=192", "bn=256", "bn=128 split=3",
                                   "bn=256 split=7", "bn=64 split=16", "pack=1", "pack=1 split=5",
-                                  "grid=3", "group_m=1", "group_m=3 bn=64"])
+                                  "grid=3", "group_m=1", "group_m=3 bn=64", "sms=5 tail=2",
+                                  "sms=5 tail=3 bn=64", "sms=7 bn=256 tail=2 pack=1", "cg=2",
+                                  "cg=2 bn=128", "cg=2 sms=6 tail=2", "cg=2 grid=1 pack=1",
+                                  "store=direct", "store=direct cg=2 sms=6 tail=2", "store=direct split=3"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_forced_variants(ctx, force, spec, ta, tb):
     force(spec)
@@ -144,7 +147,8 @@ def test_padded_leading_dimensions(ctx):
 
 # ----------------------------------------------------- exactness and edges
 
-@pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "pack=1 bn=256 split=2"])
+@pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "pack=1 bn=256 split=2",
+                                  "sms=5 tail=3", "cg=2", "cg=2 bn=128 sms=4 tail=2", "store=direct"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
     """Integer entries in [-4,4], K=2048: every partial sum is an integer
@@ -199,7 +203,7 @@ def test_identity_and_permutation(ctx):
     assert torch.equal(out, p.B.float()[perm])
 
 
-@pytest.mark.parametrize("spec", ["", "bn=128 split=6"])
+@pytest.mark.parametrize("spec", ["", "bn=128 split=6", "sms=9 tail=2", "cg=2 sms=8 tail=2"])
 def test_determinism(ctx, force, spec):
     force(spec)
     p = synthetic.make_problem(384, 512, 4096, "bf16", "f32", transpose_a=True, seed=53, dist="normal")
