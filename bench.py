@@ -133,19 +133,19 @@ def dist_env():
 
 def cpu_baseline(target_s: float = 12.0):
     """The CPU oracle, as it stands, on a band of output rows of the same
-    workload (bounded to ~target_s seconds)."""
+    workload, grown until one run takes about target_s seconds."""
     import oracle
     import synthetic
     p = synthetic.bf16_nn_4096()
     lib = oracle.load_library()
-    t0 = time.perf_counter()
-    rows = 4
-    oracle.gemm(p, 0, rows, lib=lib)
-    dt = time.perf_counter() - t0
-    rows = int(max(4, min(M, rows * target_s / max(dt, 1e-3))))
-    t0 = time.perf_counter()
-    oracle.gemm(p, 0, rows, lib=lib)
-    dt = time.perf_counter() - t0
+    rows = 16
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm(p, 0, rows, lib=lib)
+        dt = time.perf_counter() - t0
+        if dt >= 0.8 * target_s or rows >= M:
+            break
+        rows = int(min(M, max(2 * rows, rows * target_s / max(dt, 1e-3))))
     flops = 2.0 * rows * N * K
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(lib),
             "kind": "oracle", "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} problem ({dt:.1f} s)",
