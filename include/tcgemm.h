@@ -58,11 +58,12 @@ typedef enum {
     TC_ERR_SCALAR = 5,             /* alpha or beta not finite */
     TC_ERR_OVERLAP = 6,            /* C's byte range overlaps A's or B's */
     TC_ERR_OVERFLOW = 7,           /* an element or byte count overflows int64 */
-    TC_ERR_ALIGN_UNSUPPORTED = 8,  /* reserved: every valid input has a kernel */
+    TC_ERR_ALIGN_UNSUPPORTED = 8,  /* only from tc_gemm_splitk_noalloc: operands TMA cannot read in place */
     TC_ERR_CUDA = 9,               /* a CUDA runtime error (launch, copy, no device) */
     TC_ERR_DEVICE_TIMEOUT = 10,    /* a kernel's bounded wait expired; it stopped early */
     TC_ERR_STRIDE = 11,            /* batched: negative stride */
-    TC_ERR_VARIANT = 12            /* a forced variant cannot serve this problem */
+    TC_ERR_VARIANT = 12,           /* a forced variant cannot serve this problem */
+    TC_ERR_SCRATCH = 13            /* tc_gemm_splitk_noalloc: more scratch than its static buffer holds */
 } tc_status_t;
 
 /* tensorcore gemm.md, "Surface": the GEMM descriptor, field for field. */
@@ -131,6 +132,42 @@ tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d,
  * context.  Pinned host memory gives full copy bandwidth. */
 tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
                          const void *B_host, void *C_host);
+
+/* Split-K GEMM that allocates nothing.  The paper has no counterpart to
+ * this call; it exists for callers that cannot allocate device memory: code
+ * in a process whose device memory is owned by another allocator with a
+ * fixed budget (a framework's caching allocator, a plugin handed only its
+ * inputs and outputs), and latency-critical paths that cannot afford the
+ * device-wide synchronisation cudaMalloc and cudaFree imply.  It needs no
+ * context either (creating one allocates).
+ *
+ * It runs the tensor-core kernel in its split-K form (128 x 128 output tiles,
+ * K cut into `split` slices whose fp32 partial tiles are summed in slice
+ * order, so results are deterministic and equal to tc_gemm's split-K
+ * variant).  The partial tiles and arrival counters live in one file-scope
+ * device array of 16 MiB + 16 KiB that every GPU which loads this library
+ * holds until the process exits.  Limits: split * ceil(M/128) * ceil(N/128)
+ * * 64 KiB <= 16 MiB and ceil(M/128) * ceil(N/128) <= 1024 whenever
+ * split > 1, else TC_ERR_SCRATCH (nothing is launched).  split = 0 picks
+ * the slice count from the SM count (always within the limits on GB300).
+ *
+ * Arguments: d, A, B, C as for tc_gemm_async (device pointers, caller
+ * owned); cuda_stream is a cudaStream_t (NULL = legacy default stream).
+ * Only f16/bf16 operands (TC_ERR_DTYPE for f32), with 16-byte aligned bases
+ * and leading dimensions that are multiples of 8 elements
+ * (TC_ERR_ALIGN_UNSUPPORTED otherwise: repacking would need scratch sized
+ * by the operands).  The call is asynchronous: it clears the counters with
+ * cudaMemsetAsync and launches on cuda_stream; a device-side wait timeout
+ * is not reported by this call.
+ *
+ * Every call, on any stream, shares the one array and it keeps the last
+ * call's contents: calls whose kernels overlap on the GPU race and corrupt
+ * each other's results; serialise them (one stream, or events).  The first
+ * call on each device performs set-up (it looks up the array's device
+ * address and the TMA encoder and sets the kernel's shared-memory limit);
+ * make that first call before any stream capture. */
+tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const void *B, void *C, int split,
+                                   void *cuda_stream);
 
 /* Host-only checks, no device needed: the same validation every call runs
  * first.  A, B, C are only compared as addresses (overlap), never read. */

@@ -32,6 +32,7 @@ STATUS = {
     0: "TC_OK", 1: "TC_ERR_NULL", 2: "TC_ERR_DIM", 3: "TC_ERR_LD", 4: "TC_ERR_DTYPE",
     5: "TC_ERR_SCALAR", 6: "TC_ERR_OVERLAP", 7: "TC_ERR_OVERFLOW", 8: "TC_ERR_ALIGN_UNSUPPORTED",
     9: "TC_ERR_CUDA", 10: "TC_ERR_DEVICE_TIMEOUT", 11: "TC_ERR_STRIDE", 12: "TC_ERR_VARIANT",
+    13: "TC_ERR_SCRATCH",
 }
 for _code, _name in STATUS.items():
     globals()[_name] = _code
@@ -86,6 +87,7 @@ def _load():
         "tc_gemm_grouped_async": (st, [vp, ctypes.c_int, D, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                        ctypes.POINTER(vp), vp]),
         "tc_gemm_host": (st, [vp, D, vp, vp, vp]),
+        "tc_gemm_splitk_noalloc": (st, [D, vp, vp, vp, ctypes.c_int, vp]),
         "tc_gemm_validate": (st, [D, vp, vp, vp]),
         "tc_gemm_batched_validate": (st, [BD, vp, vp, vp]),
         "tc_gemm_plan": (st, [D, vp, vp, vp, ctypes.c_int, ctypes.c_char_p, ctypes.c_size_t]),
@@ -104,7 +106,8 @@ _lib = _load()
 EXPORTED = (
     "tc_ctx_create", "tc_ctx_destroy", "tc_stream_create", "tc_stream_wrap", "tc_stream_sync",
     "tc_stream_handle", "tc_stream_destroy", "tc_gemm", "tc_gemm_async", "tc_gemm_batched",
-    "tc_gemm_batched_async", "tc_gemm_grouped_async", "tc_gemm_host", "tc_gemm_validate",
+    "tc_gemm_batched_async", "tc_gemm_grouped_async", "tc_gemm_host", "tc_gemm_splitk_noalloc",
+    "tc_gemm_validate",
     "tc_gemm_batched_validate", "tc_gemm_plan", "tc_last_kernel", "tc_launch_count",
     "tc_status_string",
 )
@@ -281,6 +284,17 @@ def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):
             raise ValueError("tc_gemm_host takes host tensors")
     _check(_lib.tc_gemm_host(ctx.ptr, ctypes.byref(d), _addr(A_host), _addr(B_host), _addr(C_host)),
            "tc_gemm_host")
+
+
+def tc_gemm_splitk_noalloc(d: tc_gemm_desc, A, B, C, split: int = 0, torch_stream=None):
+    """Split-K GEMM whose scratch is the library's static device buffer:
+    nothing is allocated (for callers that must not allocate device memory;
+    see include/tcgemm.h).  Asynchronous on ``torch_stream`` (default: the
+    legacy default stream); calls that overlap on the GPU race."""
+    _check_capacity(d, A, B, C)
+    handle = torch_stream.cuda_stream if torch_stream is not None else 0
+    _check(_lib.tc_gemm_splitk_noalloc(ctypes.byref(d), _addr(A), _addr(B), _addr(C), int(split),
+                                       ctypes.c_void_p(handle)), "tc_gemm_splitk_noalloc")
 
 
 def tc_gemm_validate(d: tc_gemm_desc, A=1 << 20, B=2 << 40, C=3 << 40) -> int:

@@ -588,6 +588,7 @@ const char *tc_status_string(tc_status_t st)
     case TC_ERR_DEVICE_TIMEOUT: return "device wait timed out; the kernel stopped early";
     case TC_ERR_STRIDE: return "invalid batch stride";
     case TC_ERR_VARIANT: return "forced variant cannot serve this problem";
+    case TC_ERR_SCRATCH: return "problem needs more scratch than the static buffer of tc_gemm_splitk_noalloc holds";
     }
     return "unknown status";
 }
@@ -792,6 +793,103 @@ tc_status_t tc_gemm_plan(const tc_gemm_desc *d, const void *A, const void *B, co
     Plan p;
     if ((st = make_plan(d, n, A, B, num_sms, &p)) != TC_OK) return st;
     std::snprintf(buf, len, "%s", p.name.c_str());
+    return TC_OK;
+}
+
+tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const void *B, void *C, int split,
+                                   void *cuda_stream)
+{
+    Norm n;
+    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n);
+    if (st != TC_OK) return st;
+    if (d->a_dtype == TC_F32) return TC_ERR_DTYPE;
+    if (split < 0) return TC_ERR_DIM;
+    if (!aligned16(A) || !aligned16(B) || n.lda % 8 != 0 || n.ldb % 8 != 0) return TC_ERR_ALIGN_UNSUPPORTED;
+
+    constexpr int bn = 128;
+    const int64_t tiles = cdiv(d->M, BM) * cdiv(d->N, bn);
+    const int64_t num_kb = cdiv(d->K, BK);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return TC_ERR_CUDA;
+    int64_t S = split;
+    if (S == 0) S = std::max<int64_t>(1, std::min<int64_t>(sms / std::max<int64_t>(tiles, 1), num_kb / 4));
+    S = std::min<int64_t>(S, num_kb);
+    if (S > 1 && (tiles * S * BM * bn * (int64_t)sizeof(float) > (int64_t)NOALLOC_PARTIAL_BYTES ||
+                  tiles * 4 > (int64_t)NOALLOC_TICKETS))
+        return TC_ERR_SCRATCH;
+    if (tiles * S > INT32_MAX / 2) return TC_ERR_OVERFLOW;
+
+    NoallocScratch scratch;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return TC_ERR_CUDA;
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 encoder = nullptr;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encoder = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!encoder) return TC_ERR_CUDA;
+    tc_ctx enc;                 // carries only the encoder for encode_map; owns nothing
+    enc.encode = encoder;
+
+    MmaLaunch L{};
+    L.bn = bn;
+    L.cg = 1;
+    L.grid = (int)std::min<int64_t>(tiles * S, sms);
+    MmaArgs &a = L.args;
+    a.M = d->M;
+    a.N = d->N;
+    a.K = d->K;
+    a.num_kb = (int)num_kb;
+    a.tiles_m = (int)cdiv(d->M, BM);
+    a.tiles_n = (int)cdiv(d->N, bn);
+    a.tiles_per_batch = (int)tiles;
+    a.batch = 1;
+    a.seg0_tiles = (int)tiles;
+    a.seg0_split = (int)S;
+    a.seg1_split = 1;
+    a.split_base = 0;
+    a.total_units = (int)(tiles * S);
+    a.group_m = 4;
+    a.a_kmajor = !d->transpose_a;
+    a.b_kmajor = d->transpose_b;
+    const uint32_t fmt = d->a_dtype == TC_BF16 ? 1u : 0u;
+    a.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(!a.a_kmajor) << 15) |
+              ((uint32_t)(!a.b_kmajor) << 16) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    a.alpha = d->alpha;
+    a.beta = d->beta;
+    a.C = C;
+    a.ldc = n.ldc;
+    a.c_dtype = d->c_dtype;
+    const int64_t ec = (int64_t)elem_size(d->c_dtype);
+    a.c_vec_ok = aligned16(C) && (n.ldc * ec) % 16 == 0;
+    a.c_tma = a.c_vec_ok;
+    a.ws = S > 1 ? scratch.partials : nullptr;
+    a.tickets = S > 1 ? scratch.tickets : nullptr;
+    a.status = scratch.status;
+    a.timeout_ns = 4000000000ull + (unsigned long long)num_kb * 20000ull;
+
+    bool ok = a.a_kmajor ? encode_map(&enc, &L.tmA, d->a_dtype, A, d->K, d->M, n.lda, false, 1, 0, 64, BM)
+                         : encode_map(&enc, &L.tmA, d->a_dtype, A, d->M, d->K, n.lda, false, 1, 0, 64, 64);
+    if (ok)
+        ok = a.b_kmajor ? encode_map(&enc, &L.tmB, d->a_dtype, B, d->K, d->N, n.ldb, false, 1, 0, 64, bn)
+                        : encode_map(&enc, &L.tmB, d->a_dtype, B, d->N, d->K, n.ldb, false, 1, 0, 64, 64);
+    if (ok && a.c_tma)
+        ok = encode_map(&enc, &L.tmC, d->c_dtype, C, d->N, d->M, n.ldc, false, 1, 0, 32, 32,
+                        d->c_dtype == TC_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return TC_ERR_CUDA;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    // the counters must start at zero; the partial tiles are fully overwritten
+    if (S > 1 && cudaMemsetAsync(scratch.tickets, 0, (size_t)tiles * 4 * sizeof(unsigned), stream) != cudaSuccess)
+        return TC_ERR_CUDA;
+    if (cudaMemsetAsync(scratch.status, 0, sizeof(unsigned), stream) != cudaSuccess) return TC_ERR_CUDA;
+    if (launch_mma(L, stream) != cudaSuccess) return TC_ERR_CUDA;
     return TC_OK;
 }
 

@@ -85,6 +85,21 @@ cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st);
 // resident at once on the current device (0 if the pair kernel cannot run).
 int max_active_pairs(int bn);
 
+// Static scratch of the entry point that allocates nothing: split-K partial
+// tiles (at most NOALLOC_PARTIAL_BYTES), arrival counters (4 per output tile,
+// at most NOALLOC_TICKETS) and one status word.
+constexpr size_t NOALLOC_PARTIAL_BYTES = size_t(16) << 20;
+constexpr size_t NOALLOC_TICKETS = 4096;
+constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_PARTIAL_BYTES + NOALLOC_TICKETS * sizeof(unsigned) + 256;
+struct NoallocScratch {
+    float *partials;
+    unsigned *tickets;
+    unsigned *status;
+};
+// Device addresses of the static scratch on the current device (looked up
+// once per device).
+cudaError_t noalloc_scratch(NoallocScratch *out);
+
 // fp32 FFMA kernel (exact fp32, ascending-k fused multiply-add chain)
 struct FfmaArgs {
     int M, N, K;

@@ -38,6 +38,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 namespace tc {
 namespace {
 
@@ -654,6 +656,38 @@ cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
     case 256: return launch_kernel<256, 1>(L, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// ---------------------------------------------------------------- static scratch
+// Scratch of the entry point that allocates nothing (tc_gemm_splitk_noalloc):
+// a file-scope device array, zero at load, held by every GPU that loads this
+// library until the process exits.  Layout: split-K partial tiles, then the
+// arrival counters, then a status word.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+cudaError_t noalloc_scratch(NoallocScratch *out)
+{
+    // The array's name is only a host-side stand-in: its device address is
+    // looked up once per device, with that device current.
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (!ptr) return cudaErrorInvalidSymbol;
+        addr[dev] = ptr;
+    }
+    unsigned char *base = static_cast<unsigned char *>(addr[dev]);
+    out->partials = reinterpret_cast<float *>(base);
+    out->tickets = reinterpret_cast<unsigned *>(base + NOALLOC_PARTIAL_BYTES);
+    out->status = reinterpret_cast<unsigned *>(base + NOALLOC_PARTIAL_BYTES + NOALLOC_TICKETS * sizeof(unsigned));
+    return cudaSuccess;
 }
 
 int max_active_pairs(int bn)
