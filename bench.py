@@ -34,9 +34,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 M = N = K = 4096
+HEADLINE = "bf16_nn_4096"
 WORKLOAD = "bf16 NN GEMM M=N=K=4096, bf16 out, fp32 accumulate, alpha=1 beta=0, normal(0,1) from seed 1"
 METRIC = "GEMM TFLOP/s (2MNK/t) bf16 4096^3 NN"
 PAGES_BASELINE = 29.0     # TFLOP/s, bf16 4096^3 NN, Apple M5 Pro (tessl architecture.md, column-panel swizzle)
+PAGES_REF = "29.0 TFLOP/s bf16 4096^3 NN on Apple M5 Pro (tessl architecture.md, Column-Panel Grid Swizzling)"
 FLOPS = 2.0 * M * N * K
 
 
@@ -184,12 +186,99 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------- workloads
+# Every named GEMM configuration: (name, problem factory, single GEMM or a
+# grouped batch).  The headline is bf16_nn_4096; the others are timed for
+# the per-workload roofline summary and can be run alone with --workload.
+
+def workload_registry():
+    import synthetic
+    reg = {
+        "bf16_nn_4096": lambda: [synthetic.bf16_nn_4096()],
+        "fp32_nn_256": lambda: [synthetic.fp32_nn_256()],
+        "bf16_tn_4096x4096x8192": lambda: [synthetic.bf16_tn_nt_4096x8192("TN")],
+        "bf16_nt_4096x4096x8192": lambda: [synthetic.bf16_tn_nt_4096x8192("NT")],
+        "bf16_tn_splitk_256x256x16384": lambda: [synthetic.bf16_tn_splitk_256x16384()],
+        "fp16_nn_8192x384x4096": lambda: [synthetic.fp16_nn_narrow_8192x384x4096()],
+        "fp16_ragged_64": lambda: synthetic.fp16_ragged(),
+    }
+    for n in synthetic.SQUARE_SIZES:
+        reg[f"fp16_nn_square_{n}"] = (lambda n=n: [synthetic.fp16_nn_square(n)])
+    return reg
+
+
+def ffma_peak_tflops(sms: int, mhz: float) -> float:
+    """fp32 FFMA peak: SMs x 128 fp32 lanes x 2 flop x SM clock."""
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def roofline(probs, seconds, sms):
+    """Algorithmic flops/bytes of a step against the measured peaks: the
+    bound is whichever of compute and HBM traffic takes longer."""
+    burst, _sustained, hbm, src = peaks()
+    es = {"f16": 2, "bf16": 2, "f32": 4}
+    flops = sum(2.0 * p.M * p.N * p.K for p in probs)
+    nbytes = sum(p.M * p.K * es[p.ab_dtype] + p.K * p.N * es[p.ab_dtype] +
+                 p.M * p.N * es[p.c_dtype] * (2 if p.beta != 0 else 1) for p in probs)
+    fp32 = probs[0].ab_dtype == "f32"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = json.load(f).get("sm_max_mhz", 2070.0)
+    except Exception:
+        mhz = 2070.0
+    peak_c = ffma_peak_tflops(sms, mhz) if fp32 else burst
+    t_c = flops / (peak_c * 1e12)
+    t_m = nbytes / (hbm * 1e9)
+    if t_c >= t_m:
+        bound, achieved, peak, unit = ("alu" if fp32 else "tensor"), flops / seconds / 1e12, peak_c, "TFLOP/s"
+    else:
+        bound, achieved, peak, unit = "hbm", nbytes / seconds / 1e9, hbm, "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "flops_per_step": flops, "bytes_per_step": nbytes,
+            "peak_source": (f"{src}: " + ("FFMA lanes x clock (derived)" if fp32 else
+                                          "bf16 dense burst" if bound != "hbm" else "HBM copy"))}
+
+
+class Runner:
+    """Device-resident operands of one workload and its launch."""
+
+    def __init__(self, tg, ctx, stream, probs):
+        self.tg, self.ctx, self.stream, self.probs = tg, ctx, stream, probs
+        self.A = [p.A.cuda() for p in probs]
+        self.B = [p.B.cuda() for p in probs]
+        self.C = [p.C.cuda() for p in probs]
+        self.d = [tg.make_desc(p.M, p.N, p.K, p.ab_dtype, p.c_dtype, transpose_a=p.transpose_a,
+                               transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta) for p in probs]
+
+    def step(self):
+        tg = self.tg
+        if len(self.probs) == 1:
+            tg.tc_gemm_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.stream)
+        else:
+            tg.tc_gemm_grouped_async(self.ctx, self.d, self.A, self.B, self.C, self.stream)
+
+
+def time_steps(torch, runner, tstream, flush, steps, warmup):
+    for _ in range(warmup):
+        flush.zero_()
+        runner.step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(tstream)
+        runner.step()
+        ends[i].record(tstream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     import matrix_multiply_gb300 as tg
-    import synthetic
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -203,19 +292,18 @@ def run_ours(args):
     ctx = tg.Context(local)
     tstream = torch.cuda.current_stream()
     stream = tg.Stream(ctx, torch_stream=tstream)
-    p = synthetic.bf16_nn_4096()
-    A, B = p.A.cuda(), p.B.cuda()
-    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    d = tg.make_desc(M, N, K, "bf16", "bf16")
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
-
-    def step():
-        tg.tc_gemm_async(ctx, d, A, B, C, stream)
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    flush = torch.empty(max(2 * props.L2_cache_size, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    reg = workload_registry()
+    name = args.workload
+    probs = reg[name]()
+    runner = Runner(tg, ctx, stream, probs)
+    flops = sum(2.0 * p.M * p.N * p.K for p in probs)
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        runner.step()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -228,7 +316,7 @@ def run_ours(args):
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(tstream)
-            step()
+            runner.step()
             ends[i].record(tstream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -244,24 +332,31 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = world * FLOPS * args.steps / (total_ms / 1e3) / 1e12
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
 
     # end to end through the host-buffer ABI call (copies inside the timed region)
-    Ah, Bh = p.A.pin_memory(), p.B.pin_memory()
-    Ch = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
-    for _ in range(2):
-        tg.tc_gemm_host(ctx, d, Ah, Bh, Ch)
-    e2e_steps = max(5, min(args.steps, 30))
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        tg.tc_gemm_host(ctx, d, Ah, Bh, Ch)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_ms = e2e_s * 1e3
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * FLOPS / (e2e_ms / 1e3) / 1e12
+    e2e = None
+    if len(probs) == 1:
+        p = probs[0]
+        Ah, Bh, Ch = p.A.pin_memory(), p.B.pin_memory(), p.C.clone().pin_memory()
+        d = runner.d[0]
+        for _ in range(2):
+            tg.tc_gemm_host(ctx, d, Ah, Bh, Ch)
+        e2e_steps = max(5, min(args.steps, 30))
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            tg.tc_gemm_host(ctx, d, Ah, Bh, Ch)
+        e2e_ms = (time.perf_counter() - t0) / e2e_steps * 1e3
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        es = {"f16": 2, "bf16": 2, "f32": 4}
+        e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (p.M * p.K + p.K * p.N) * es[p.ab_dtype] +
+               (p.M * p.N * es[p.c_dtype] if p.beta != 0 else 0),
+               "d2h_bytes_per_step": p.M * p.N * es[p.c_dtype], "ms_per_step": e2e_ms,
+               "call": "tc_gemm_host (pinned host A, B, C)"}
 
     if world > 1:
         dist.barrier()
@@ -270,31 +365,31 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    burst, sustained, hbm, src = peaks()
-    achieved = FLOPS / (statistics.mean(ms) / 1e3) / 1e12
-    traffic = profile_traffic(kernel_source_hash())
+    rl = roofline(probs, statistics.mean(ms) / 1e3, sms)
+    rl["traffic"] = profile_traffic(kernel_source_hash()) if name == HEADLINE else None
+    p0 = probs[0]
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if name == HEADLINE else f"GEMM TFLOP/s (2MNK/t) {name}",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": value / (world * PAGES_BASELINE), "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "layout": "NN",
-                   "global_batch": 1, "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "variant": kernel,
-                   "l2": "flushed before every step (write of >= 2x L2); flush outside the timed events",
-                   "vs_baseline_ref": "29.0 TFLOP/s bf16 4096^3 NN on Apple M5 Pro (tessl architecture.md)"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
-                     "frac": achieved / burst, "traffic": traffic,
-                     "peak_source": f"{src} bf16 dense burst (MEASURED_PEAKS.json)" if src == "measured"
-                     else "fallback 1.9 PFLOP/s"},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * (M * K + K * N),
-                "d2h_bytes_per_step": 2 * M * N, "ms_per_step": e2e_ms,
-                "call": "tc_gemm_host (pinned host A, B, C)"},
+        "scaling": "weak",
+        "vs_baseline": value / (world * PAGES_BASELINE) if name == HEADLINE else None,
+        "dtype": p0.ab_dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD if name == HEADLINE else name, "problems": len(probs),
+                   "M": p0.M, "N": p0.N, "K": p0.K, "layout": p0.layout, "global_batch": len(probs),
+                   "parallelism": f"replicas{world}" if world > 1 else "single", "variant": kernel,
+                   "l2": "flushed before every step (write of >= 2x L2); flush outside the timed events"},
+        "roofline": rl,
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
-    if not args.no_cpu_baseline and world >= 1:
+    if name == HEADLINE:
+        line["config"]["vs_baseline_ref"] = PAGES_REF
+    if args.summary and name == HEADLINE and world == 1:
+        line["workloads"] = summary(torch, tg, ctx, stream, tstream, flush, reg, sms)
+    if not args.no_cpu_baseline and name == HEADLINE:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
     stream.close()
@@ -304,6 +399,29 @@ def run_ours(args):
     return 0
 
 
+def summary(torch, tg, ctx, stream, tstream, flush, reg, sms):
+    """Every other named workload: TFLOP/s and roofline fraction, each timed
+    for about a third of a second of device time (cold L2 per step)."""
+    out = {}
+    for name, factory in reg.items():
+        if name == HEADLINE:
+            continue
+        probs = factory()
+        runner = Runner(tg, ctx, stream, probs)
+        probe = time_steps(torch, runner, tstream, flush, 3, 2)
+        steps = int(max(10, min(2000, 0.3e3 / max(statistics.mean(probe), 1e-3))))
+        ms = time_steps(torch, runner, tstream, flush, steps, 3)
+        t = statistics.mean(ms) / 1e3
+        flops = sum(2.0 * p.M * p.N * p.K for p in probs)
+        rl = roofline(probs, t, sms)
+        out[name] = {"tflops": flops / t / 1e12, "ms": t * 1e3, "steps": steps,
+                     "bound": rl["bound"], "achieved": rl["achieved"], "unit": rl["unit"],
+                     "frac": rl["frac"], "variant": ctx.last_kernel}
+        del runner
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -311,6 +429,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="which named workload to time (default: the headline bf16 NN 4096^3)")
+    ap.add_argument("--no-summary", dest="summary", action="store_false",
+                    help="skip the per-workload roofline summary of the other workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

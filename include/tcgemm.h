@@ -142,23 +142,23 @@ tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
  * context either (creating one allocates).
  *
  * It runs the tensor-core kernel in its split-K form (128 x 128 output tiles,
- * K cut into `split` slices whose fp32 partial tiles are summed in slice
- * order, so results are deterministic and equal to tc_gemm's split-K
- * variant).  The partial tiles and arrival counters live in one file-scope
- * device array of 16 MiB + 16 KiB that every GPU which loads this library
- * holds until the process exits.  Limits: split * ceil(M/128) * ceil(N/128)
- * * 64 KiB <= 16 MiB and ceil(M/128) * ceil(N/128) <= 1024 whenever
- * split > 1, else TC_ERR_SCRATCH (nothing is launched).  split = 0 picks
- * the slice count from the SM count (always within the limits on GB300).
+ * K cut into `split` slices) followed by the reduction kernel that sums the
+ * slices' fp32 partial tiles in slice order, so results are deterministic
+ * and equal to tc_gemm's split-K variant with the same slice count.  The
+ * partial tiles live in one file-scope device array of 16 MiB + 256 B that
+ * every GPU which loads this library holds until the process exits.  Limit:
+ * split * ceil(M/128) * ceil(N/128) * 64 KiB <= 16 MiB whenever split > 1,
+ * else TC_ERR_SCRATCH (nothing is launched).  split = 0 picks the slice
+ * count from the SM count (always within the limit on GB300).
  *
  * Arguments: d, A, B, C as for tc_gemm_async (device pointers, caller
  * owned); cuda_stream is a cudaStream_t (NULL = legacy default stream).
  * Only f16/bf16 operands (TC_ERR_DTYPE for f32), with 16-byte aligned bases
  * and leading dimensions that are multiples of 8 elements
  * (TC_ERR_ALIGN_UNSUPPORTED otherwise: repacking would need scratch sized
- * by the operands).  The call is asynchronous: it clears the counters with
- * cudaMemsetAsync and launches on cuda_stream; a device-side wait timeout
- * is not reported by this call.
+ * by the operands).  The call is asynchronous: it clears the array's status
+ * word with cudaMemsetAsync and launches on cuda_stream; a device-side wait
+ * timeout is not reported by this call.
  *
  * Every call, on any stream, shares the one array and it keeps the last
  * call's contents: calls whose kernels overlap on the GPU race and corrupt

@@ -28,8 +28,6 @@ struct tc_stream {
     bool owned = false;
     void *ws = nullptr;              // repacked operands + split-K partials
     size_t ws_cap = 0;
-    unsigned *tickets = nullptr;     // split-K arrival counters, kept at zero
-    size_t tickets_cap = 0;
     unsigned *status_host = nullptr; // mapped, pinned: kernels report timeouts here
     unsigned *status_dev = nullptr;
 };
@@ -339,24 +337,6 @@ tc_status_t ensure_ws(tc_stream *s, size_t bytes)
     return TC_OK;
 }
 
-tc_status_t ensure_tickets(tc_stream *s, size_t count)
-{
-    if (count <= s->tickets_cap) return TC_OK;
-    size_t cap = round_up(count, 4096);
-    if (s->tickets) {
-        if (cudaFreeAsync(s->tickets, s->st) != cudaSuccess) return TC_ERR_CUDA;
-        s->tickets = nullptr;
-        s->tickets_cap = 0;
-    }
-    if (cudaMallocAsync(reinterpret_cast<void **>(&s->tickets), cap * sizeof(unsigned), s->st) != cudaSuccess) {
-        s->tickets = nullptr;
-        return TC_ERR_CUDA;
-    }
-    if (cudaMemsetAsync(s->tickets, 0, cap * sizeof(unsigned), s->st) != cudaSuccess) return TC_ERR_CUDA;
-    s->tickets_cap = cap;
-    return TC_OK;
-}
-
 bool encode_map(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, int64_t inner, int64_t outer,
                 int64_t ld_elems, bool three_d, int64_t batch, int64_t bstride_elems, uint32_t box_inner,
                 uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
@@ -427,7 +407,6 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         p.split > 1 ? (size_t)(p.units - p.split_base) * BM * p.cg * p.bn * sizeof(float) : 0;
     tc_status_t st = ensure_ws(s, a_pack_bytes + b_pack_bytes + part_bytes + 256);
     if (st != TC_OK) return st;
-    if (p.split > 1 && (st = ensure_tickets(s, (size_t)p.tiles * p.cg * 4)) != TC_OK) return st;
     uint8_t *ws = static_cast<uint8_t *>(s->ws);
     const void *Ause = A, *Buse = B;
     int64_t sa = n.sa, sb = n.sb;
@@ -499,7 +478,6 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.c_tma = a.c_vec_ok && p.tma_store;
     a.c_3d = n.batch > 1;
     a.ws = p.split > 1 ? reinterpret_cast<float *>(ws + a_pack_bytes + b_pack_bytes) : nullptr;
-    a.tickets = p.split > 1 ? s->tickets : nullptr;
     a.status = s->status_dev;
     const int64_t kb_per_unit = a.num_kb;
     a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
@@ -521,9 +499,40 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     if (ok && a.c_tma)
         ok = encode_map(ctx, &L.tmC, d->c_dtype, C, d->N, d->M, n.ldc, a.c_3d, n.batch, a.stride_c, 32, 32,
                         d->c_dtype == TC_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    // split-K workspace: one row-major fp32 (BM*cg) x BN tile per K-slice unit
+    const int64_t rows_per_tile = (int64_t)BM * p.cg;
+    if (ok && a.ws)
+        ok = encode_map(ctx, &L.tmW, TC_F32, a.ws, p.bn, (p.units - p.split_base) * rows_per_tile, p.bn, false, 1,
+                        0, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return TC_ERR_CUDA;
     if ((e = launch_mma(L, s->st)) != cudaSuccess) return TC_ERR_CUDA;
     ++launches;
+    if (a.ws) {
+        ReduceArgs r{};
+        r.ws = a.ws;
+        r.rows_per_tile = (int)rows_per_tile;
+        r.bn = p.bn;
+        r.first_tile = (int)(p.seg0_split > 1 ? 0 : p.seg0_tiles);
+        r.ntiles = (int)(p.seg0_split > 1 ? p.seg0_tiles : p.tiles - p.seg0_tiles);
+        r.S = p.seg0_split > 1 ? p.seg0_split : p.seg1_split;
+        r.tiles_m = a.tiles_m;
+        r.tiles_n = a.tiles_n;
+        r.tiles_per_batch = a.tiles_per_batch;
+        r.group_m = a.group_m;
+        r.M = d->M;
+        r.N = d->N;
+        r.alpha = d->alpha;
+        r.beta = d->beta;
+        r.C = C;
+        r.ldc = n.ldc;
+        r.stride_c = a.stride_c;
+        r.c_dtype = d->c_dtype;
+        r.c_vec_ok = aligned16(C) && n.ldc % 4 == 0 && a.stride_c % 4 == 0;   // 4-element vectors
+        const int64_t work = (int64_t)r.ntiles * rows_per_tile * (p.bn / 4);
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), (int64_t)ctx->num_sms * 8));
+        if ((e = launch_reduce(r, grid, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        ++launches;
+    }
     ctx->launches += launches;
     ctx->last = p.name;
     return TC_OK;
@@ -560,7 +569,6 @@ void stream_free(tc_stream *s)
     if (!s) return;
     if (s->st) cudaStreamSynchronize(s->st);
     if (s->ws) cudaFree(s->ws);
-    if (s->tickets) cudaFree(s->tickets);
     if (s->status_host) cudaFreeHost(s->status_host);
     if (s->owned && s->st) cudaStreamDestroy(s->st);
     delete s;
@@ -816,8 +824,7 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
     int64_t S = split;
     if (S == 0) S = std::max<int64_t>(1, std::min<int64_t>(sms / std::max<int64_t>(tiles, 1), num_kb / 4));
     S = std::min<int64_t>(S, num_kb);
-    if (S > 1 && (tiles * S * BM * bn * (int64_t)sizeof(float) > (int64_t)NOALLOC_PARTIAL_BYTES ||
-                  tiles * 4 > (int64_t)NOALLOC_TICKETS))
+    if (S > 1 && tiles * S * BM * bn * (int64_t)sizeof(float) > (int64_t)NOALLOC_PARTIAL_BYTES)
         return TC_ERR_SCRATCH;
     if (tiles * S > INT32_MAX / 2) return TC_ERR_OVERFLOW;
 
@@ -870,7 +877,6 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
     a.c_vec_ok = aligned16(C) && (n.ldc * ec) % 16 == 0;
     a.c_tma = a.c_vec_ok;
     a.ws = S > 1 ? scratch.partials : nullptr;
-    a.tickets = S > 1 ? scratch.tickets : nullptr;
     a.status = scratch.status;
     a.timeout_ns = 4000000000ull + (unsigned long long)num_kb * 20000ull;
 
@@ -882,14 +888,40 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
     if (ok && a.c_tma)
         ok = encode_map(&enc, &L.tmC, d->c_dtype, C, d->N, d->M, n.ldc, false, 1, 0, 32, 32,
                         d->c_dtype == TC_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && a.ws)
+        ok = encode_map(&enc, &L.tmW, TC_F32, a.ws, bn, tiles * S * BM, bn, false, 1, 0, 32, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return TC_ERR_CUDA;
 
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    // the counters must start at zero; the partial tiles are fully overwritten
-    if (S > 1 && cudaMemsetAsync(scratch.tickets, 0, (size_t)tiles * 4 * sizeof(unsigned), stream) != cudaSuccess)
-        return TC_ERR_CUDA;
+    // the status word must start at zero; the partial tiles are fully overwritten
     if (cudaMemsetAsync(scratch.status, 0, sizeof(unsigned), stream) != cudaSuccess) return TC_ERR_CUDA;
     if (launch_mma(L, stream) != cudaSuccess) return TC_ERR_CUDA;
+    if (a.ws) {
+        ReduceArgs r{};
+        r.ws = a.ws;
+        r.rows_per_tile = BM;
+        r.bn = bn;
+        r.first_tile = 0;
+        r.ntiles = (int)tiles;
+        r.S = (int)S;
+        r.tiles_m = a.tiles_m;
+        r.tiles_n = a.tiles_n;
+        r.tiles_per_batch = a.tiles_per_batch;
+        r.group_m = a.group_m;
+        r.M = d->M;
+        r.N = d->N;
+        r.alpha = d->alpha;
+        r.beta = d->beta;
+        r.C = C;
+        r.ldc = n.ldc;
+        r.stride_c = 0;
+        r.c_dtype = d->c_dtype;
+        r.c_vec_ok = aligned16(C) && n.ldc % 4 == 0;   // 4-element vectors
+        const int64_t work = tiles * BM * (bn / 4);
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), (int64_t)sms * 8));
+        if (launch_reduce(r, grid, stream) != cudaSuccess) return TC_ERR_CUDA;
+    }
     return TC_OK;
 }
 

@@ -66,8 +66,7 @@ struct MmaArgs {
     int c_vec_ok;          // 16-byte vector loads/stores allowed on C
     int c_tma;             // C is written by TMA stores through the third descriptor
     int c_3d;              // that descriptor is 3-D (batch index third)
-    float *ws;             // split-K partial tiles
-    unsigned *tickets;     // split-K arrival counters (zero between launches)
+    float *ws;             // split-K partial tiles (written through the fourth descriptor)
     unsigned *status;      // device status word (0 = fine)
     unsigned long long timeout_ns;
 };
@@ -76,7 +75,7 @@ struct MmaLaunch {
     int bn;
     int cg;      // CTAs per tile: 1, or 2 for a CTA pair (cluster of two)
     int grid;    // CTAs (a multiple of cg)
-    CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmA, tmB, tmC, tmW;   // A, B, C and the split-K workspace
     MmaArgs args;
 };
 
@@ -85,15 +84,28 @@ cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st);
 // resident at once on the current device (0 if the pair kernel cannot run).
 int max_active_pairs(int bn);
 
+// Split-K reduction: tiles [first_tile, first_tile + ntiles) each have S
+// fp32 partial tiles (rows_per_tile x bn, row-major) at
+// ws + ((tile - first_tile) * S + s) * rows_per_tile * bn.
+struct ReduceArgs {
+    const float *ws;
+    int rows_per_tile, bn;
+    int first_tile, ntiles, S;
+    int tiles_m, tiles_n, tiles_per_batch, group_m;
+    int M, N;
+    float alpha, beta;
+    void *C;
+    long long ldc, stride_c;
+    int c_dtype, c_vec_ok;
+};
+cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st);
+
 // Static scratch of the entry point that allocates nothing: split-K partial
-// tiles (at most NOALLOC_PARTIAL_BYTES), arrival counters (4 per output tile,
-// at most NOALLOC_TICKETS) and one status word.
+// tiles (at most NOALLOC_PARTIAL_BYTES) and one status word.
 constexpr size_t NOALLOC_PARTIAL_BYTES = size_t(16) << 20;
-constexpr size_t NOALLOC_TICKETS = 4096;
-constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_PARTIAL_BYTES + NOALLOC_TICKETS * sizeof(unsigned) + 256;
+constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_PARTIAL_BYTES + 256;
 struct NoallocScratch {
     float *partials;
-    unsigned *tickets;
     unsigned *status;
 };
 // Device addresses of the static scratch on the current device (looked up

@@ -305,3 +305,20 @@ __device__ __forceinline__ void bulk_wait()
 }
 
 }  // namespace tc
+
+// ------------------------------------------------------------------ dependent launch
+
+namespace tc {
+
+// allow the next kernel in the stream (launched as a programmatic dependent)
+// to start launching
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// wait until the preceding kernel in the stream has completed and its
+// memory operations are visible (no-op without a programmatic dependency)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+}  // namespace tc

@@ -96,6 +96,22 @@ struct Unit {
     int ufirst;          // unit of slice 0 of this tile
 };
 
+// Linear tile id -> (batch entry, tile row, tile column): bands of group_m
+// tile rows, column-major inside a band.
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int tiles_per_batch, int group_m,
+                                            int &b, int &tm, int &tn)
+{
+    b = tile / tiles_per_batch;
+    const int t = tile - b * tiles_per_batch;
+    const int band = group_m * tiles_n;
+    const int g = t / band;
+    const int first_m = g * group_m;
+    const int rows_in_band = min(tiles_m - first_m, group_m);
+    const int in_band = t - g * band;
+    tm = first_m + in_band % rows_in_band;
+    tn = in_band / rows_in_band;
+}
+
 __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
 {
     Unit r;
@@ -112,16 +128,7 @@ __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
         r.S = a.seg1_split;
     }
     r.ufirst = u - r.s;
-    r.b = r.tile / a.tiles_per_batch;
-    const int t = r.tile - r.b * a.tiles_per_batch;
-    // bands of group_m tile rows, column-major inside a band
-    const int band = a.group_m * a.tiles_n;
-    const int g = t / band;
-    const int first_m = g * a.group_m;
-    const int rows_in_band = min(a.tiles_m - first_m, a.group_m);
-    const int in_band = t - g * band;
-    r.tm = first_m + in_band % rows_in_band;
-    r.tn = in_band / rows_in_band;
+    tile_coords(r.tile, a.tiles_m, a.tiles_n, a.tiles_per_batch, a.group_m, r.b, r.tm, r.tn);
     r.kb0 = (int)(((long long)r.s * a.num_kb) / r.S);
     r.kb1 = (int)(((long long)(r.s + 1) * a.num_kb) / r.S);
     return r;
@@ -230,16 +237,16 @@ __device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long 
 }
 
 // The warp's 32 x 32 chunk (lane = row) goes through a swizzled shared
-// buffer and one TMA store, which also clips rows >= M and columns >= N.
-// fp32 rows are 128 bytes (128-byte swizzle: 16-byte unit q of row r sits at
-// q ^ (r % 8)); 16-bit rows are 64 bytes (64-byte swizzle: q ^ ((r / 2) % 4)).
-// Either way each group of 8 lanes covers all 32 banks.
-__device__ __forceinline__ void store_tma(const MmaArgs &a, const CUtensorMap *tmC, uint8_t *buf, int lane,
+// buffer and one TMA store, which also clips rows and columns beyond the
+// tensor.  fp32 rows are 128 bytes (128-byte swizzle: 16-byte unit q of row
+// r sits at q ^ (r % 8)); 16-bit rows are 64 bytes (64-byte swizzle:
+// q ^ ((r / 2) % 4)).  Either way each group of 8 lanes covers all 32 banks.
+__device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int dtype, uint8_t *buf, int lane,
                                           int b, long long row0, long long col0, const float (&v)[32])
 {
     if (lane == 0) bulk_wait_read<1>();      // this buffer's previous store has read it
     __syncwarp();
-    if (a.c_dtype == TC_F32) {
+    if (dtype == TC_F32) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             *reinterpret_cast<float4 *>(buf + lane * 128 + ((q ^ (lane & 7)) << 4)) =
@@ -248,20 +255,20 @@ __device__ __forceinline__ void store_tma(const MmaArgs &a, const CUtensorMap *t
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack2(v[8 * q + 0], v[8 * q + 1], a.c_dtype);
-            w.y = pack2(v[8 * q + 2], v[8 * q + 3], a.c_dtype);
-            w.z = pack2(v[8 * q + 4], v[8 * q + 5], a.c_dtype);
-            w.w = pack2(v[8 * q + 6], v[8 * q + 7], a.c_dtype);
+            w.x = pack2(v[8 * q + 0], v[8 * q + 1], dtype);
+            w.y = pack2(v[8 * q + 2], v[8 * q + 3], dtype);
+            w.z = pack2(v[8 * q + 4], v[8 * q + 5], dtype);
+            w.w = pack2(v[8 * q + 6], v[8 * q + 7], dtype);
             *reinterpret_cast<uint4 *>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
         }
     }
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-        if (a.c_3d)
-            tma_store_3d(tmC, smem_u32(buf), (int)col0, (int)row0, b);
+        if (is3d)
+            tma_store_3d(map, smem_u32(buf), (int)col0, (int)row0, b);
         else
-            tma_store_2d(tmC, smem_u32(buf), (int)col0, (int)row0);
+            tma_store_2d(map, smem_u32(buf), (int)col0, (int)row0);
         bulk_commit();
     }
 }
@@ -279,7 +286,8 @@ __device__ __forceinline__ void store_tma(const MmaArgs &a, const CUtensorMap *t
 template <int BN, int CG>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const MmaArgs args)
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+               const MmaArgs args)
 {
     constexpr int BNL = BN / CG;                   // B columns loaded by this CTA
     constexpr int STAGE = stage_bytes(BN, CG);
@@ -328,6 +336,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         if (args.c_tma) prefetch_tmap(&tmC);
+        if (args.ws) prefetch_tmap(&tmW);
+        // let the split-K reduction kernel (if any) launch early; it waits
+        // for this grid to finish before it reads the partial tiles
+        griddep_launch_dependents();
     }
     __syncwarp();
     if (warp == 0) {
@@ -473,7 +485,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 // buffer is reused only after one newer store was committed
                 const long long row0 = row - lane;
                 if (row0 < args.M && col0 < args.N) {
-                    store_tma(args, &tmC, my_stage + ebuf * EPI_STAGE_BYTES, lane, b, row0, col0, v);
+                    store_tma(&tmC, args.c_3d, args.c_dtype, my_stage + ebuf * EPI_STAGE_BYTES, lane, b, row0,
+                              col0, v);
                     ebuf ^= 1u;
                 }
             } else {
@@ -517,14 +530,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     emit(w.b, row, (long long)w.tn * BN + c * 32, v);
                 }
             } else {
-                // K slices: park this slice's partial tile (this warp's 32
-                // rows), column-interleaved so each store instruction is
-                // coalesced; the last slice to arrive sums them in slice order
-                const size_t slab = (size_t)BN * 32;          // floats per warp quarter
-                auto slot = [&](int unit) {
-                    return args.ws + (((size_t)(unit - args.split_base) * CG + rank) * 4 + warp) * slab;
-                };
-                float *mine = slot(w.ufirst + w.s);
+                // K slice: the raw fp32 partial tile goes to its workspace
+                // slot (row-major, (BM * CG) x BN per unit); the reduction
+                // kernel sums the slices in slice order afterwards
+                const long long wrow0 =
+                    (long long)(w.ufirst + w.s - args.split_base) * (BM * CG) + (int)rank * BM + warp * 32;
 #pragma unroll 1
                 for (int c = 0; c < CHUNKS; ++c) {
                     uint32_t r[32];
@@ -532,30 +542,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     tmem_ld_32x32b_x32(taddr + c * 32, r);
                     tmem_ld_wait();
                     if (c == CHUNKS - 1) release();
+                    float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(c * 32 + j) * 32 + lane, __uint_as_float(r[j]));
-                }
-                __threadfence();
-                __syncwarp();
-                unsigned old = 0;
-                unsigned *ticket = args.tickets + ((size_t)w.tile * CG + rank) * 4 + warp;
-                if (lane == 0) old = atomicAdd(ticket, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (unsigned)(w.S - 1)) {
-                    __threadfence();
-#pragma unroll 1
-                    for (int c = 0; c < CHUNKS; ++c) {
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                        for (int s = 0; s < w.S; ++s) {
-                            const float *p = slot(w.ufirst + s) + (size_t)(c * 32) * 32 + lane;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] += __ldcg(p + j * 32);
-                        }
-                        emit(w.b, row, (long long)w.tn * BN + c * 32, v);
-                    }
-                    if (lane == 0) *ticket = 0u;       // ready for the next launch
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    store_tma(&tmW, false, TC_F32, my_stage + ebuf * EPI_STAGE_BYTES, lane, 0, wrow0, c * 32, v);
+                    ebuf ^= 1u;
                 }
             }
         }
@@ -595,7 +586,7 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st)
         configured[dev] = true;
     }
     if (CG == 1) {
-        mma_kernel<BN, CG><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.args);
+        mma_kernel<BN, CG><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -610,7 +601,7 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG>, L.tmA, L.tmB, L.tmC, L.args);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG>, L.tmA, L.tmB, L.tmC, L.tmW, L.args);
 }
 
 template <int BN>
@@ -638,7 +629,80 @@ int pairs_for()
     return n;
 }
 
+// ---------------------------------------------------------------- split-K reduction
+// C tile = alpha * (p_0 + p_1 + ... + p_{S-1}) + beta * C_old, the slices
+// summed in slice order (deterministic).  Each thread owns four consecutive
+// columns of one tile row: loads of a slice and stores of C are contiguous
+// across a warp.  Launched as a programmatic dependent of the GEMM kernel:
+// griddepcontrol.wait returns once that grid has finished and its partial
+// tiles are visible.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
+{
+    griddep_wait();
+    const int groups = r.bn / 4;
+    const long long per_tile = (long long)r.rows_per_tile * groups;
+    const long long total = per_tile * r.ntiles;
+    const size_t slice = (size_t)r.rows_per_tile * r.bn;      // floats per partial tile
+    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+         g += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(g / per_tile);
+        const long long rem = g - (long long)t * per_tile;
+        const int row = (int)(rem / groups);
+        const int c4 = (int)(rem - (long long)row * groups);
+        int b, tm, tn;
+        tile_coords(r.first_tile + t, r.tiles_m, r.tiles_n, r.tiles_per_batch, r.group_m, b, tm, tn);
+        const long long grow = (long long)tm * r.rows_per_tile + row;
+        const long long gcol = (long long)tn * r.bn + c4 * 4;
+        if (grow >= r.M || gcol >= r.N) continue;
+        const float *src = r.ws + (size_t)t * r.S * slice + (size_t)row * r.bn + c4 * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < r.S; ++s) {
+            const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + s * slice));
+            acc.x += p.x;
+            acc.y += p.y;
+            acc.z += p.z;
+            acc.w += p.w;
+        }
+        float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        const long long base = (long long)b * r.stride_c + grow * r.ldc + gcol;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float c = (r.beta != 0.0f && gcol + j < r.N) ? load_c(r.C, base + j, r.c_dtype) : 0.0f;
+            v[j] = (r.beta != 0.0f) ? fmaf(r.beta, c, r.alpha * v[j]) : r.alpha * v[j];
+        }
+        if (r.c_vec_ok && gcol + 4 <= r.N) {
+            if (r.c_dtype == TC_F32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(r.C) + base) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                uint2 w;
+                w.x = pack2(v[0], v[1], r.c_dtype);
+                w.y = pack2(v[2], v[3], r.c_dtype);
+                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(r.C) + base) = w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gcol + j < r.N) store_c1(r.C, base + j, v[j], r.c_dtype);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, r);
+}
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
@@ -661,8 +725,8 @@ cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 // ---------------------------------------------------------------- static scratch
 // Scratch of the entry point that allocates nothing (tc_gemm_splitk_noalloc):
 // a file-scope device array, zero at load, held by every GPU that loads this
-// library until the process exits.  Layout: split-K partial tiles, then the
-// arrival counters, then a status word.
+// library until the process exits.  Layout: split-K partial tiles, then a
+// status word.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 cudaError_t noalloc_scratch(NoallocScratch *out)
@@ -685,8 +749,7 @@ cudaError_t noalloc_scratch(NoallocScratch *out)
     }
     unsigned char *base = static_cast<unsigned char *>(addr[dev]);
     out->partials = reinterpret_cast<float *>(base);
-    out->tickets = reinterpret_cast<unsigned *>(base + NOALLOC_PARTIAL_BYTES);
-    out->status = reinterpret_cast<unsigned *>(base + NOALLOC_PARTIAL_BYTES + NOALLOC_TICKETS * sizeof(unsigned));
+    out->status = reinterpret_cast<unsigned *>(base + NOALLOC_PARTIAL_BYTES);
     return cudaSuccess;
 }
 

@@ -3,8 +3,8 @@
 Some callers cannot allocate device memory -- their device memory belongs to
 another allocator with a fixed budget, or they cannot afford the
 device-wide synchronisation of cudaMalloc/cudaFree.  For them the library
-keeps the split-K partial tiles and counters in a static device array and
-needs no context.  This file checks, through the C ABI, that two calls in a
+keeps the split-K partial tiles in a static device array and needs no
+context.  This file checks, through the C ABI, that two calls in a
 row give the same output as the ordinary entry point (tc_gemm) within the
 parity bound used everywhere in these tests, and that requests beyond the
 static array's size are refused.  It is named so that pytest collects it
