@@ -141,7 +141,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Environment override for tests and sweeps: TC_FORCE_VARIANT holds
 // space/comma separated tokens: bn=<64|128|192|256> split=<S> grid=<G>
-// group_m=<G> ffma=<small|large> pack=<1> tail=<S> (K slices of the
+// group_m=<G> ffma=<small|large|panel> pack=<1> tail=<S> (K slices of the
 // last-wave tiles; 0 or 1 disables) sms=<N> (plan for N SMs) cg=<1|2>
 // (CTAs per tile) store=direct (plain stores of C instead of TMA stores).
 struct Force {
@@ -170,7 +170,7 @@ Force read_force()
         else if (k == "split") f.split = std::atoi(v.c_str());
         else if (k == "grid") f.grid = std::atoi(v.c_str());
         else if (k == "group_m") f.group_m = std::atoi(v.c_str());
-        else if (k == "ffma") f.ffma = (v == "large") ? FFMA_LARGE : FFMA_SMALL;
+        else if (k == "ffma") f.ffma = (v == "large") ? FFMA_LARGE : (v == "panel") ? FFMA_PANEL : FFMA_SMALL;
         else if (k == "pack") f.pack = std::atoi(v.c_str());
         else if (k == "tail") f.tail = std::atoi(v.c_str());
         else if (k == "sms") f.sms = std::atoi(v.c_str());
@@ -233,12 +233,15 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     char buf[160];
 
     if (d->a_dtype == TC_F32) {
-        // fp32-exact path on CUDA cores
+        // fp32-exact path on CUDA cores: 128x128 tiles when they fill the
+        // SMs, whole-K panels of 16x32 tiles for small outputs, else 32x32
         p.ffma = true;
         const int64_t big_tiles = cdiv(d->M, 128) * cdiv(d->N, 128) * n.batch;
-        p.ffma_tile = (big_tiles >= num_sms) ? FFMA_LARGE : FFMA_SMALL;
+        const int64_t panel_tiles = cdiv(d->M, 16) * cdiv(d->N, 32) * n.batch;
+        p.ffma_tile = big_tiles >= num_sms ? FFMA_LARGE : panel_tiles <= 8 * num_sms ? FFMA_PANEL : FFMA_SMALL;
         if (f.ffma >= 0) p.ffma_tile = f.ffma;
-        std::snprintf(buf, sizeof buf, "ffma_f32_%s_%s", lay, p.ffma_tile == FFMA_LARGE ? "128x128" : "32x32");
+        std::snprintf(buf, sizeof buf, "ffma_f32_%s_%s", lay,
+                      p.ffma_tile == FFMA_LARGE ? "128x128" : p.ffma_tile == FFMA_PANEL ? "16x32_panel" : "32x32");
         p.name = buf;
         *out = p;
         return TC_OK;
@@ -399,8 +402,9 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     // ---- workspace: [packed A | packed B | split-K partials]
     const int64_t a_batch = (n.batch > 1 && n.sa != 0) ? n.batch : 1;
     const int64_t b_batch = (n.batch > 1 && n.sb != 0) ? n.batch : 1;
-    const int64_t lda_p = p.pack_a ? (int64_t)round_up((size_t)n.a_cols, 8) : n.lda;
-    const int64_t ldb_p = p.pack_b ? (int64_t)round_up((size_t)n.b_cols, 8) : n.ldb;
+    // repacked rows padded to 64 elements: 128-byte aligned rows for TMA
+    const int64_t lda_p = p.pack_a ? (int64_t)round_up((size_t)n.a_cols, 64) : n.lda;
+    const int64_t ldb_p = p.pack_b ? (int64_t)round_up((size_t)n.b_cols, 64) : n.ldb;
     const size_t a_pack_bytes = p.pack_a ? round_up((size_t)(n.a_rows * lda_p * a_batch * 2), 256) : 0;
     const size_t b_pack_bytes = p.pack_b ? round_up((size_t)(n.b_rows * ldb_p * b_batch * 2), 256) : 0;
     const size_t part_bytes =

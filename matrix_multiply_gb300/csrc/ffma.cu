@@ -142,10 +142,117 @@ __global__ void __launch_bounds__(256) ffma_kernel(const FfmaArgs a)
     }
 }
 
+// Small problems: each CTA stages whole K panels (up to KC columns of A's
+// 16 rows and KC rows of B's 32 columns) into shared memory with every load
+// issued back to back, then runs the chains; one global-load latency per
+// panel instead of one per 32-wide K block.  16 x 32 tiles, 256 threads, two
+// outputs per thread.
+constexpr int PBM = 16, PBN = 32;
+constexpr int PANEL_SMEM = 96 * 1024;
+constexpr int PANEL_KC = PANEL_SMEM / ((PBM + PBN) * 4);    // 512
+
+__global__ void __launch_bounds__(256) ffma_panel_kernel(const FfmaArgs a)
+{
+    extern __shared__ float panel[];
+    float *As = panel;                    // [KC][PBM]
+    float *Bs = panel + PANEL_KC * PBM;   // [KC][PBN]
+    const int tid = threadIdx.x;
+    const int tx = tid % 16;              // columns tx and tx + 16
+    const int ty = tid / 16;              // row ty
+    const long long n0 = (long long)blockIdx.x * PBN;
+    const long long tiles_m = ((long long)a.M + PBM - 1) / PBM;
+    for (int b = blockIdx.z; b < a.batch; b += gridDim.z)
+    for (long long mt = blockIdx.y; mt < tiles_m; mt += gridDim.y) {
+        const long long m0 = mt * PBM;
+        const float *A = a.A + (long long)b * a.stride_a;
+        const float *B = a.B + (long long)b * a.stride_b;
+        float *C = a.C + (long long)b * a.stride_c;
+        float acc0 = 0.0f, acc1 = 0.0f;
+        for (long long k0 = 0; k0 < a.K; k0 += PANEL_KC) {
+            const int kc = (int)min((long long)PANEL_KC, a.K - k0);
+            // A panel: PBM x kc; consecutive threads walk the stored-contiguous
+            // dimension.  Loads go to registers 32 at a time before any
+            // shared-memory store, so 32 loads are in flight per thread.
+            const int na = PBM * kc, nb = PBN * kc;
+            for (int e0 = tid; e0 < na; e0 += 32 * 256) {
+                float r[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int e = e0 + q * 256;
+                    int m, k;
+                    if (a.ta) { m = e % PBM; k = e / PBM; } else { k = e % kc; m = e / kc; }
+                    const long long gm = m0 + m, gk = k0 + k;
+                    r[q] = (e < na && gm < a.M) ? (a.ta ? A[gk * a.lda + gm] : A[gm * a.lda + gk]) : 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int e = e0 + q * 256;
+                    if (e >= na) break;
+                    int m, k;
+                    if (a.ta) { m = e % PBM; k = e / PBM; } else { k = e % kc; m = e / kc; }
+                    As[k * PBM + m] = r[q];
+                }
+            }
+            for (int e0 = tid; e0 < nb; e0 += 32 * 256) {
+                float r[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int e = e0 + q * 256;
+                    int k, n;
+                    if (a.tb) { k = e % kc; n = e / kc; } else { n = e % PBN; k = e / PBN; }
+                    const long long gk = k0 + k, gn = n0 + n;
+                    r[q] = (e < nb && gn < a.N) ? (a.tb ? B[gn * a.ldb + gk] : B[gk * a.ldb + gn]) : 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int e = e0 + q * 256;
+                    if (e >= nb) break;
+                    int k, n;
+                    if (a.tb) { k = e % kc; n = e / kc; } else { n = e % PBN; k = e / PBN; }
+                    Bs[k * PBN + n] = r[q];
+                }
+            }
+            __syncthreads();
+            for (int k = 0; k < kc; ++k) {
+                const float av = As[k * PBM + ty];
+                acc0 = fmaf(av, Bs[k * PBN + tx], acc0);
+                acc1 = fmaf(av, Bs[k * PBN + tx + 16], acc1);
+            }
+            __syncthreads();
+        }
+        const long long gm = m0 + ty;
+        if (gm < a.M) {
+            const float accs[2] = {acc0, acc1};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const long long gn = n0 + tx + 16 * j;
+                if (gn >= a.N) continue;
+                float *c = C + gm * a.ldc + gn;
+                const float r = a.alpha * accs[j];
+                *c = (a.beta != 0.0f) ? fmaf(a.beta, *c, r) : r;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st)
 {
+    if (tile == FFMA_PANEL) {
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e =
+                cudaFuncSetAttribute(ffma_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PANEL_SMEM);
+            if (e != cudaSuccess) return e;
+            configured = true;
+        }
+        const int zb = a.batch < 65535 ? a.batch : 65535;
+        const long long ty = ((long long)a.M + PBM - 1) / PBM;
+        dim3 grid((unsigned)(((long long)a.N + PBN - 1) / PBN), (unsigned)(ty < 65535 ? ty : 65535), zb);
+        ffma_panel_kernel<<<grid, 256, PANEL_SMEM, st>>>(a);
+        return cudaGetLastError();
+    }
     const int zb = a.batch < 65535 ? a.batch : 65535;
     if (tile == FFMA_LARGE) {
         const long long ty = ((long long)a.M + 127) / 128;

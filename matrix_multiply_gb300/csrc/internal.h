@@ -123,12 +123,12 @@ struct FfmaArgs {
     long long stride_a, stride_b, stride_c;
     float alpha, beta;
 };
-enum FfmaTile { FFMA_SMALL = 0, FFMA_LARGE = 1 };
+enum FfmaTile { FFMA_SMALL = 0, FFMA_LARGE = 1, FFMA_PANEL = 2 };
 cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st);
 
 // Copy a strided batch of 16-bit matrices (rows x cols, leading dimension
-// ld_src) into a buffer with leading dimension ld_dst (a multiple of 8) and a
-// 16-byte aligned base, so that TMA can read it.
+// ld_src) into a buffer with leading dimension ld_dst (a multiple of 64) and
+// a 256-byte aligned base, so that TMA can read it.
 struct PackArgs {
     const uint16_t *src;
     uint16_t *dst;

@@ -5,7 +5,8 @@
 // row length (the ragged shapes of the tessl architecture.md "Edge-Slice
 // Support" discussion) breaks the second rule.  Such an operand is copied
 // once, in the same layout, into a workspace whose rows are padded to a
-// multiple of 8 elements; the tensor-core kernel then reads the copy.  The
+// multiple of 64 elements (128 bytes, so every TMA box row starts on a
+// cache-line boundary); the tensor-core kernel then reads the copy.  The
 // padding is never read: the TMA descriptor keeps the logical extent and
 // fills out-of-bounds elements with zeros.
 #include "internal.h"
@@ -13,27 +14,27 @@
 namespace tc {
 namespace {
 
+// One CTA row of 256 threads copies 256 consecutive elements of a row, so
+// each warp instruction reads and writes one contiguous 64-byte segment;
+// every thread handles four rows per iteration (four loads in flight).
+// Only the logical columns are written: TMA never reads the padding.
 __global__ void __launch_bounds__(256) pack_kernel(const PackArgs p)
 {
-    const long long groups = (p.cols + 7) / 8;           // 8 elements -> one 16-byte store
-    const long long per_mat = groups * p.rows;
-    const long long total = per_mat * p.batch;
-    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total;
-         g += (long long)gridDim.x * blockDim.x) {
-        const long long b = g / per_mat;
-        const long long rem = g - b * per_mat;
-        const long long r = rem / groups;
-        const long long c = (rem - r * groups) * 8;
-        const uint16_t *s = p.src + b * p.stride_src + r * p.ld_src + c;
-        uint16_t v[8];
+    const long long c = (long long)blockIdx.x * 256 + threadIdx.x;
+    if (c >= p.cols) return;
+    const long long step = (long long)gridDim.y * 4;
+    for (int b = 0; b < p.batch; ++b) {
+        const uint16_t *src = p.src + b * p.stride_src + c;
+        uint16_t *dst = p.dst + b * p.stride_dst + c;
+        for (long long r0 = (long long)blockIdx.y * 4; r0 < p.rows; r0 += step) {
+            uint16_t v[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = (c + i < p.cols) ? s[i] : (uint16_t)0;
-        uint4 w;
-        w.x = (uint32_t)v[0] | ((uint32_t)v[1] << 16);
-        w.y = (uint32_t)v[2] | ((uint32_t)v[3] << 16);
-        w.z = (uint32_t)v[4] | ((uint32_t)v[5] << 16);
-        w.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
-        *reinterpret_cast<uint4 *>(p.dst + b * p.stride_dst + r * p.ld_dst + c) = w;
+            for (int q = 0; q < 4; ++q)
+                if (r0 + q < p.rows) v[q] = src[(r0 + q) * p.ld_src];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (r0 + q < p.rows) dst[(r0 + q) * p.ld_dst] = v[q];
+        }
     }
 }
 
@@ -41,11 +42,14 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackArgs p)
 
 cudaError_t launch_pack(const PackArgs &p, cudaStream_t st)
 {
-    const long long total = ((p.cols + 7) / 8) * p.rows * p.batch;
-    long long blocks = (total + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    if (blocks < 1) blocks = 1;
-    pack_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+    const long long gx = (p.cols + 255) / 256;
+    const long long rows4 = (p.rows + 3) / 4;
+    long long gy = (2048 + gx - 1) / gx;           // about 2048 CTAs in total
+    if (gy > rows4) gy = rows4;
+    if (gy > 65535) gy = 65535;
+    if (gy < 1) gy = 1;
+    if (gx > 0x7fffffffLL) return cudaErrorInvalidValue;
+    pack_kernel<<<dim3((unsigned)gx, (unsigned)gy, 1), 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

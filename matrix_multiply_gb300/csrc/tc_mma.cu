@@ -236,6 +236,53 @@ __device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long 
     }
 }
 
+// C layouts TMA cannot address (rows not 16-byte multiples): the warp's
+// 32 x 32 chunk is transposed through shared memory (32 x 33 floats, so
+// both the row-wise and the column-wise accesses hit 32 distinct banks) and
+// every global access touches one contiguous 32-element row segment per
+// instruction instead of 32 separate rows.
+constexpr int XPOSE_LD = 33;
+
+// v <- alpha * v + beta * C_old, C_old read row-coalesced through `buf`
+__device__ __forceinline__ void apply_alpha_beta_staged(const MmaArgs &a, float *buf, int lane, int b,
+                                                        long long row0, long long col0, float (&v)[32])
+{
+    if (a.beta == 0.0f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = a.alpha * v[j];
+        return;
+    }
+    const long long col = col0 + lane;
+    for (int r = 0; r < 32; ++r) {
+        const long long row = row0 + r;
+        buf[r * XPOSE_LD + lane] = (row < a.M && col < a.N)
+                                       ? load_c(a.C, (long long)b * a.stride_c + row * a.ldc + col, a.c_dtype)
+                                       : 0.0f;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = fmaf(a.beta, buf[lane * XPOSE_LD + j], a.alpha * v[j]);
+    __syncwarp();
+}
+
+// C[row0 .. row0+31, col0 .. col0+31] = the warp's chunk, row-coalesced through `buf`
+__device__ __forceinline__ void store_staged(const MmaArgs &a, float *buf, int lane, int b, long long row0,
+                                             long long col0, const float (&v)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j) buf[lane * XPOSE_LD + j] = v[j];
+    __syncwarp();
+    const long long col = col0 + lane;
+    if (col < a.N) {
+        for (int r = 0; r < 32; ++r) {
+            const long long row = row0 + r;
+            if (row >= a.M) break;
+            store_c1(a.C, (long long)b * a.stride_c + row * a.ldc + col, buf[r * XPOSE_LD + lane], a.c_dtype);
+        }
+    }
+    __syncwarp();
+}
+
 // The warp's 32 x 32 chunk (lane = row) goes through a swizzled shared
 // buffer and one TMA store, which also clips rows and columns beyond the
 // tensor.  fp32 rows are 128 bytes (128-byte swizzle: 16-byte unit q of row
@@ -479,6 +526,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         uint8_t *my_stage = cstage + warp * 2 * EPI_STAGE_BYTES;
         // alpha/beta, then the chunk to C (TMA store when C allows it)
         auto emit = [&](int b, long long row, long long col0, float (&v)[32]) {
+            if (!args.c_tma) {
+                // both staging buffers of this warp serve as one transpose buffer
+                float *xbuf = reinterpret_cast<float *>(my_stage);
+                apply_alpha_beta_staged(args, xbuf, lane, b, row - lane, col0, v);
+                store_staged(args, xbuf, lane, b, row - lane, col0, v);
+                return;
+            }
             apply_alpha_beta(args, b, row, col0, v);
             if (args.c_tma) {
                 // buffers alternate over the stores actually issued, so a

@@ -142,7 +142,7 @@ def plan(M, N, K, ab, c, ta=False, tb=False, A=1 << 20, B=1 << 40, C=1 << 41, **
 
 
 def test_plan_fp32_goes_to_ffma():
-    assert plan(256, 256, 256, "f32", "f32").startswith("ffma_f32_nn")
+    assert plan(256, 256, 256, "f32", "f32") == "ffma_f32_nn_16x32_panel"
     assert plan(4096, 4096, 4096, "f32", "f32", tb=True) == "ffma_f32_nt_128x128"
 
 

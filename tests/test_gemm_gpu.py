@@ -101,10 +101,13 @@ def test_ffma_parity(ctx, ta, tb, shape):
     assert ctx.last_kernel.startswith("ffma_f32_" + p.layout.lower())
 
 
-@pytest.mark.parametrize("spec", ["ffma=small", "ffma=large"])
-def test_ffma_tiles(ctx, force, spec):
+@pytest.mark.parametrize("spec", ["ffma=small", "ffma=large", "ffma=panel"])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_ffma_tiles(ctx, force, spec, ta, tb):
     force(spec)
-    p = synthetic.make_problem(333, 290, 517, "f32", "f32", transpose_b=True, seed=5)
+    # K = 1100 spans several 512-wide panels; ragged M and N
+    p = synthetic.make_problem(333, 290, 1100, "f32", "f32", transpose_a=ta, transpose_b=tb, seed=5,
+                               alpha=0.75, beta=-0.5, c_fill="uniform")
     check_full(ctx, p, spec)
 
 
