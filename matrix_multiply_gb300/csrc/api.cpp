@@ -144,9 +144,13 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // group_m=<G> ffma=<small|large|panel> pack=<1> tail=<S> (K slices of the
 // last-wave tiles; 0 or 1 disables) sms=<N> (plan for N SMs) cg=<1|2>
 // (CTAs per tile) store=direct (plain stores of C instead of TMA stores).
+// Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
+// "accumulator ready" signal, so the epilogue's wait expires) and
+// debug_timeout_ms=<ms> (the bound on every device wait).
 struct Force {
     int bn = 0, split = 0, grid = 0, group_m = 0, ffma = -1, pack = 0, tail = -1, sms = 0, cg = 0;
     bool direct_store = false;
+    int debug_drop = 0, debug_timeout_ms = 0;
 };
 
 Force read_force()
@@ -176,6 +180,8 @@ Force read_force()
         else if (k == "sms") f.sms = std::atoi(v.c_str());
         else if (k == "cg") f.cg = std::atoi(v.c_str());
         else if (k == "store") f.direct_store = (v == "direct");
+        else if (k == "debug_drop") f.debug_drop = std::atoi(v.c_str());
+        else if (k == "debug_timeout_ms") f.debug_timeout_ms = std::atoi(v.c_str());
     }
     return f;
 }
@@ -485,6 +491,11 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.status = s->status_dev;
     const int64_t kb_per_unit = a.num_kb;
     a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
+    {
+        const Force f = read_force();
+        if (f.debug_timeout_ms > 0) a.timeout_ns = (unsigned long long)f.debug_timeout_ms * 1000000ull;
+        a.debug_drop_tfull = f.debug_drop;
+    }
 
     const int64_t lda_use = p.pack_a ? lda_p : n.lda;
     const int64_t ldb_use = p.pack_b ? ldb_p : n.ldb;

@@ -69,6 +69,7 @@ struct MmaArgs {
     float *ws;             // split-K partial tiles (written through the fourth descriptor)
     unsigned *status;      // device status word (0 = fine)
     unsigned long long timeout_ns;
+    int debug_drop_tfull;  // test hook: never signal the first tile's accumulator
 };
 
 struct MmaLaunch {

@@ -505,6 +505,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     ++it;
                 }
                 if (!ok) break;
+                // test hook: withhold the "accumulator ready" signal of this
+                // CTA's first tile, so that the epilogue's bounded wait expires
+                if (args.debug_drop_tfull && local == 0) continue;
                 if (CG == 1)
                     mma_commit(smem_u32(&tfull_bar[acc]));
                 else
