@@ -17,8 +17,11 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
+#include <memory>
 #include <mutex>
 #include <string>
+#include <vector>
 
 using namespace tc;
 
@@ -143,13 +146,15 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // space/comma separated tokens: bn=<64|128|192|256> split=<S> grid=<G>
 // group_m=<G> ffma=<small|large|panel> pack=<1> tail=<S> (K slices of the
 // last-wave tiles; 0 or 1 disables) sms=<N> (plan for N SMs) cg=<1|2>
-// (CTAs per tile) store=direct (plain stores of C instead of TMA stores).
+// (CTAs per tile) store=direct (plain stores of C instead of TMA stores)
+// grouped=0 (a grouped call enqueues its problems one by one).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
 struct Force {
     int bn = 0, split = 0, grid = 0, group_m = 0, ffma = -1, pack = 0, tail = -1, sms = 0, cg = 0;
     bool direct_store = false;
+    int grouped = 1;
     int debug_drop = 0, debug_timeout_ms = 0;
 };
 
@@ -180,6 +185,7 @@ Force read_force()
         else if (k == "sms") f.sms = std::atoi(v.c_str());
         else if (k == "cg") f.cg = std::atoi(v.c_str());
         else if (k == "store") f.direct_store = (v == "direct");
+        else if (k == "grouped") f.grouped = std::atoi(v.c_str());
         else if (k == "debug_drop") f.debug_drop = std::atoi(v.c_str());
         else if (k == "debug_timeout_ms") f.debug_timeout_ms = std::atoi(v.c_str());
     }
@@ -421,21 +427,23 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     const void *Ause = A, *Buse = B;
     int64_t sa = n.sa, sb = n.sb;
     uint64_t launches = 0;
+    PackBatch pb;
+    pb.count = 0;
     if (p.pack_a) {
-        PackArgs pk{static_cast<const uint16_t *>(A), reinterpret_cast<uint16_t *>(ws), n.a_rows, n.a_cols,
-                    n.lda, lda_p, a_batch > 1 ? n.sa : 0, n.a_rows * lda_p, (int)a_batch};
-        if ((e = launch_pack(pk, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        pb.seg[pb.count++] = PackArgs{static_cast<const uint16_t *>(A), reinterpret_cast<uint16_t *>(ws), n.a_rows,
+                                      n.a_cols, n.lda, lda_p, a_batch > 1 ? n.sa : 0, n.a_rows * lda_p, (int)a_batch};
         Ause = ws;
         sa = a_batch > 1 ? n.a_rows * lda_p : 0;
-        ++launches;
     }
     if (p.pack_b) {
         uint8_t *dst = ws + a_pack_bytes;
-        PackArgs pk{static_cast<const uint16_t *>(B), reinterpret_cast<uint16_t *>(dst), n.b_rows, n.b_cols,
-                    n.ldb, ldb_p, b_batch > 1 ? n.sb : 0, n.b_rows * ldb_p, (int)b_batch};
-        if ((e = launch_pack(pk, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        pb.seg[pb.count++] = PackArgs{static_cast<const uint16_t *>(B), reinterpret_cast<uint16_t *>(dst), n.b_rows,
+                                      n.b_cols, n.ldb, ldb_p, b_batch > 1 ? n.sb : 0, n.b_rows * ldb_p, (int)b_batch};
         Buse = dst;
         sb = b_batch > 1 ? n.b_rows * ldb_p : 0;
+    }
+    if (pb.count > 0) {
+        if ((e = launch_pack(pb, s->st)) != cudaSuccess) return TC_ERR_CUDA;
         ++launches;
     }
 
@@ -550,6 +558,201 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     }
     ctx->launches += launches;
     ctx->last = p.name;
+    return TC_OK;
+}
+
+// ----------------------------------------------------------- grouped launch
+
+// One f16/bf16 problem of a grouped call, after validation.
+struct GItem {
+    int idx;                    // position in the caller's arrays
+    Norm n;
+    bool pack_a, pack_b;
+    int64_t lda_p, ldb_p;       // leading dims of the operands the kernel reads
+    size_t a_off, b_off;        // workspace offsets of the packed copies
+    int64_t num_kb;
+};
+
+// Every f16/bf16 problem of a group goes through one batched repack launch
+// (operands TMA cannot read in place) and one persistent tensor-core launch
+// per GROUP_MAX problems, whose CTAs walk the tiles of all problems (tessl
+// architecture.md, "Edge-Slice Support": ragged problems; one launch
+// instead of one per problem removes the per-problem launch, pipeline fill
+// and partial last wave).  Problems are ordered by K-loop length, longest
+// first, so that the last waves hold the shortest tiles.
+tc_status_t enqueue_grouped(tc_ctx *ctx, int n, const tc_gemm_desc *d, const void *const *A, const void *const *B,
+                            void *const *C, const std::vector<int> &tc_idx, const std::vector<Norm> &norms,
+                            tc_stream *s)
+{
+    const Force f = read_force();
+    const int num_sms = f.sms > 0 ? f.sms : ctx->num_sms;
+    std::vector<GItem> items;
+    items.reserve(tc_idx.size());
+    size_t ws_bytes = 0;
+    for (int i : tc_idx) {
+        GItem g{};
+        g.idx = i;
+        g.n = norms[i];
+        g.pack_a = !aligned16(A[i]) || (g.n.lda % 8) != 0 || f.pack;
+        g.pack_b = !aligned16(B[i]) || (g.n.ldb % 8) != 0 || f.pack;
+        g.lda_p = g.pack_a ? (int64_t)round_up((size_t)g.n.a_cols, 64) : g.n.lda;
+        g.ldb_p = g.pack_b ? (int64_t)round_up((size_t)g.n.b_cols, 64) : g.n.ldb;
+        g.a_off = ws_bytes;
+        if (g.pack_a) ws_bytes += round_up((size_t)(g.n.a_rows * g.lda_p * 2), 256);
+        g.b_off = ws_bytes;
+        if (g.pack_b) ws_bytes += round_up((size_t)(g.n.b_rows * g.ldb_p * 2), 256);
+        g.num_kb = cdiv(d[i].K, BK);
+        items.push_back(g);
+    }
+    (void)n;
+
+    // kernel shape: the least modelled time over all problems' tiles
+    static const int shapes[][2] = {{2, 256}, {1, 256}, {2, 128}, {1, 128}};
+    int bn = 0, cg = 1;
+    double best = 1e300;
+    for (const auto &sh : shapes) {
+        const int c = sh[0], b = sh[1];
+        if (f.cg && c != f.cg) continue;
+        if (f.bn && b != f.bn) continue;
+        const int workers = c == 2 ? std::max(num_sms / 2, 1) : num_sms;
+        double work = 0.0;
+        int64_t tiles = 0;
+        for (const GItem &g : items) {
+            const int64_t t = cdiv(d[g.idx].M, BM * c) * cdiv(d[g.idx].N, b);
+            tiles += t;
+            work += (double)t * (double)g.num_kb;
+        }
+        const double waves = std::ceil((double)tiles / workers);
+        const double t = std::max(work / workers, waves) * b / tile_rate(c, b);
+        if (t < best - 1e-9) {
+            best = t;
+            bn = b;
+            cg = c;
+        }
+    }
+    if (bn == 0) return TC_ERR_VARIANT;
+
+    tc_status_t st = ensure_ws(s, ws_bytes + 256);
+    if (st != TC_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(s->ws);
+    uint64_t launches = 0;
+    cudaError_t e;
+
+    // repack, PACK_MAX operands per launch
+    {
+        PackBatch pb;
+        pb.count = 0;
+        auto flush = [&]() -> bool {
+            if (pb.count == 0) return true;
+            if (launch_pack(pb, s->st) != cudaSuccess) return false;
+            ++launches;
+            pb.count = 0;
+            return true;
+        };
+        for (const GItem &g : items) {
+            if (g.pack_a) {
+                pb.seg[pb.count++] = PackArgs{static_cast<const uint16_t *>(A[g.idx]),
+                                              reinterpret_cast<uint16_t *>(ws + g.a_off), g.n.a_rows, g.n.a_cols,
+                                              g.n.lda, g.lda_p, 0, 0, 1};
+                if (pb.count == PACK_MAX && !flush()) return TC_ERR_CUDA;
+            }
+            if (g.pack_b) {
+                pb.seg[pb.count++] = PackArgs{static_cast<const uint16_t *>(B[g.idx]),
+                                              reinterpret_cast<uint16_t *>(ws + g.b_off), g.n.b_rows, g.n.b_cols,
+                                              g.n.ldb, g.ldb_p, 0, 0, 1};
+                if (pb.count == PACK_MAX && !flush()) return TC_ERR_CUDA;
+            }
+        }
+        if (!flush()) return TC_ERR_CUDA;
+    }
+
+    std::stable_sort(items.begin(), items.end(),
+                     [](const GItem &x, const GItem &y) { return x.num_kb > y.num_kb; });
+
+    int pairs = 0;
+    if (cg == 2) {
+        int &mp = ctx->max_pairs[bn == 256 ? 1 : 0];
+        if (mp < 0) mp = max_active_pairs(bn);
+        if (mp < 1) return TC_ERR_VARIANT;
+        pairs = mp;
+    }
+    const int workers = cg == 2 ? std::max(num_sms / 2, 1) : num_sms;
+    std::unique_ptr<GroupTable> table(new GroupTable());
+    for (size_t first = 0; first < items.size(); first += GROUP_MAX) {
+        const size_t cnt = std::min(items.size() - first, (size_t)GROUP_MAX);
+        GroupTable &gt = *table;
+        std::memset(static_cast<void *>(&gt), 0, sizeof(GroupTable));
+        gt.count = (int)cnt;
+        int64_t units = 0, max_kb = 1;
+        for (size_t j = 0; j < cnt; ++j) {
+            const GItem &g = items[first + j];
+            const tc_gemm_desc &q = d[g.idx];
+            GroupInfo &gi = gt.info[j];
+            gi.M = q.M;
+            gi.N = q.N;
+            gi.num_kb = (int)g.num_kb;
+            gi.tiles_m = (int)cdiv(q.M, BM * cg);
+            gi.tiles_n = (int)cdiv(q.N, bn);
+            gi.unit_begin = (int)units;
+            units += (int64_t)gi.tiles_m * gi.tiles_n;
+            if (units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
+            max_kb = std::max<int64_t>(max_kb, g.num_kb);
+            gi.a_kmajor = !q.transpose_a;
+            gi.b_kmajor = q.transpose_b;
+            const uint32_t fmt = q.a_dtype == TC_BF16 ? 1u : 0u;
+            gi.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(!gi.a_kmajor) << 15) |
+                       ((uint32_t)(!gi.b_kmajor) << 16) | ((uint32_t)(bn >> 3) << 17) |
+                       ((uint32_t)((BM * cg) >> 4) << 24);
+            gi.c_dtype = q.c_dtype;
+            const int64_t ec = (int64_t)elem_size(q.c_dtype);
+            gi.c_vec_ok = aligned16(C[g.idx]) && (g.n.ldc * ec) % 16 == 0;
+            gi.c_tma = gi.c_vec_ok && !f.direct_store;
+            gi.alpha = q.alpha;
+            gi.beta = q.beta;
+            gi.C = C[g.idx];
+            gi.ldc = g.n.ldc;
+            const void *Au = g.pack_a ? static_cast<const void *>(ws + g.a_off) : A[g.idx];
+            const void *Bu = g.pack_b ? static_cast<const void *>(ws + g.b_off) : B[g.idx];
+            bool ok = gi.a_kmajor
+                          ? encode_map(ctx, &gt.tmA[j], q.a_dtype, Au, q.K, q.M, g.lda_p, false, 1, 0, 64, BM)
+                          : encode_map(ctx, &gt.tmA[j], q.a_dtype, Au, q.M, q.K, g.lda_p, false, 1, 0, 64, 64);
+            if (ok)
+                ok = gi.b_kmajor ? encode_map(ctx, &gt.tmB[j], q.a_dtype, Bu, q.K, q.N, g.ldb_p, false, 1, 0, 64,
+                                              (uint32_t)(bn / cg))
+                                 : encode_map(ctx, &gt.tmB[j], q.a_dtype, Bu, q.N, q.K, g.ldb_p, false, 1, 0, 64, 64);
+            if (ok && gi.c_tma)
+                ok = encode_map(ctx, &gt.tmC[j], q.c_dtype, C[g.idx], q.N, q.M, g.n.ldc, false, 1, 0, 32, 32,
+                                q.c_dtype == TC_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+            if (!ok) return TC_ERR_CUDA;
+        }
+        MmaLaunch L{};
+        L.bn = bn;
+        L.cg = cg;
+        int grid = (int)std::min<int64_t>(units, workers);
+        if (f.grid > 0) grid = (int)std::min<int64_t>(f.grid, units);
+        if (cg == 2) grid = std::min(grid, pairs);
+        L.grid = grid * cg;
+        MmaArgs &a = L.args;
+        a.num_kb = (int)max_kb;
+        a.batch = 1;
+        a.seg0_tiles = (int)units;
+        a.seg0_split = 1;
+        a.seg1_split = 1;
+        a.split_base = (int)units;
+        a.total_units = (int)units;
+        a.group_m = f.group_m > 0 ? f.group_m : 4;
+        a.status = s->status_dev;
+        a.timeout_ns = 4000000000ull + (unsigned long long)max_kb * 20000ull;
+        if (f.debug_timeout_ms > 0) a.timeout_ns = (unsigned long long)f.debug_timeout_ms * 1000000ull;
+        a.debug_drop_tfull = f.debug_drop;
+        if ((e = launch_mma_grouped(L, gt, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        ++launches;
+    }
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "grouped_tcgen05_%dx%d%s_n%d", BM * cg, bn, cg == 2 ? "_pair" : "",
+                  (int)items.size());
+    ctx->launches += launches;
+    ctx->last = buf;
     return TC_OK;
 }
 
@@ -745,16 +948,26 @@ tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d, con
     if (!ctx || !s || !d || !A || !B || !C) return TC_ERR_NULL;
     if (n < 0) return TC_ERR_DIM;
     // validate everything before enqueueing anything
+    std::vector<Norm> norms((size_t)n);
+    std::vector<int> tc_idx, other_idx;
     for (int i = 0; i < n; ++i) {
-        Norm nn;
-        tc_status_t st = validate(&d[i], A[i], B[i], C[i], 1, 0, 0, 0, &nn);
+        tc_status_t st = validate(&d[i], A[i], B[i], C[i], 1, 0, 0, 0, &norms[(size_t)i]);
         if (st != TC_OK) return st;
+        (d[i].a_dtype == TC_F32 ? other_idx : tc_idx).push_back(i);
     }
-    for (int i = 0; i < n; ++i) {
+    // a lone tensor-core problem takes the single-problem dispatcher
+    if (tc_idx.size() < 2 || read_force().grouped == 0) {
+        other_idx.insert(other_idx.end(), tc_idx.begin(), tc_idx.end());
+        tc_idx.clear();
+    }
+    for (int i : other_idx) {
         tc_status_t st = run(ctx, &d[i], A[i], B[i], C[i], 1, 0, 0, 0, s);
         if (st != TC_OK) return st;
     }
-    return TC_OK;
+    if (tc_idx.empty()) return TC_OK;
+    std::lock_guard<std::mutex> g(ctx->mu);
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    return enqueue_grouped(ctx, n, d, A, B, C, tc_idx, norms, s);
 }
 
 tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host, const void *B_host, void *C_host)

@@ -81,6 +81,32 @@ struct MmaLaunch {
 };
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st);
+
+// A group of independent problems in one persistent launch.  Every problem
+// has its own TMA descriptors and epilogue fields; all share the kernel
+// shape (BN, CTAs per tile) and take one K slice per tile.  Unit u (one
+// output tile) belongs to the problem p with unit_begin[p] <= u <
+// unit_begin[p + 1]; the table travels as a kernel parameter.
+constexpr int GROUP_MAX = 64;
+struct GroupInfo {
+    int M, N, num_kb;
+    int tiles_m, tiles_n;
+    int unit_begin;
+    int a_kmajor, b_kmajor;
+    uint32_t idesc;
+    int c_dtype, c_vec_ok, c_tma;
+    float alpha, beta;
+    void *C;
+    long long ldc;
+};
+struct GroupTable {
+    CUtensorMap tmA[GROUP_MAX], tmB[GROUP_MAX], tmC[GROUP_MAX];
+    GroupInfo info[GROUP_MAX];
+    int count;
+};
+// L.args carries the launch-wide fields (total_units, group_m, status,
+// timeout); the per-problem ones come from the table.
+cudaError_t launch_mma_grouped(const MmaLaunch &L, const GroupTable &g, cudaStream_t st);
 // Largest number of CTA pairs of the BN-wide pair kernel that can be
 // resident at once on the current device (0 if the pair kernel cannot run).
 int max_active_pairs(int bn);
@@ -136,6 +162,14 @@ struct PackArgs {
     long long rows, cols, ld_src, ld_dst, stride_src, stride_dst;
     int batch;
 };
-cudaError_t launch_pack(const PackArgs &p, cudaStream_t st);
+// Up to PACK_MAX such copies in one launch (block_begin is filled in by
+// launch_pack: the first CTA of each copy, then the total).
+constexpr int PACK_MAX = 128;
+struct PackBatch {
+    int count;
+    long long block_begin[PACK_MAX + 1];
+    PackArgs seg[PACK_MAX];
+};
+cudaError_t launch_pack(PackBatch &pb, cudaStream_t st);
 
 }  // namespace tc

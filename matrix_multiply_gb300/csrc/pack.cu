@@ -9,47 +9,93 @@
 // cache-line boundary); the tensor-core kernel then reads the copy.  The
 // padding is never read: the TMA descriptor keeps the logical extent and
 // fills out-of-bounds elements with zeros.
+//
+// One launch repacks every operand of a call (a whole group of problems):
+// the CTAs are split between the operands by a prefix table.
 #include "internal.h"
 
 namespace tc {
 namespace {
 
-// One CTA row of 256 threads copies 256 consecutive elements of a row, so
-// each warp instruction reads and writes one contiguous 64-byte segment;
-// every thread handles four rows per iteration (four loads in flight).
-// Only the logical columns are written: TMA never reads the padding.
-__global__ void __launch_bounds__(256) pack_kernel(const PackArgs p)
+constexpr int PACK_THREADS = 256;
+constexpr int PACK_ITEMS = 4;      // 16-byte output chunks per thread (loads in flight)
+
+__device__ __forceinline__ uint32_t fsr(uint32_t lo, uint32_t hi, uint32_t sh) { return __funnelshift_r(lo, hi, sh); }
+
+// The 16 bytes at byte offset `off` (even, 0..14) of the 32-byte window a|b.
+__device__ __forceinline__ uint4 window16(const uint4 &a, const uint4 &b, uint32_t off)
 {
-    const long long c = (long long)blockIdx.x * 256 + threadIdx.x;
-    if (c >= p.cols) return;
-    const long long step = (long long)gridDim.y * 4;
-    for (int b = 0; b < p.batch; ++b) {
-        const uint16_t *src = p.src + b * p.stride_src + c;
-        uint16_t *dst = p.dst + b * p.stride_dst + c;
-        for (long long r0 = (long long)blockIdx.y * 4; r0 < p.rows; r0 += step) {
-            uint16_t v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (r0 + q < p.rows) v[q] = src[(r0 + q) * p.ld_src];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (r0 + q < p.rows) dst[(r0 + q) * p.ld_dst] = v[q];
-        }
+    const uint32_t sh = (off & 2u) * 8u;
+    uint4 o;
+    switch (off >> 2) {
+    case 0: o = make_uint4(fsr(a.x, a.y, sh), fsr(a.y, a.z, sh), fsr(a.z, a.w, sh), fsr(a.w, b.x, sh)); break;
+    case 1: o = make_uint4(fsr(a.y, a.z, sh), fsr(a.z, a.w, sh), fsr(a.w, b.x, sh), fsr(b.x, b.y, sh)); break;
+    case 2: o = make_uint4(fsr(a.z, a.w, sh), fsr(a.w, b.x, sh), fsr(b.x, b.y, sh), fsr(b.y, b.z, sh)); break;
+    default: o = make_uint4(fsr(a.w, b.x, sh), fsr(b.x, b.y, sh), fsr(b.y, b.z, sh), fsr(b.z, b.w, sh)); break;
     }
+    return o;
+}
+
+// Each thread moves PACK_ITEMS chunks of 8 elements; consecutive threads
+// take consecutive chunks of a row, so loads and stores are contiguous
+// across a warp.  A source chunk that is not 16-byte aligned is read as the
+// one or two aligned 16-byte words that hold its valid elements (each word
+// read holds at least one of them) and shifted into place.  The 16-byte
+// store may write past the row's last column into the row padding, which
+// nothing reads.
+__global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const __grid_constant__ PackBatch pb)
+{
+    int e = 0;
+    while (e + 1 < pb.count && pb.block_begin[e + 1] <= (long long)blockIdx.x) ++e;
+    const PackArgs &p = pb.seg[e];
+    const long long chunks = (p.cols + 7) / 8;
+    const long long per_entry = p.rows * chunks;
+    const long long items = per_entry * p.batch;
+    const long long first = ((long long)blockIdx.x - pb.block_begin[e]) * (PACK_THREADS * PACK_ITEMS) + threadIdx.x;
+
+    uint4 q0[PACK_ITEMS], q1[PACK_ITEMS];
+    uint32_t off[PACK_ITEMS];
+    uint16_t *dst[PACK_ITEMS];
+#pragma unroll
+    for (int k = 0; k < PACK_ITEMS; ++k) {
+        const long long it = first + (long long)k * PACK_THREADS;
+        dst[k] = nullptr;
+        if (it >= items) continue;
+        const long long b = it / per_entry;
+        const long long rem = it - b * per_entry;
+        const long long r = rem / chunks;
+        const long long c = (rem - r * chunks) * 8;
+        const uint16_t *s = p.src + b * p.stride_src + r * p.ld_src + c;
+        const int valid = (int)min(8LL, p.cols - c);
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
+        off[k] = (uint32_t)(addr & 15u);
+        const uint4 *w = reinterpret_cast<const uint4 *>(addr - off[k]);
+        q0[k] = __ldg(w);
+        q1[k] = (off[k] + 2u * (uint32_t)valid > 16u) ? __ldg(w + 1) : make_uint4(0u, 0u, 0u, 0u);
+        dst[k] = p.dst + b * p.stride_dst + r * p.ld_dst + c;
+    }
+#pragma unroll
+    for (int k = 0; k < PACK_ITEMS; ++k)
+        if (dst[k]) *reinterpret_cast<uint4 *>(dst[k]) = window16(q0[k], q1[k], off[k]);
 }
 
 }  // namespace
 
-cudaError_t launch_pack(const PackArgs &p, cudaStream_t st)
+cudaError_t launch_pack(PackBatch &pb, cudaStream_t st)
 {
-    const long long gx = (p.cols + 255) / 256;
-    const long long rows4 = (p.rows + 3) / 4;
-    long long gy = (2048 + gx - 1) / gx;           // about 2048 CTAs in total
-    if (gy > rows4) gy = rows4;
-    if (gy > 65535) gy = 65535;
-    if (gy < 1) gy = 1;
-    if (gx > 0x7fffffffLL) return cudaErrorInvalidValue;
-    pack_kernel<<<dim3((unsigned)gx, (unsigned)gy, 1), 256, 0, st>>>(p);
+    if (pb.count < 1 || pb.count > PACK_MAX) return cudaErrorInvalidValue;
+    long long blocks = 0;
+    for (int i = 0; i < pb.count; ++i) {
+        const PackArgs &p = pb.seg[i];
+        if ((reinterpret_cast<uintptr_t>(p.dst) & 15u) || (p.ld_dst % 8) || (p.stride_dst % 8))
+            return cudaErrorInvalidValue;
+        const long long items = p.rows * ((p.cols + 7) / 8) * p.batch;
+        pb.block_begin[i] = blocks;
+        blocks += (items + PACK_THREADS * PACK_ITEMS - 1) / (PACK_THREADS * PACK_ITEMS);
+    }
+    pb.block_begin[pb.count] = blocks;
+    if (blocks < 1 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    pack_kernel<<<(unsigned)blocks, PACK_THREADS, 0, st>>>(pb);
     return cudaGetLastError();
 }
 

@@ -39,6 +39,7 @@
 #include <cuda_fp16.h>
 
 #include <mutex>
+#include <type_traits>
 
 namespace tc {
 namespace {
@@ -94,7 +95,16 @@ struct Unit {
     int s, S;            // K slice of this unit and the tile's slice count
     int kb0, kb1;        // K-block range [kb0, kb1)
     int ufirst;          // unit of slice 0 of this tile
+    int p;               // problem of a grouped launch (0 otherwise)
 };
+
+// Kernel parameter holding the problem table of a grouped launch; a
+// single-problem launch carries an empty stand-in.
+struct NoTable {
+    int count;
+};
+template <bool GROUPED>
+using TableOf = std::conditional_t<GROUPED, GroupTable, NoTable>;
 
 // Linear tile id -> (batch entry, tile row, tile column): bands of group_m
 // tile rows, column-major inside a band.
@@ -131,7 +141,37 @@ __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
     tile_coords(r.tile, a.tiles_m, a.tiles_n, a.tiles_per_batch, a.group_m, r.b, r.tm, r.tn);
     r.kb0 = (int)(((long long)r.s * a.num_kb) / r.S);
     r.kb1 = (int)(((long long)(r.s + 1) * a.num_kb) / r.S);
+    r.p = 0;
     return r;
+}
+
+// Grouped launch: unit u is one whole-K tile of problem p, found by a
+// forward scan from `hint` (each warp visits units in increasing order).
+__device__ __forceinline__ Unit decode_grouped(const GroupTable &g, int group_m, int u, int &hint)
+{
+    int p = hint;
+    while (p + 1 < g.count && g.info[p + 1].unit_begin <= u) ++p;
+    hint = p;
+    const GroupInfo &q = g.info[p];
+    Unit r;
+    r.p = p;
+    r.tile = u - q.unit_begin;
+    r.s = 0;
+    r.S = 1;
+    r.ufirst = u;
+    tile_coords(r.tile, q.tiles_m, q.tiles_n, q.tiles_m * q.tiles_n, group_m, r.b, r.tm, r.tn);
+    r.kb0 = 0;
+    r.kb1 = q.num_kb;
+    return r;
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ Unit decode(const MmaArgs &a, const TableOf<GROUPED> &g, int u, int &hint)
+{
+    if constexpr (GROUPED)
+        return decode_grouped(g, a.group_m, u, hint);
+    else
+        return decode_unit(a, u);
 }
 
 __device__ __forceinline__ void tma_load(const void *tmap, bool is3d, uint32_t dst, uint32_t bar, int c0,
@@ -330,11 +370,15 @@ __device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int
 //   CTA's "full" barriers; its MMA commits arrive on both CTAs' "empty" and
 //   "tmem full" barriers; both CTAs' epilogues release the accumulator on
 //   the even CTA's "tmem empty" barrier.
-template <int BN, int CG>
+//
+// GROUPED: the units are the tiles of several problems (a GroupTable); each
+// warp switches descriptors and epilogue fields when its next unit belongs
+// to another problem.
+template <int BN, int CG, bool GROUPED>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
-               const MmaArgs args)
+               const MmaArgs args, const __grid_constant__ TableOf<GROUPED> gt)
 {
     constexpr int BNL = BN / CG;                   // B columns loaded by this CTA
     constexpr int STAGE = stage_bytes(BN, CG);
@@ -380,10 +424,12 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         fence_barrier_init();
     }
     if (warp == 4 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        if (args.c_tma) prefetch_tmap(&tmC);
-        if (args.ws) prefetch_tmap(&tmW);
+        if constexpr (!GROUPED) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+            if (args.c_tma) prefetch_tmap(&tmC);
+            if (args.ws) prefetch_tmap(&tmW);
+        }
         // let the split-K reduction kernel (if any) launch early; it waits
         // for this grid to finish before it reads the partial tiles
         griddep_launch_dependents();
@@ -408,8 +454,19 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            int hint = 0;
             for (int u = cluster; ok && u < args.total_units; u += nclusters) {
-                const Unit w = decode_unit(args, u);
+                const Unit w = decode<GROUPED>(args, gt, u, hint);
+                const CUtensorMap *mapA = &tmA, *mapB = &tmB;
+                int a_kmajor = args.a_kmajor, b_kmajor = args.b_kmajor;
+                bool a_3d = args.a_3d, b_3d = args.b_3d;
+                if constexpr (GROUPED) {
+                    mapA = &gt.tmA[w.p];
+                    mapB = &gt.tmB[w.p];
+                    a_kmajor = gt.info[w.p].a_kmajor;
+                    b_kmajor = gt.info[w.p].b_kmajor;
+                    a_3d = b_3d = false;
+                }
                 const int m0 = w.tm * (BM * CG) + (int)rank * BM;
                 const int n0 = w.tn * BN + (int)rank * BNL;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -439,17 +496,17 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                             tma_load_2d_pair(dst, tm, fb, c0, c1);
                         }
                     };
-                    if (args.a_kmajor) {
-                        load(&tmA, args.a_3d, sa, k0, m0);
+                    if (a_kmajor) {
+                        load(mapA, a_3d, sa, k0, m0);
                     } else {
-                        load(&tmA, args.a_3d, sa, m0, k0);
-                        load(&tmA, args.a_3d, sa + 8192, m0 + 64, k0);
+                        load(mapA, a_3d, sa, m0, k0);
+                        load(mapA, a_3d, sa + 8192, m0 + 64, k0);
                     }
-                    if (args.b_kmajor) {
-                        load(&tmB, args.b_3d, sb, k0, n0);
+                    if (b_kmajor) {
+                        load(mapB, b_3d, sb, k0, n0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BNL / 64; ++j) load(&tmB, args.b_3d, sb + j * 8192, n0 + 64 * j, k0);
+                        for (int j = 0; j < BNL / 64; ++j) load(mapB, b_3d, sb + j * 8192, n0 + 64 * j, k0);
                     }
                     ++it;
                 }
@@ -466,8 +523,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (lane == 0 && rank == 0) {
             uint32_t it = 0, local = 0;
             bool ok = true;
+            int hint = 0;
             for (int u = cluster; ok && u < args.total_units; u += nclusters, ++local) {
-                const Unit w = decode_unit(args, u);
+                const Unit w = decode<GROUPED>(args, gt, u, hint);
+                int a_kmajor = args.a_kmajor, b_kmajor = args.b_kmajor;
+                uint32_t idesc = args.idesc;
+                if constexpr (GROUPED) {
+                    a_kmajor = gt.info[w.p].a_kmajor;
+                    b_kmajor = gt.info[w.p].b_kmajor;
+                    idesc = gt.info[w.p].idesc;
+                }
                 const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
                 if (!wait_bar(smem_u32(&tempty_bar[acc]), aph ^ 1u, watch, W_TMEM_EMPTY)) {
                     ok = false;
@@ -488,15 +553,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     for (int k = 0; k < BK / MMA_K; ++k) {
                         // K-major: advance 32 bytes along the swizzled row;
                         // MN-major: advance 16 rows of 128 bytes.
-                        const uint64_t ad = args.a_kmajor ? smem_desc_sw128(sa + 32 * k, 16, 1024)
-                                                          : smem_desc_sw128(sa + 2048 * k, 8192, 1024);
-                        const uint64_t bd = args.b_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
-                                                          : smem_desc_sw128(sb + 2048 * k, 8192, 1024);
+                        const uint64_t ad = a_kmajor ? smem_desc_sw128(sa + 32 * k, 16, 1024)
+                                                     : smem_desc_sw128(sa + 2048 * k, 8192, 1024);
+                        const uint64_t bd = b_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
+                                                     : smem_desc_sw128(sb + 2048 * k, 8192, 1024);
                         const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
                         if (CG == 1)
-                            mma_f16_ss(d_tmem, ad, bd, args.idesc, accum);
+                            mma_f16_ss(d_tmem, ad, bd, idesc, accum);
                         else
-                            mma_f16_ss_pair(d_tmem, ad, bd, args.idesc, accum);
+                            mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
                     }
                     if (CG == 1)
                         mma_commit(smem_u32(&empty_bar[stage]));
@@ -527,33 +592,57 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         uint32_t local = 0, ebuf = 0;
         const int row_in_tile = (int)rank * BM + warp * 32 + lane;
         uint8_t *my_stage = cstage + warp * 2 * EPI_STAGE_BYTES;
+        // grouped: the launch-wide arguments with the current problem's
+        // epilogue fields (M, N, C, ldc, dtype, alpha, beta) swapped in
+        MmaArgs ga = args;
+        const CUtensorMap *mapC = &tmC;
+        int cur_p = -1, hint = 0;
+        const MmaArgs &ea = GROUPED ? ga : args;
         // alpha/beta, then the chunk to C (TMA store when C allows it)
         auto emit = [&](int b, long long row, long long col0, float (&v)[32]) {
-            if (!args.c_tma) {
+            if (!ea.c_tma) {
                 // both staging buffers of this warp serve as one transpose buffer
                 float *xbuf = reinterpret_cast<float *>(my_stage);
-                apply_alpha_beta_staged(args, xbuf, lane, b, row - lane, col0, v);
-                store_staged(args, xbuf, lane, b, row - lane, col0, v);
+                apply_alpha_beta_staged(ea, xbuf, lane, b, row - lane, col0, v);
+                store_staged(ea, xbuf, lane, b, row - lane, col0, v);
                 return;
             }
-            apply_alpha_beta(args, b, row, col0, v);
-            if (args.c_tma) {
+            apply_alpha_beta(ea, b, row, col0, v);
+            if (ea.c_tma) {
                 // buffers alternate over the stores actually issued, so a
                 // buffer is reused only after one newer store was committed
                 const long long row0 = row - lane;
-                if (row0 < args.M && col0 < args.N) {
-                    store_tma(&tmC, args.c_3d, args.c_dtype, my_stage + ebuf * EPI_STAGE_BYTES, lane, b, row0,
+                if (row0 < ea.M && col0 < ea.N) {
+                    store_tma(mapC, ea.c_3d, ea.c_dtype, my_stage + ebuf * EPI_STAGE_BYTES, lane, b, row0,
                               col0, v);
                     ebuf ^= 1u;
                 }
             } else {
-                store_direct(args, b, row, col0, v);
+                store_direct(ea, b, row, col0, v);
             }
         };
         const uint32_t tempty_leader0 = CG == 2 ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
         const uint32_t tempty_leader1 = CG == 2 ? mapa_shared(smem_u32(&tempty_bar[1]), 0) : 0u;
         for (int u = cluster; u < args.total_units; u += nclusters, ++local) {
-            const Unit w = decode_unit(args, u);
+            const Unit w = decode<GROUPED>(args, gt, u, hint);
+            if constexpr (GROUPED) {
+                if (w.p != cur_p) {
+                    const GroupInfo &q = gt.info[w.p];
+                    ga.M = q.M;
+                    ga.N = q.N;
+                    ga.C = q.C;
+                    ga.ldc = q.ldc;
+                    ga.stride_c = 0;
+                    ga.c_dtype = q.c_dtype;
+                    ga.c_vec_ok = q.c_vec_ok;
+                    ga.c_tma = q.c_tma;
+                    ga.c_3d = 0;
+                    ga.alpha = q.alpha;
+                    ga.beta = q.beta;
+                    mapC = &gt.tmC[w.p];
+                    cur_p = w.p;
+                }
+            }
             const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
             bool ok = wait_bar(smem_u32(&tfull_bar[acc]), aph, watch, W_TMEM_FULL);
             ok = __all_sync(0xffffffffu, ok);
@@ -625,8 +714,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
 }
 
-template <int BN, int CG>
-cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st)
+template <int BN, int CG, bool GROUPED = false>
+cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
     constexpr int smem = mma_smem_bytes(BN, CG);
     static bool configured[64] = {};
@@ -634,16 +723,17 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st)
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(mma_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (CG == 2) {
-            e = cudaFuncSetAttribute(mma_kernel<BN, CG>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
         configured[dev] = true;
     }
     if (CG == 1) {
-        mma_kernel<BN, CG><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args);
+        mma_kernel<BN, CG, GROUPED><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -658,14 +748,15 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG>, L.tmA, L.tmB, L.tmC, L.tmW, L.args);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG, GROUPED>, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
 }
 
 template <int BN>
 int pairs_for()
 {
     constexpr int smem = mma_smem_bytes(BN, 2);
-    if (cudaFuncSetAttribute(mma_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(mma_kernel<BN, 2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
@@ -679,7 +770,7 @@ int pairs_for()
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<BN, 2>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<BN, 2, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -777,6 +868,16 @@ cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
     case 256: return launch_kernel<256, 1>(L, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_mma_grouped(const MmaLaunch &L, const GroupTable &g, cudaStream_t st)
+{
+    if (g.count < 1 || g.count > GROUP_MAX) return cudaErrorInvalidValue;
+    if (L.cg == 2 && L.bn == 256) return launch_kernel<256, 2, true>(L, st, g);
+    if (L.cg == 2 && L.bn == 128) return launch_kernel<128, 2, true>(L, st, g);
+    if (L.cg == 1 && L.bn == 256) return launch_kernel<256, 1, true>(L, st, g);
+    if (L.cg == 1 && L.bn == 128) return launch_kernel<128, 1, true>(L, st, g);
+    return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------- static scratch

@@ -285,6 +285,110 @@ def test_grouped_ragged(ctx):
     s.close()
 
 
+def _shifted(t, off):
+    """A device copy of t whose first element sits `off` elements past a
+    256-byte aligned allocation (so its base is misaligned for off % 8 != 0)."""
+    flat = torch.empty(off + t.numel(), dtype=t.dtype, device="cuda")
+    flat[off:] = t.reshape(-1).cuda()
+    return flat[off:]
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_repack_every_misalignment(ctx, ta, tb):
+    # every 2-byte offset of the base inside a 16-byte word, with odd leading
+    # dimensions: the repack kernel's shifted 16-byte loads and row tails
+    M, N, K = 150, 97, 203
+    for off in range(8):
+        a_cols, b_cols = (M if ta else K), (K if tb else N)
+        lda = a_cols + 2 * off + (1 - a_cols % 2)            # odd
+        ldb = b_cols + 2 * (7 - off) + (1 - b_cols % 2)      # odd
+        p = synthetic.make_problem(M, N, K, "f16", "f32", transpose_a=ta, transpose_b=tb, seed=400 + off,
+                                   dist="int", scale=3.0, lda=lda, ldb=ldb)
+        A, B, C = _shifted(p.A, off), _shifted(p.B, (off * 3) % 8), p.C.cuda()
+        d = tg.make_desc(M, N, K, "f16", "f32", transpose_a=ta, transpose_b=tb, lda=lda, ldb=ldb)
+        tg.tc_gemm(ctx, d, A, B, C)
+        assert "_packA_packB" in ctx.last_kernel
+        R, _ = oracle.gemm(p)
+        got = C.cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, R), f"offset {off}: {np.argwhere(got != R)[:5]}"
+
+
+def _grouped_specs():
+    """Problems of every dtype pair, layout, alpha/beta, aligned and ragged
+    shapes, padded leading dims, plus two fp32 problems; more than one
+    table of problems (the launch takes at most 64)."""
+    g = torch.Generator().manual_seed(91)
+    specs = []
+    for i in range(70):
+        ab, c = DT_PAIRS[i % 4]
+        ta, tb = LAYOUTS[(i // 4) % 4]
+        M, N, K = (int(v) for v in torch.randint(1, 400, (3,), generator=g))
+        if i % 5 == 0:
+            M, N, K = 128 * (1 + i % 3), 64 * (1 + i % 4), 64 * (1 + i % 5)   # TMA-aligned C
+        alpha, beta = [(1.0, 0.0), (0.5, 1.0), (-1.5, 0.25)][i % 3]
+        pad = (i % 7 == 3)
+        specs.append(dict(M=M, N=N, K=K, ab=ab, c=c, ta=ta, tb=tb, alpha=alpha, beta=beta, pad=pad,
+                          dist="int" if i % 2 else "normal"))
+    specs.append(dict(M=33, N=17, K=65, ab="f32", c="f32", ta=False, tb=True, alpha=1.0, beta=0.0,
+                      pad=False, dist="normal"))
+    specs.append(dict(M=70, N=90, K=9, ab="f32", c="f32", ta=True, tb=False, alpha=0.5, beta=1.0,
+                      pad=False, dist="int"))
+    return specs
+
+
+def _run_grouped(ctx, specs, seed0):
+    probs, descs, As, Bs, Cs = [], [], [], [], []
+    for j, sp in enumerate(specs):
+        a_cols = sp["M"] if sp["ta"] else sp["K"]
+        b_cols = sp["K"] if sp["tb"] else sp["N"]
+        lda, ldb, ldc = (a_cols + 5, b_cols + 8, sp["N"] + 3) if sp["pad"] else (0, 0, 0)
+        p = synthetic.make_problem(sp["M"], sp["N"], sp["K"], sp["ab"], sp["c"], transpose_a=sp["ta"],
+                                   transpose_b=sp["tb"], alpha=sp["alpha"], beta=sp["beta"], seed=seed0 + j,
+                                   dist=sp["dist"], scale=3.0,
+                                   c_fill=("int" if sp["dist"] == "int" else "uniform") if sp["beta"] else "zero",
+                                   lda=lda, ldb=ldb, ldc=ldc)
+        probs.append(p)
+        As.append(p.A.cuda())
+        Bs.append(p.B.cuda())
+        Cs.append(p.C.cuda())
+        descs.append(tg.make_desc(p.M, p.N, p.K, p.ab_dtype, p.c_dtype, transpose_a=p.transpose_a,
+                                  transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta,
+                                  lda=p.A.shape[1], ldb=p.B.shape[1], ldc=p.C.shape[1]))
+    s = tg.Stream(ctx)
+    tg.tc_gemm_grouped_async(ctx, descs, As, Bs, Cs, s)
+    s.sync()
+    s.close()
+    return probs, [C.cpu() for C in Cs]
+
+
+@pytest.mark.parametrize("spec", ["", "cg=1 bn=128", "cg=2 bn=128", "cg=1 bn=256", "store=direct",
+                                  "grouped=0"])
+def test_grouped_mixed(ctx, force, spec):
+    force(spec)
+    specs = _grouped_specs()
+    probs, outs = _run_grouped(ctx, specs, 500)
+    if spec != "grouped=0":
+        assert ctx.last_kernel.startswith("grouped_tcgen05_"), ctx.last_kernel
+    for sp, p, out in zip(specs, probs, outs):
+        R, T = oracle.gemm(p)
+        got = oracle.decode(out)[:, : p.N]
+        what = f"{spec or 'default'} {sp} {ctx.last_kernel}"
+        if sp["dist"] == "int" and p.c_dtype == "f32" and p.ab_dtype != "f32":
+            # integer data with alpha, beta in {1, 0.5, -1.5, 0.25}: exact
+            assert np.array_equal(got, R), what
+        else:
+            parity.check(got, R, T, p.c_dtype, exact_f32=(p.ab_dtype == "f32"), what=what)
+
+
+def test_grouped_deterministic(ctx):
+    specs = _grouped_specs()[:20]
+    _, first = _run_grouped(ctx, specs, 700)
+    _, second = _run_grouped(ctx, specs, 700)
+    bits = lambda t: t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+    for a, b in zip(first, second):
+        assert torch.equal(bits(a), bits(b))
+
+
 def test_torch_stream_wrap(ctx):
     ts = torch.cuda.Stream()
     s = tg.Stream(ctx, torch_stream=ts)
