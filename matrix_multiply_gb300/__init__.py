@@ -266,15 +266,33 @@ def tc_gemm_batched_async(ctx: Context, bd: tc_gemm_batched_desc, A, B, C, strea
                                       stream.ptr), "tc_gemm_batched_async")
 
 
+class GroupedGemm:
+    """The arguments of tc_gemm_grouped_async marshalled once: descriptors
+    and operand addresses in C arrays, capacities checked here.  enqueue()
+    then costs one C call, so that a group issued many times with the same
+    operands does not pay the per-problem Python work each time.  The
+    tensors stay referenced (alive) as long as this object."""
+
+    def __init__(self, descs, As, Bs, Cs):
+        n = len(descs)
+        if not (len(As) == len(Bs) == len(Cs) == n):
+            raise ValueError("descs, As, Bs and Cs must have the same length")
+        for d, a, b, c in zip(descs, As, Bs, Cs):
+            _check_capacity(d, a, b, c)
+        self.n = n
+        self._keep = (list(As), list(Bs), list(Cs))
+        self._descs = (tc_gemm_desc * n)(*descs)
+        self._A = (ctypes.c_void_p * n)(*[_addr(x) for x in As])
+        self._B = (ctypes.c_void_p * n)(*[_addr(x) for x in Bs])
+        self._C = (ctypes.c_void_p * n)(*[_addr(x) for x in Cs])
+
+    def enqueue(self, ctx: Context, stream: Stream):
+        _check(_lib.tc_gemm_grouped_async(ctx.ptr, self.n, self._descs, self._A, self._B, self._C, stream.ptr),
+               "tc_gemm_grouped_async")
+
+
 def tc_gemm_grouped_async(ctx: Context, descs, As, Bs, Cs, stream: Stream):
-    n = len(descs)
-    for d, a, b, c in zip(descs, As, Bs, Cs):
-        _check_capacity(d, a, b, c)
-    arr = (tc_gemm_desc * n)(*descs)
-    pa = (ctypes.c_void_p * n)(*[_addr(x) for x in As])
-    pb = (ctypes.c_void_p * n)(*[_addr(x) for x in Bs])
-    pc = (ctypes.c_void_p * n)(*[_addr(x) for x in Cs])
-    _check(_lib.tc_gemm_grouped_async(ctx.ptr, n, arr, pa, pb, pc, stream.ptr), "tc_gemm_grouped_async")
+    GroupedGemm(descs, As, Bs, Cs).enqueue(ctx, stream)
 
 
 def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):

@@ -18,7 +18,7 @@ namespace tc {
 namespace {
 
 constexpr int PACK_THREADS = 256;
-constexpr int PACK_ITEMS = 4;      // 16-byte output chunks per thread (loads in flight)
+constexpr int PACK_ITEMS = 8;      // 16-byte output chunks per thread (loads in flight)
 
 __device__ __forceinline__ uint32_t fsr(uint32_t lo, uint32_t hi, uint32_t sh) { return __funnelshift_r(lo, hi, sh); }
 
@@ -42,37 +42,67 @@ __device__ __forceinline__ uint4 window16(const uint4 &a, const uint4 &b, uint32
 // one or two aligned 16-byte words that hold its valid elements (each word
 // read holds at least one of them) and shifted into place.  The 16-byte
 // store may write past the row's last column into the row padding, which
-// nothing reads.
+// nothing reads.  Index = 32-bit unsigned when every copy has fewer than
+// 2^31 chunks (the divisions dominate the instruction count), else 64-bit.
+template <typename Index>
 __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const __grid_constant__ PackBatch pb)
 {
-    int e = 0;
-    while (e + 1 < pb.count && pb.block_begin[e + 1] <= (long long)blockIdx.x) ++e;
-    const PackArgs &p = pb.seg[e];
-    const long long chunks = (p.cols + 7) / 8;
-    const long long per_entry = p.rows * chunks;
-    const long long items = per_entry * p.batch;
-    const long long first = ((long long)blockIdx.x - pb.block_begin[e]) * (PACK_THREADS * PACK_ITEMS) + threadIdx.x;
+    // the copy this CTA works on: the last e with block_begin[e] <= blockIdx.x
+    int lo = 0, hi = pb.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pb.block_begin[mid] <= (long long)blockIdx.x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const PackArgs &p = pb.seg[lo];
+    const Index chunks = (Index)((p.cols + 7) / 8);
+    const Index rows = (Index)p.rows;
+    const Index per_entry = rows * chunks;
+    const Index items = per_entry * (Index)p.batch;
+    Index it = (Index)((long long)blockIdx.x - pb.block_begin[lo]) * (PACK_THREADS * PACK_ITEMS) + (Index)threadIdx.x;
+    if (it >= items) return;
+
+    // (entry, row, chunk) of the first item, then stepped by PACK_THREADS
+    // chunks per item without further divisions
+    Index b = 0, rem = it;
+    if (p.batch > 1) {
+        b = it / per_entry;
+        rem = it - b * per_entry;
+    }
+    Index r = rem / chunks, ch = rem - r * chunks;
+    const Index dr = PACK_THREADS / chunks, dc = PACK_THREADS - dr * chunks;
 
     uint4 q0[PACK_ITEMS], q1[PACK_ITEMS];
     uint32_t off[PACK_ITEMS];
     uint16_t *dst[PACK_ITEMS];
 #pragma unroll
     for (int k = 0; k < PACK_ITEMS; ++k) {
-        const long long it = first + (long long)k * PACK_THREADS;
         dst[k] = nullptr;
-        if (it >= items) continue;
-        const long long b = it / per_entry;
-        const long long rem = it - b * per_entry;
-        const long long r = rem / chunks;
-        const long long c = (rem - r * chunks) * 8;
-        const uint16_t *s = p.src + b * p.stride_src + r * p.ld_src + c;
-        const int valid = (int)min(8LL, p.cols - c);
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
-        off[k] = (uint32_t)(addr & 15u);
-        const uint4 *w = reinterpret_cast<const uint4 *>(addr - off[k]);
-        q0[k] = __ldg(w);
-        q1[k] = (off[k] + 2u * (uint32_t)valid > 16u) ? __ldg(w + 1) : make_uint4(0u, 0u, 0u, 0u);
-        dst[k] = p.dst + b * p.stride_dst + r * p.ld_dst + c;
+        if (it < items) {
+            const Index c = ch * 8;
+            const uint16_t *s = p.src + (long long)b * p.stride_src + (long long)r * p.ld_src + c;
+            const int valid = (int)min((long long)8, p.cols - (long long)c);
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
+            off[k] = (uint32_t)(addr & 15u);
+            const uint4 *w = reinterpret_cast<const uint4 *>(addr - off[k]);
+            q0[k] = __ldg(w);
+            q1[k] = (off[k] + 2u * (uint32_t)valid > 16u) ? __ldg(w + 1) : make_uint4(0u, 0u, 0u, 0u);
+            dst[k] = p.dst + (long long)b * p.stride_dst + (long long)r * p.ld_dst + c;
+        }
+        it += PACK_THREADS;
+        r += dr;
+        ch += dc;
+        if (ch >= chunks) {
+            ch -= chunks;
+            ++r;
+        }
+        if (r >= rows) {     // into a later batch entry (rows * chunks items each)
+            const Index q = r / rows;
+            b += q;
+            r -= q * rows;
+        }
     }
 #pragma unroll
     for (int k = 0; k < PACK_ITEMS; ++k)
@@ -85,17 +115,23 @@ cudaError_t launch_pack(PackBatch &pb, cudaStream_t st)
 {
     if (pb.count < 1 || pb.count > PACK_MAX) return cudaErrorInvalidValue;
     long long blocks = 0;
+    bool narrow = true;
     for (int i = 0; i < pb.count; ++i) {
         const PackArgs &p = pb.seg[i];
         if ((reinterpret_cast<uintptr_t>(p.dst) & 15u) || (p.ld_dst % 8) || (p.stride_dst % 8))
             return cudaErrorInvalidValue;
         const long long items = p.rows * ((p.cols + 7) / 8) * p.batch;
+        // 32-bit indices: every item index, plus one CTA's span, below 2^31
+        if (items + PACK_THREADS * PACK_ITEMS >= (1LL << 31)) narrow = false;
         pb.block_begin[i] = blocks;
         blocks += (items + PACK_THREADS * PACK_ITEMS - 1) / (PACK_THREADS * PACK_ITEMS);
     }
     pb.block_begin[pb.count] = blocks;
     if (blocks < 1 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    pack_kernel<<<(unsigned)blocks, PACK_THREADS, 0, st>>>(pb);
+    if (narrow)
+        pack_kernel<uint32_t><<<(unsigned)blocks, PACK_THREADS, 0, st>>>(pb);
+    else
+        pack_kernel<unsigned long long><<<(unsigned)blocks, PACK_THREADS, 0, st>>>(pb);
     return cudaGetLastError();
 }
 

@@ -283,6 +283,11 @@ __device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long 
 // instruction instead of 32 separate rows.
 constexpr int XPOSE_LD = 33;
 
+// Row r of the chunk in column `lane`: C + ((b * stride_c + (row0 + r) * ldc + col) elements.
+// Every access of the two functions below is unrolled and predicated (no
+// early exit), so the 32 row accesses of a lane are independent and in
+// flight together.
+
 // v <- alpha * v + beta * C_old, C_old read row-coalesced through `buf`
 __device__ __forceinline__ void apply_alpha_beta_staged(const MmaArgs &a, float *buf, int lane, int b,
                                                         long long row0, long long col0, float (&v)[32])
@@ -293,12 +298,28 @@ __device__ __forceinline__ void apply_alpha_beta_staged(const MmaArgs &a, float 
         return;
     }
     const long long col = col0 + lane;
-    for (int r = 0; r < 32; ++r) {
-        const long long row = row0 + r;
-        buf[r * XPOSE_LD + lane] = (row < a.M && col < a.N)
-                                       ? load_c(a.C, (long long)b * a.stride_c + row * a.ldc + col, a.c_dtype)
-                                       : 0.0f;
+    const long long nrows = (col < a.N) ? min(32LL, a.M - row0) : 0LL;
+    const long long first = (long long)b * a.stride_c + row0 * a.ldc + col;
+    float c[32];
+    if (a.c_dtype == TC_F32) {
+        const float *src = static_cast<const float *>(a.C) + first;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) c[r] = (r < nrows) ? src[r * a.ldc] : 0.0f;
+    } else {
+        const uint16_t *src = static_cast<const uint16_t *>(a.C) + first;
+        uint16_t h[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) h[r] = (r < nrows) ? src[r * a.ldc] : (uint16_t)0;
+        if (a.c_dtype == TC_BF16) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) c[r] = __bfloat162float(__ushort_as_bfloat16(h[r]));
+        } else {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) c[r] = __half2float(__ushort_as_half(h[r]));
+        }
     }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) buf[r * XPOSE_LD + lane] = c[r];
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = fmaf(a.beta, buf[lane * XPOSE_LD + j], a.alpha * v[j]);
@@ -313,12 +334,26 @@ __device__ __forceinline__ void store_staged(const MmaArgs &a, float *buf, int l
     for (int j = 0; j < 32; ++j) buf[lane * XPOSE_LD + j] = v[j];
     __syncwarp();
     const long long col = col0 + lane;
-    if (col < a.N) {
-        for (int r = 0; r < 32; ++r) {
-            const long long row = row0 + r;
-            if (row >= a.M) break;
-            store_c1(a.C, (long long)b * a.stride_c + row * a.ldc + col, buf[r * XPOSE_LD + lane], a.c_dtype);
-        }
+    const long long nrows = (col < a.N) ? min(32LL, a.M - row0) : 0LL;
+    const long long first = (long long)b * a.stride_c + row0 * a.ldc + col;
+    float w[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) w[r] = buf[r * XPOSE_LD + lane];
+    if (a.c_dtype == TC_F32) {
+        float *dst = static_cast<float *>(a.C) + first;
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            if (r < nrows) dst[r * a.ldc] = w[r];
+    } else if (a.c_dtype == TC_BF16) {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.C) + first;
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            if (r < nrows) dst[r * a.ldc] = __float2bfloat16_rn(w[r]);
+    } else {
+        __half *dst = static_cast<__half *>(a.C) + first;
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            if (r < nrows) dst[r * a.ldc] = __float2half_rn(w[r]);
     }
     __syncwarp();
 }
