@@ -685,8 +685,12 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * ACC_STRIDE;
             const long long row = (long long)w.tm * (BM * CG) + row_in_tile;
-            // accumulator fully read: hand it back to the MMA warp
+            // accumulator fully read: hand it back to the MMA warp (not after
+            // this CTA's last unit: nothing waits for it then, and the
+            // arrival would sit on the kernel's final critical path)
+            const bool more = u + nclusters < args.total_units;
             auto release = [&]() {
+                if (!more) return;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -731,8 +735,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 }
             }
         }
-        // every TMA store has finished before shared memory is released
-        if (lane == 0) bulk_wait<0>();
+        // every TMA store has read its shared-memory source before the CTA
+        // releases it (the global writes complete with the kernel)
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
     }
 
