@@ -10,11 +10,17 @@ tensorcore gemm.md "Surface" (row-major BLAS layout, ld = 0 means contiguous),
 the phobos matmul page ("matmul", "matmul_t", the "sgemm" alpha/beta
 epilogue).  Results are fp64 ``R`` plus the absolute-product sum ``T``.
 
+The fused epilogue (tessl architecture.md, "Fused Epilogue": C =
+activation(alpha * A@B + beta * C_prev + bias), bias per column, the
+GeluTanh activation) is applied here in fp64 on top of the same R, by
+``gemm_epilogue`` / ``gemm_epilogue_points``.
+
 Every function here is pinned by ``tests/test_oracle.py`` against things
 other than itself: exact rational brute force, numpy's float64 matmul on
 operands decoded by PyTorch, the worked 2x2 input of the Foundry metal.md
 "Quick Start", closed forms (identity, permutation, rank one, alpha/beta),
-and an exhaustive check of the half-precision decoders.
+an exhaustive check of the half-precision decoders, and, for the epilogue,
+PyTorch's tanh-approximated GELU in float64 and the GELU identities.
 """
 from __future__ import annotations
 
@@ -171,3 +177,48 @@ def decode(t: torch.Tensor, lib=None) -> np.ndarray:
 def num_threads(lib=None) -> int:
     lib = lib or load_library()
     return int(lib.oracle_num_threads())
+
+
+# ------------------------------------------------------------------ epilogue
+# tessl architecture.md, "Fused Epilogue": C = activation(alpha * A@B +
+# beta * C_prev + bias); the bias is one value per output column (a
+# row-stride-0 view, broadcast over the rows) stored in C's dtype; the
+# activation is none or GeluTanh.  The page names a clamped tanh without
+# printing it; the oracle uses the exact tanh (clamping only matters where
+# tanh is +-1 to working precision).
+
+SQRT_2_OVER_PI = float(np.sqrt(2.0 / np.pi))
+GELU_CUBIC = 0.044715
+ACTIVATIONS = ("none", "gelu_tanh")
+
+
+def gelu_tanh(x):
+    """GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(SQRT_2_OVER_PI * (x + GELU_CUBIC * x * x * x)))
+
+
+def apply_activation(y, activation: str):
+    if activation == "none":
+        return np.asarray(y, dtype=np.float64)
+    if activation == "gelu_tanh":
+        return gelu_tanh(y)
+    raise ValueError(activation)
+
+
+def gemm_epilogue(p, bias, activation: str, row0: int = 0, row1: int | None = None, lib=None):
+    """Rows [row0,row1) of activation(alpha*op(A)@op(B) + beta*C_old + bias)
+    (``bias`` a stored tensor of N values, or None), with T and the
+    pre-activation value: returns (R, T, Y) fp64, Y = R before activation."""
+    R, T = gemm(p, row0, row1, lib=lib)
+    Y = R if bias is None else R + decode(bias, lib=lib).reshape(1, -1)[:, : p.N]
+    return apply_activation(Y, activation), T, Y
+
+
+def gemm_epilogue_points(p, bias, activation: str, rows, cols, lib=None):
+    """gemm_epilogue at the listed (row, col) positions (1-D arrays)."""
+    R, T = gemm_points(p, rows, cols, lib=lib)
+    cols = np.asarray(cols, dtype=np.int64)
+    Y = R if bias is None else R + decode(bias, lib=lib).reshape(-1)[cols]
+    return apply_activation(Y, activation), T, Y
+

@@ -313,3 +313,99 @@ def test_row_band_matches_full():
     R, T = oracle.gemm(p)
     Rb, Tb = oracle.gemm(p, 7, 19)
     assert np.array_equal(Rb, R[7:19]) and np.array_equal(Tb, T[7:19])
+
+
+# ---------------------------------------------------------------- epilogue
+# tessl architecture.md, "Fused Epilogue": C = activation(alpha * A@B +
+# beta * C_prev + bias), bias one value per column, activation GeluTanh.
+
+def epilogue_pins_fail(gelu, epilogue):
+    """Failing epilogue pins for the given GELU and epilogue functions
+    (the oracle's own, or planted-mistake copies)."""
+    fails = []
+    # a library routine: PyTorch's tanh-approximated GELU in float64
+    x = np.concatenate([np.linspace(-12.0, 12.0, 4001), [0.0, -0.0, 1.0, -1.0, 3.0, 1e-8, -1e-8, 40.0, -40.0]])
+    ref = torch.nn.functional.gelu(torch.tensor(x, dtype=torch.float64), approximate="tanh").numpy()
+    # (absolute 1e-14: far in the negative tail 1 + tanh rounds to 0 or to
+    # a few ulp of 1 depending on the routine; the true value is ~1e-16)
+    if not np.allclose(gelu(x), ref, rtol=1e-12, atol=1e-14):
+        fails.append("gelu vs torch tanh-GELU")
+    # identities: gelu(x) - gelu(-x) = x; gelu(0) = 0; gelu(x) -> x for large x
+    y = np.linspace(-6.0, 6.0, 1201)
+    if not np.allclose(gelu(y) - gelu(-y), y, rtol=0, atol=1e-14):
+        fails.append("odd part")
+    if gelu(np.array([0.0]))[0] != 0.0 or abs(gelu(np.array([30.0]))[0] - 30.0) > 1e-12:
+        fails.append("gelu(0), gelu(30)")
+    # zero A: C = act(beta * C_old + bias), with bias broadcast over rows
+    # (M != N so a per-row bias cannot pass)
+    M, N, K = 5, 7, 3
+    g = torch.Generator().manual_seed(11)
+    Cold = (torch.rand(M, N, generator=g) * 4 - 2).to(torch.bfloat16)
+    bias = (torch.rand(N, generator=g) * 4 - 2).to(torch.bfloat16)
+    p = synthetic.Problem(M, N, K, "bf16", "bf16", False, False, 1.0, 0.5,
+                          torch.zeros(M, K, dtype=torch.bfloat16), torch.ones(K, N, dtype=torch.bfloat16), Cold)
+    pre = 0.5 * torch_decode(Cold) + torch_decode(bias)[None, :]
+    for act, f in (("none", lambda v: v), ("gelu_tanh", lambda v: torch.nn.functional.gelu(
+            torch.tensor(v), approximate="tanh").numpy())):
+        R, _, Y = epilogue(p, bias, act)
+        if not (np.allclose(Y, pre, rtol=1e-15, atol=0) and np.allclose(R, f(pre), rtol=1e-12, atol=1e-15)):
+            fails.append(f"zero A, bias, {act}")
+    # identity A: C = act(B + bias) on every column
+    p = synthetic.Problem(4, 6, 4, "f32", "f32", False, False, 1.0, 0.0, torch.eye(4),
+                          torch.arange(24, dtype=torch.float32).reshape(4, 6) / 8 - 1, torch.zeros(4, 6))
+    b = torch.tensor([0.5, -1.0, 0.25, 2.0, -3.0, 0.0])
+    R, _, _ = epilogue(p, b, "gelu_tanh")
+    want = torch.nn.functional.gelu(p.B.double() + b.double()[None, :], approximate="tanh").numpy()
+    if not np.allclose(R, want, rtol=1e-12, atol=1e-15):
+        fails.append("identity A")
+    return fails
+
+
+def test_epilogue_pins_pass_on_oracle():
+    assert epilogue_pins_fail(oracle.gelu_tanh, oracle.gemm_epilogue) == []
+
+
+def _wrong_cubic(x):
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(oracle.SQRT_2_OVER_PI * (x + 0.0447 * x ** 3)))
+
+
+def _wrong_scale(x):
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0) / np.pi * (x + oracle.GELU_CUBIC * x ** 3)))
+
+
+def _bias_after_activation(p, bias, act):
+    R, T = oracle.gemm(p)
+    Y = oracle.apply_activation(R, act)
+    return (Y if bias is None else Y + oracle.decode(bias).reshape(1, -1)), T, R
+
+
+def _bias_per_row(p, bias, act):
+    R, T = oracle.gemm(p)
+    bd = oracle.decode(bias).reshape(-1)
+    Y = R + np.resize(bd, p.M)[:, None]
+    return oracle.apply_activation(Y, act), T, Y
+
+
+EPILOGUE_MUTATIONS = {
+    "gelu cubic coefficient 0.0447": (_wrong_cubic, oracle.gemm_epilogue),
+    "gelu scale sqrt(2)/pi": (_wrong_scale, oracle.gemm_epilogue),
+    "bias added after the activation": (oracle.gelu_tanh, _bias_after_activation),
+    "bias indexed by row": (oracle.gelu_tanh, _bias_per_row),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EPILOGUE_MUTATIONS))
+def test_planted_epilogue_mistake_is_caught(name):
+    gelu, epi = EPILOGUE_MUTATIONS[name]
+    assert epilogue_pins_fail(gelu, epi) != [], f"planted mistake {name!r} went unnoticed"
+
+
+def test_epilogue_points_match_rows():
+    p = synthetic.make_problem(9, 11, 13, "f16", "f16", alpha=0.5, beta=1.0, seed=12, c_fill="uniform")
+    bias = (torch.linspace(-1, 1, 11)).to(torch.float16)
+    R, T, Y = oracle.gemm_epilogue(p, bias, "gelu_tanh")
+    ii, jj = np.meshgrid(np.arange(9), np.arange(11), indexing="ij")
+    Rp, Tp, Yp = oracle.gemm_epilogue_points(p, bias, "gelu_tanh", ii.ravel(), jj.ravel())
+    assert np.array_equal(Rp, R.ravel()) and np.array_equal(Tp, T.ravel()) and np.array_equal(Yp, Y.ravel())
