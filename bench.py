@@ -249,6 +249,15 @@ def workload_registry():
     }
     for n in synthetic.SQUARE_SIZES:
         reg[f"fp16_nn_square_{n}"] = (lambda n=n: [synthetic.fp16_nn_square(n)])
+
+    # the fused bias + GELU epilogue (tessl architecture.md, "Fused Epilogue")
+    def epilogue(shape):
+        p, bias = synthetic.bf16_epilogue(*shape)
+        p.bias, p.activation = bias, "gelu_tanh"
+        return [p]
+    for (m, n, k) in synthetic.EPILOGUE_SHAPES:
+        tag = f"{m}" if m == n == k else f"{m}x{n}x{k}"
+        reg[f"bf16_bias_gelu_{tag}"] = (lambda s=(m, n, k): epilogue(s))
     return reg
 
 
@@ -264,7 +273,8 @@ def roofline(probs, seconds, sms):
     es = {"f16": 2, "bf16": 2, "f32": 4}
     flops = sum(2.0 * p.M * p.N * p.K for p in probs)
     nbytes = sum(p.M * p.K * es[p.ab_dtype] + p.K * p.N * es[p.ab_dtype] +
-                 p.M * p.N * es[p.c_dtype] * (2 if p.beta != 0 else 1) for p in probs)
+                 p.M * p.N * es[p.c_dtype] * (2 if p.beta != 0 else 1) +
+                 (p.N * es[p.c_dtype] if getattr(p, "bias", None) is not None else 0) for p in probs)
     fp32 = probs[0].ab_dtype == "f32"
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -296,10 +306,17 @@ class Runner:
                                transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta) for p in probs]
         # a group's arguments are marshalled once; each step is one C call
         self.group = tg.GroupedGemm(self.d, self.A, self.B, self.C) if len(probs) > 1 else None
+        # the fused-epilogue workloads carry a bias and an activation
+        p0 = probs[0]
+        self.activation = getattr(p0, "activation", None)
+        self.bias = p0.bias.cuda() if getattr(p0, "bias", None) is not None else None
 
     def step(self):
         tg = self.tg
-        if len(self.probs) == 1:
+        if self.activation is not None:
+            tg.tc_gemm_epilogue_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.stream,
+                                      bias=self.bias, activation=self.activation)
+        elif len(self.probs) == 1:
             tg.tc_gemm_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.stream)
         else:
             self.group.enqueue(self.ctx, self.stream)

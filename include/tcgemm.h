@@ -63,7 +63,8 @@ typedef enum {
     TC_ERR_DEVICE_TIMEOUT = 10,    /* a kernel's bounded wait expired; it stopped early */
     TC_ERR_STRIDE = 11,            /* batched: negative stride */
     TC_ERR_VARIANT = 12,           /* a forced variant cannot serve this problem */
-    TC_ERR_SCRATCH = 13            /* tc_gemm_splitk_noalloc: more scratch than its static buffer holds */
+    TC_ERR_SCRATCH = 13,           /* tc_gemm_splitk_noalloc: more scratch than its static buffer holds */
+    TC_ERR_EPILOGUE = 14           /* fused epilogue: unknown activation, or f32 operands (see tc_gemm_epilogue) */
 } tc_status_t;
 
 /* tensorcore gemm.md, "Surface": the GEMM descriptor, field for field. */
@@ -83,6 +84,19 @@ typedef struct {
     int32_t batch;
     int64_t stride_a, stride_b, stride_c;
 } tc_gemm_batched_desc;
+
+/* tessl architecture.md, "Fused Epilogue": the operation
+ *   C = activation(alpha * op(A) @ op(B) + beta * C_prev + bias)
+ * computed in fp32 while the accumulator is on chip, with one rounding to
+ * c_dtype at the end.  `bias` is a DEVICE pointer to N values of c_dtype,
+ * one per output column (the page's row-stride-0 view: the same value for
+ * every row), or NULL for no bias; it must not overlap C.  GeluTanh is
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))). */
+typedef enum { TC_ACT_NONE = 0, TC_ACT_GELU_TANH = 1 } tc_activation_t;
+typedef struct {
+    const void *bias;
+    tc_activation_t activation;
+} tc_epilogue;
 
 typedef struct tc_ctx tc_ctx;
 typedef struct tc_stream tc_stream;
@@ -127,6 +141,18 @@ tc_status_t tc_gemm_batched_async(tc_ctx *ctx, const tc_gemm_batched_desc *bd, c
 tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d,
                                   const void *const *A, const void *const *B, void *const *C,
                                   tc_stream *s);
+/* GEMM with the fused bias + activation epilogue (tc_epilogue above); the
+ * same kernels, tiles, split-K and determinism as tc_gemm.  Refused with
+ * TC_ERR_EPILOGUE, nothing enqueued, for an unknown activation and for f32
+ * operands: the exact-fp32 kernel accumulates in registers per output with
+ * no separate epilogue to fuse into, and the page refuses that path rather
+ * than falling back to separate passes.  TC_ERR_NULL when epi is NULL,
+ * TC_ERR_OVERLAP when the bias overlaps C. */
+tc_status_t tc_gemm_epilogue(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                             const void *B, void *C);
+tc_status_t tc_gemm_epilogue_async(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi,
+                                   const void *A, const void *B, void *C, tc_stream *s);
+
 /* Same GEMM with HOST operands: copies A and B (and C when beta != 0) to the
  * device, runs, copies C back and waits.  Device buffers are cached in the
  * context.  Pinned host memory gives full copy bandwidth. */
@@ -174,6 +200,8 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
 tc_status_t tc_gemm_validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C);
 tc_status_t tc_gemm_batched_validate(const tc_gemm_batched_desc *bd, const void *A,
                                      const void *B, const void *C);
+tc_status_t tc_gemm_epilogue_validate(const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                                      const void *B, const void *C);
 /* Host-only: the kernel variant the dispatcher would pick for this problem
  * on a GPU with num_sms SMs, written into buf (NUL-terminated, truncated to
  * len).  A, B, C are inspected for 16-byte alignment only. */

@@ -32,7 +32,7 @@ STATUS = {
     0: "TC_OK", 1: "TC_ERR_NULL", 2: "TC_ERR_DIM", 3: "TC_ERR_LD", 4: "TC_ERR_DTYPE",
     5: "TC_ERR_SCALAR", 6: "TC_ERR_OVERLAP", 7: "TC_ERR_OVERFLOW", 8: "TC_ERR_ALIGN_UNSUPPORTED",
     9: "TC_ERR_CUDA", 10: "TC_ERR_DEVICE_TIMEOUT", 11: "TC_ERR_STRIDE", 12: "TC_ERR_VARIANT",
-    13: "TC_ERR_SCRATCH",
+    13: "TC_ERR_SCRATCH", 14: "TC_ERR_EPILOGUE",
 }
 for _code, _name in STATUS.items():
     globals()[_name] = _code
@@ -47,6 +47,16 @@ class tc_gemm_desc(ctypes.Structure):
         ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
         ("lda", ctypes.c_int32), ("ldb", ctypes.c_int32), ("ldc", ctypes.c_int32),
     ]
+
+
+TC_ACT_NONE, TC_ACT_GELU_TANH = 0, 1
+_ACTIVATIONS = {None: TC_ACT_NONE, "none": TC_ACT_NONE, "gelu_tanh": TC_ACT_GELU_TANH}
+
+
+class tc_epilogue(ctypes.Structure):
+    """Fused epilogue: bias (device pointer to N values of C's dtype, or
+    None) and activation (TC_ACT_*)."""
+    _fields_ = [("bias", ctypes.c_void_p), ("activation", ctypes.c_int)]
 
 
 class tc_gemm_batched_desc(ctypes.Structure):
@@ -72,6 +82,7 @@ def _load():
     vp, st = ctypes.c_void_p, ctypes.c_int
     D = ctypes.POINTER(tc_gemm_desc)
     BD = ctypes.POINTER(tc_gemm_batched_desc)
+    E = ctypes.POINTER(tc_epilogue)
     sig = {
         "tc_ctx_create": (st, [ctypes.POINTER(vp), ctypes.c_int]),
         "tc_ctx_destroy": (None, [vp]),
@@ -86,6 +97,9 @@ def _load():
         "tc_gemm_batched_async": (st, [vp, BD, vp, vp, vp, vp]),
         "tc_gemm_grouped_async": (st, [vp, ctypes.c_int, D, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                        ctypes.POINTER(vp), vp]),
+        "tc_gemm_epilogue": (st, [vp, D, E, vp, vp, vp]),
+        "tc_gemm_epilogue_async": (st, [vp, D, E, vp, vp, vp, vp]),
+        "tc_gemm_epilogue_validate": (st, [D, E, vp, vp, vp]),
         "tc_gemm_host": (st, [vp, D, vp, vp, vp]),
         "tc_gemm_splitk_noalloc": (st, [D, vp, vp, vp, ctypes.c_int, vp]),
         "tc_gemm_validate": (st, [D, vp, vp, vp]),
@@ -109,7 +123,7 @@ EXPORTED = (
     "tc_gemm_batched_async", "tc_gemm_grouped_async", "tc_gemm_host", "tc_gemm_splitk_noalloc",
     "tc_gemm_validate",
     "tc_gemm_batched_validate", "tc_gemm_plan", "tc_last_kernel", "tc_launch_count",
-    "tc_status_string",
+    "tc_status_string", "tc_gemm_epilogue", "tc_gemm_epilogue_async", "tc_gemm_epilogue_validate",
 )
 
 
@@ -293,6 +307,45 @@ class GroupedGemm:
 
 def tc_gemm_grouped_async(ctx: Context, descs, As, Bs, Cs, stream: Stream):
     GroupedGemm(descs, As, Bs, Cs).enqueue(ctx, stream)
+
+
+def make_epilogue(bias=None, activation=None) -> tc_epilogue:
+    """bias: a CUDA tensor of N values in C's dtype (or an address, or
+    None); activation: None/"none" or "gelu_tanh" (or a TC_ACT_* code)."""
+    act = _ACTIVATIONS.get(activation, activation)
+    return tc_epilogue(_addr(bias) or None, int(act))
+
+
+def _check_bias(d: tc_gemm_desc, bias):
+    if bias is None or isinstance(bias, int):
+        return
+    _require(bias, d.N, "bias")
+    if d.c_dtype in (TC_F16, TC_BF16, TC_F32) and _torch_dtype_code(bias) != d.c_dtype:
+        raise ValueError("bias must have C's dtype")
+
+
+def tc_gemm_epilogue(ctx: Context, d: tc_gemm_desc, A, B, C, bias=None, activation=None):
+    """C = activation(alpha*op(A)@op(B) + beta*C + bias), synchronously."""
+    _check_capacity(d, A, B, C)
+    _check_bias(d, bias)
+    e = make_epilogue(bias, activation)
+    _check(_lib.tc_gemm_epilogue(ctx.ptr, ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C)),
+           "tc_gemm_epilogue")
+
+
+def tc_gemm_epilogue_async(ctx: Context, d: tc_gemm_desc, A, B, C, stream: Stream, bias=None, activation=None):
+    _check_capacity(d, A, B, C)
+    _check_bias(d, bias)
+    e = make_epilogue(bias, activation)
+    _check(_lib.tc_gemm_epilogue_async(ctx.ptr, ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C),
+                                       stream.ptr), "tc_gemm_epilogue_async")
+
+
+def tc_gemm_epilogue_validate(d: tc_gemm_desc, bias=None, activation=None, A=1 << 20, B=2 << 40,
+                              C=3 << 40) -> int:
+    """Host-only validation status of a fused-epilogue call."""
+    e = make_epilogue(bias, activation)
+    return int(_lib.tc_gemm_epilogue_validate(ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C)))
 
 
 def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):

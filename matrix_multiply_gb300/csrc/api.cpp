@@ -380,9 +380,10 @@ tc_status_t read_status(tc_stream *s)
     return TC_OK;
 }
 
-// Enqueue one validated, planned problem on stream s.
+// Enqueue one validated, planned problem on stream s (epi: the fused
+// bias/activation epilogue, or null).
 tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Plan &p, const void *A,
-                    const void *B, void *C, tc_stream *s)
+                    const void *B, void *C, tc_stream *s, const tc_epilogue *epi = nullptr)
 {
     cudaError_t e;
     if (p.ffma) {
@@ -497,6 +498,8 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.c_3d = n.batch > 1;
     a.ws = p.split > 1 ? reinterpret_cast<float *>(ws + a_pack_bytes + b_pack_bytes) : nullptr;
     a.status = s->status_dev;
+    a.bias = epi ? epi->bias : nullptr;
+    a.act = epi ? (int)epi->activation : (int)TC_ACT_NONE;
     const int64_t kb_per_unit = a.num_kb;
     a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
     {
@@ -551,6 +554,8 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         r.stride_c = a.stride_c;
         r.c_dtype = d->c_dtype;
         r.c_vec_ok = aligned16(C) && n.ldc % 4 == 0 && a.stride_c % 4 == 0;   // 4-element vectors
+        r.bias = a.bias;
+        r.act = a.act;
         const int64_t work = (int64_t)r.ntiles * rows_per_tile * (p.bn / 4);
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), (int64_t)ctx->num_sms * 8));
         if ((e = launch_reduce(r, grid, s->st)) != cudaSuccess) return TC_ERR_CUDA;
@@ -558,6 +563,8 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     }
     ctx->launches += launches;
     ctx->last = p.name;
+    if (a.bias) ctx->last += "_bias";
+    if (a.act == TC_ACT_GELU_TANH) ctx->last += "_gelu";
     return TC_OK;
 }
 
@@ -756,18 +763,31 @@ tc_status_t enqueue_grouped(tc_ctx *ctx, int n, const tc_gemm_desc *d, const voi
     return TC_OK;
 }
 
+// The fused epilogue's own checks (after the GEMM's): an activation this
+// library knows, a tensor-core path to fuse into, a bias apart from C.
+tc_status_t validate_epilogue(const tc_gemm_desc *d, const Norm &n, const tc_epilogue *epi, const void *C)
+{
+    if (!epi) return TC_ERR_NULL;
+    if (epi->activation != TC_ACT_NONE && epi->activation != TC_ACT_GELU_TANH) return TC_ERR_EPILOGUE;
+    if (d->a_dtype == TC_F32) return TC_ERR_EPILOGUE;
+    if (epi->bias && ranges_overlap(epi->bias, (int64_t)d->N * (int64_t)elem_size(d->c_dtype), C, n.c_bytes))
+        return TC_ERR_OVERLAP;
+    return TC_OK;
+}
+
 tc_status_t run(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B, void *C, int64_t batch,
-                int64_t sa, int64_t sb, int64_t sc, tc_stream *s)
+                int64_t sa, int64_t sb, int64_t sc, tc_stream *s, const tc_epilogue *epi = nullptr)
 {
     if (!ctx || !s) return TC_ERR_NULL;
     Norm n;
     tc_status_t st = validate(d, A, B, C, batch, sa, sb, sc, &n);
     if (st != TC_OK) return st;
+    if (epi && (st = validate_epilogue(d, n, epi, C)) != TC_OK) return st;
     Plan p;
     if ((st = make_plan(d, n, A, B, ctx->num_sms, &p)) != TC_OK) return st;
     std::lock_guard<std::mutex> g(ctx->mu);
     if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
-    return enqueue(ctx, d, n, p, A, B, C, s);
+    return enqueue(ctx, d, n, p, A, B, C, s, epi);
 }
 
 tc_status_t stream_init(tc_ctx *ctx, tc_stream *s)
@@ -815,6 +835,7 @@ const char *tc_status_string(tc_status_t st)
     case TC_ERR_STRIDE: return "invalid batch stride";
     case TC_ERR_VARIANT: return "forced variant cannot serve this problem";
     case TC_ERR_SCRATCH: return "problem needs more scratch than the static buffer of tc_gemm_splitk_noalloc holds";
+    case TC_ERR_EPILOGUE: return "fused epilogue refused: unknown activation, or f32 operands (exact-fp32 path)";
     }
     return "unknown status";
 }
@@ -927,6 +948,22 @@ tc_status_t tc_gemm(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const voi
     return tc_stream_sync(ctx->def);
 }
 
+tc_status_t tc_gemm_epilogue_async(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                                   const void *B, void *C, tc_stream *s)
+{
+    if (!epi) return TC_ERR_NULL;
+    return run(ctx, d, A, B, C, 1, 0, 0, 0, s, epi);
+}
+
+tc_status_t tc_gemm_epilogue(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                             const void *B, void *C)
+{
+    if (!ctx) return TC_ERR_NULL;
+    tc_status_t st = tc_gemm_epilogue_async(ctx, d, epi, A, B, C, ctx->def);
+    if (st != TC_OK) return st;
+    return tc_stream_sync(ctx->def);
+}
+
 tc_status_t tc_gemm_batched_async(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A, const void *B,
                                   void *C, tc_stream *s)
 {
@@ -1016,6 +1053,15 @@ tc_status_t tc_gemm_batched_validate(const tc_gemm_batched_desc *bd, const void 
     if (!bd) return TC_ERR_NULL;
     Norm n;
     return validate(&bd->base, A, B, C, bd->batch, bd->stride_a, bd->stride_b, bd->stride_c, &n);
+}
+
+tc_status_t tc_gemm_epilogue_validate(const tc_gemm_desc *d, const tc_epilogue *epi, const void *A, const void *B,
+                                      const void *C)
+{
+    Norm n;
+    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n);
+    if (st != TC_OK) return st;
+    return validate_epilogue(d, n, epi, C);
 }
 
 tc_status_t tc_gemm_plan(const tc_gemm_desc *d, const void *A, const void *B, const void *C, int num_sms, char *buf,

@@ -70,6 +70,10 @@ struct MmaArgs {
     unsigned *status;      // device status word (0 = fine)
     unsigned long long timeout_ns;
     int debug_drop_tfull;  // test hook: never signal the first tile's accumulator
+    // fused epilogue: bias (N values of c_dtype, or null) and activation
+    // (TC_ACT_*) applied after alpha/beta, before the one rounding
+    const void *bias;
+    int act;
 };
 
 struct MmaLaunch {
@@ -124,6 +128,8 @@ struct ReduceArgs {
     void *C;
     long long ldc, stride_c;
     int c_dtype, c_vec_ok;
+    const void *bias;      // fused epilogue, as in MmaArgs
+    int act;
 };
 cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st);
 

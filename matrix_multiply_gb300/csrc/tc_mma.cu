@@ -245,6 +245,37 @@ __device__ __forceinline__ void apply_alpha_beta(const MmaArgs &a, int b, long l
     }
 }
 
+// Fused epilogue (tessl architecture.md, "Fused Epilogue"): activation(y +
+// bias[col]) in fp32 on the value y = alpha * acc + beta * C_old.
+// GeluTanh: 0.5 x (1 + tanh(z)), z = sqrt(2/pi) (x + 0.044715 x^3),
+// evaluated through the identity 1 + tanh(z) = 2 / (1 + exp(-2z)) as
+// x / (1 + exp(-2z)) with the __expf intrinsic: a few instructions, and a
+// relative error of about 1e-6 (the intrinsic's error in exp, damped by
+// e / (1 + e)).  Large positive z gives x; large negative z overflows exp to
+// +inf and gives -0.
+__device__ __forceinline__ float gelu_tanh(float x)
+{
+    const float z = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    return __fdividef(x, 1.0f + __expf(-2.0f * z));
+}
+
+// The warp's chunk, lane = row, v[j] = column col0 + j: add the column's
+// bias (each lane loads one column's value, shared by shuffles) and apply
+// the activation.  Every lane of the warp calls it.
+__device__ __forceinline__ void bias_act(const MmaArgs &a, int lane, long long col0, float (&v)[32])
+{
+    if (a.bias) {
+        const long long col = col0 + lane;
+        const float bl = (col < a.N) ? load_c(a.bias, col, a.c_dtype) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, bl, j);
+    }
+    if (a.act == TC_ACT_GELU_TANH) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+    }
+}
+
 // C[row, col0 .. col0+31] = v with plain stores (C not readable by TMA)
 __device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long row, long long col0,
                                              const float (&v)[32])
@@ -409,7 +440,10 @@ __device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int
 // GROUPED: the units are the tiles of several problems (a GroupTable); each
 // warp switches descriptors and epilogue fields when its next unit belongs
 // to another problem.
-template <int BN, int CG, bool GROUPED>
+//
+// EPI: the fused bias/activation epilogue is compiled in (the plain GEMM
+// kernels carry none of its code).
+template <int BN, int CG, bool GROUPED, bool EPI>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -639,10 +673,12 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 // both staging buffers of this warp serve as one transpose buffer
                 float *xbuf = reinterpret_cast<float *>(my_stage);
                 apply_alpha_beta_staged(ea, xbuf, lane, b, row - lane, col0, v);
+                if constexpr (EPI) bias_act(ea, lane, col0, v);
                 store_staged(ea, xbuf, lane, b, row - lane, col0, v);
                 return;
             }
             apply_alpha_beta(ea, b, row, col0, v);
+            if constexpr (EPI) bias_act(ea, lane, col0, v);
             if (ea.c_tma) {
                 // buffers alternate over the stores actually issued, so a
                 // buffer is reused only after one newer store was committed
@@ -754,7 +790,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
 }
 
-template <int BN, int CG, bool GROUPED = false>
+template <int BN, int CG, bool GROUPED = false, bool EPI = false>
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
     constexpr int smem = mma_smem_bytes(BN, CG);
@@ -764,16 +800,16 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (CG == 2) {
-            e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
         configured[dev] = true;
     }
     if (CG == 1) {
-        mma_kernel<BN, CG, GROUPED><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+        mma_kernel<BN, CG, GROUPED, EPI><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -788,14 +824,14 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG, GROUPED>, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG, GROUPED, EPI>, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
 }
 
 template <int BN>
 int pairs_for()
 {
     constexpr int smem = mma_smem_bytes(BN, 2);
-    if (cudaFuncSetAttribute(mma_kernel<BN, 2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(mma_kernel<BN, 2, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -810,7 +846,7 @@ int pairs_for()
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<BN, 2, false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<BN, 2, false, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -857,6 +893,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
         for (int j = 0; j < 4; ++j) {
             const float c = (r.beta != 0.0f && gcol + j < r.N) ? load_c(r.C, base + j, r.c_dtype) : 0.0f;
             v[j] = (r.beta != 0.0f) ? fmaf(r.beta, c, r.alpha * v[j]) : r.alpha * v[j];
+            if (r.bias && gcol + j < r.N) v[j] += load_c(r.bias, gcol + j, r.c_dtype);
+            if (r.act == TC_ACT_GELU_TANH) v[j] = gelu_tanh(v[j]);
         }
         if (r.c_vec_ok && gcol + 4 <= r.N) {
             if (r.c_dtype == TC_F32) {
@@ -894,18 +932,19 @@ cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st)
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
+    const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE;
     if (L.cg == 2) {
         switch (L.bn) {
-        case 128: return launch_kernel<128, 2>(L, st);
-        case 256: return launch_kernel<256, 2>(L, st);
+        case 128: return epi ? launch_kernel<128, 2, false, true>(L, st) : launch_kernel<128, 2>(L, st);
+        case 256: return epi ? launch_kernel<256, 2, false, true>(L, st) : launch_kernel<256, 2>(L, st);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (L.bn) {
-    case 64: return launch_kernel<64, 1>(L, st);
-    case 128: return launch_kernel<128, 1>(L, st);
-    case 192: return launch_kernel<192, 1>(L, st);
-    case 256: return launch_kernel<256, 1>(L, st);
+    case 64: return epi ? launch_kernel<64, 1, false, true>(L, st) : launch_kernel<64, 1>(L, st);
+    case 128: return epi ? launch_kernel<128, 1, false, true>(L, st) : launch_kernel<128, 1>(L, st);
+    case 192: return epi ? launch_kernel<192, 1, false, true>(L, st) : launch_kernel<192, 1>(L, st);
+    case 256: return epi ? launch_kernel<256, 1, false, true>(L, st) : launch_kernel<256, 1>(L, st);
     default: return cudaErrorInvalidValue;
     }
 }

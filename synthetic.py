@@ -149,3 +149,19 @@ def fp16_ragged(count: int = 64, lo: int = 1, hi: int = 3000, seed: int = 4):
     """64 independent fp16 NN problems, M,N,K ~ U[1,3000], contiguous, uniform[-1,1]."""
     g, shapes = ragged_shapes(count, lo, hi, seed)
     return [make_problem(M, N, K, "f16", "f16", gen=g, dist="uniform") for (M, N, K) in shapes]
+
+
+# The fused bias + GELU epilogue (tessl architecture.md, "Fused Epilogue"):
+# the page times 512^3, 1024^3 and 2048x2048x512 with bf16 operands.
+EPILOGUE_SHAPES = ((512, 512, 512), (1024, 1024, 1024), (2048, 2048, 512))
+
+
+def bf16_epilogue(M: int, N: int, K: int, seed: int = 5):
+    """bf16 NN, bf16 out, alpha=1 beta=0, A and B normal(0,1) then the bias
+    (N values, normal(0,1), bf16) from the same fresh generator.  Returns
+    (problem, bias)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    p = make_problem(M, N, K, "bf16", "bf16", gen=g, dist="normal", scale=1.0)
+    bias = _draw(g, (N,), "normal", 1.0).to(torch.bfloat16)
+    return p, bias
+

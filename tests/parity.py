@@ -39,6 +39,44 @@ def bound(R, T, c_dtype: str, exact_f32: bool = False) -> np.ndarray:
     return b
 
 
+# Largest slope of the tanh-form GELU (near x = 1.5); an error e in its
+# argument moves the output by at most GELU_LIPSCHITZ * e.
+GELU_LIPSCHITZ = 1.13
+
+
+def bound_epilogue(R, T, Y, bias_abs, c_dtype: str, activation: str) -> np.ndarray:
+    """Bound for C = act(alpha*acc + beta*C_old + bias) against the oracle's
+    R = act(Y): the GEMM's 1e-4*T plus the fp32 roundings of the bias add
+    (2^-20 of |Y| + |bias|), carried through the activation's slope, plus
+    the fp32 evaluation of GELU (2e-6 |Y|: the device forms x / (1 +
+    exp(-2z)) with a fast exp of relative error below ~1.5e-6 for the
+    arguments that matter, plus a few ulp in z and the division) and one
+    output ulp for f16/bf16."""
+    Y = np.abs(np.asarray(Y, dtype=np.float64))
+    pre = 1e-4 * T + 2.0 ** -20 * (Y + bias_abs)
+    if activation == "gelu_tanh":
+        b = GELU_LIPSCHITZ * pre + 2e-6 * Y + 1e-30
+    else:
+        b = pre
+    if c_dtype in ("bf16", "f16"):
+        b = b + ulp_out(R, c_dtype)
+    return b
+
+
+def check_epilogue(C, R, T, Y, bias_abs, c_dtype: str, activation: str, what: str = "") -> dict:
+    """Assert the fused-epilogue bound per element; return error statistics."""
+    C = np.asarray(C, dtype=np.float64)
+    err = np.abs(C - R)
+    lim = bound_epilogue(R, T, Y, bias_abs, c_dtype, activation)
+    bad = ~(err <= lim)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        detail = ", ".join(f"{tuple(int(v) for v in i)}: got {C[tuple(i)]!r} want {R[tuple(i)]!r} "
+                           f"(lim={lim[tuple(i)]:.3g})" for i in idx)
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} elements out of bound; {detail}")
+    return {"max_err": float(err.max()) if err.size else 0.0, "n": int(err.size)}
+
+
 def check(C: np.ndarray, R: np.ndarray, T: np.ndarray, c_dtype: str,
           exact_f32: bool = False, what: str = "") -> dict:
     """Assert the per-element bound; return error statistics."""

@@ -175,3 +175,22 @@ def test_plan_repacks_unaligned_operands():
     assert plan(100, 63, 64, "f16", "f16").endswith("_packB")          # ldb = 63
     assert "pack" not in plan(100, 64, 64, "f16", "f16")
     assert plan(100, 64, 64, "f16", "f16", A=(1 << 20) + 2).endswith("_packA")   # misaligned base
+
+
+# ---------------------------------------------------------- fused epilogue
+
+def test_epilogue_validation():
+    d = desc(M=64, N=48, K=32)
+    assert tg.tc_gemm_epilogue_validate(d, bias=1 << 30, activation="gelu_tanh") == tg.TC_OK
+    assert tg.tc_gemm_epilogue_validate(d, bias=None, activation=None) == tg.TC_OK
+    assert tg.tc_gemm_epilogue_validate(d, activation=7) == tg.TC_ERR_EPILOGUE
+    # the exact-fp32 path is refused (nothing to fuse into)
+    assert tg.tc_gemm_epilogue_validate(desc(a_dtype="f32", c_dtype="f32"), activation="gelu_tanh") \
+        == tg.TC_ERR_EPILOGUE
+    # a bias inside C's byte range (C at 3 << 40, 64 x 48 bf16)
+    assert tg.tc_gemm_epilogue_validate(d, bias=(3 << 40) + 64, activation="none") == tg.TC_ERR_OVERLAP
+    assert tg.tc_gemm_epilogue_validate(d, bias=(3 << 40) - 96, activation="none") == tg.TC_OK
+    # the GEMM's own checks come first
+    assert tg.tc_gemm_epilogue_validate(desc(M=0), activation="gelu_tanh") == tg.TC_ERR_DIM
+    lib = tg.library()
+    assert lib.tc_gemm_epilogue_validate(ctypes.byref(d), None, 1 << 20, 2 << 40, 3 << 40) == tg.TC_ERR_NULL
