@@ -72,7 +72,7 @@ def profile_traffic(src_hash: str):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("tc_mma.cu", "ptx.cuh", "internal.h"):
+    for name in ("tc_mma.cu", "ptx.cuh", "internal.h", "elem.cuh"):
         with open(os.path.join(ROOT, "matrix_multiply_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -258,6 +258,9 @@ def workload_registry():
     for (m, n, k) in synthetic.EPILOGUE_SHAPES:
         tag = f"{m}" if m == n == k else f"{m}x{n}x{k}"
         reg[f"bf16_bias_gelu_{tag}"] = (lambda s=(m, n, k): epilogue(s))
+    # the small-M decode shape (the skinny-product kernel)
+    for (m, n, k) in synthetic.DECODE_SHAPES:
+        reg[f"f16_decode_m{m}_{n}x{k}"] = (lambda s=(m, n, k): [synthetic.f16_decode(*s)])
     return reg
 
 

@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]
 SOURCES = ["api.cpp", "tc_mma.cu", "ffma.cu", "pack.cu"]
-HEADERS = ["internal.h", "ptx.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "elem.cuh"]
 
 
 def nvcc() -> str:

@@ -165,3 +165,15 @@ def bf16_epilogue(M: int, N: int, K: int, seed: int = 5):
     bias = _draw(g, (N,), "normal", 1.0).to(torch.bfloat16)
     return p, bias
 
+
+# The GEMV / small-M decode shape (tensorcore gemm.md: "M <= 4 GEMV", fp16
+# out, "the synthetic 7B decode shape"): activations x[M, K] times a weight
+# W stored [N, K] (transpose_b), with the layer sizes of a 7B model (hidden
+# 4096, MLP 11008).
+DECODE_SHAPES = ((1, 4096, 4096), (4, 11008, 4096), (4, 4096, 11008))
+
+
+def f16_decode(M: int, N: int, K: int, seed: int = 6) -> Problem:
+    """fp16 x[M, K] @ W[N, K]^T, fp16 out, normal(0,1) from a fresh generator."""
+    return make_problem(M, N, K, "f16", "f16", transpose_b=True, seed=seed, dist="normal")
+

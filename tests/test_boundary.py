@@ -194,3 +194,12 @@ def test_epilogue_validation():
     assert tg.tc_gemm_epilogue_validate(desc(M=0), activation="gelu_tanh") == tg.TC_ERR_DIM
     lib = tg.library()
     assert lib.tc_gemm_epilogue_validate(ctypes.byref(d), None, 1 << 20, 2 << 40, 3 << 40) == tg.TC_ERR_NULL
+
+
+def test_plan_skinny_products():
+    """M or N <= 8 stay on the tensor-core kernel (split-K when the tiles are
+    few); fp32 stays on the exact path."""
+    assert plan(4, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_splitk")
+    assert plan(1, 32000, 4096, "bf16", "bf16", tb=True).startswith("tcgen05_nt_bf16_bf16_128x")
+    assert plan(4096, 3, 4096, "bf16", "f32").startswith("tcgen05_nn_bf16_f32_128x")
+    assert plan(4, 256, 256, "f32", "f32").startswith("ffma_")
