@@ -153,6 +153,22 @@ tc_status_t tc_gemm_epilogue(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilog
 tc_status_t tc_gemm_epilogue_async(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi,
                                    const void *A, const void *B, void *C, tc_stream *s);
 
+/* Relaxed fp32 (tessl architecture.md, "GEMM Pipeline & Kernel Selection":
+ * a relaxed precision mode beside f32-exact): fp32 A and B (a_dtype ==
+ * b_dtype == TC_F32, so c_dtype == TC_F32) on the bf16 tensor cores.  Each
+ * value is split into two bf16 parts, x = hi + lo (+ less than 2^-16 |x|),
+ * and the three products hi*hi + hi*lo + lo*hi are summed by one tensor-core
+ * GEMM over 3K: every product is exact in fp32, so the result meets the
+ * 1e-4 * sum_k |a b| bound of the non-exact paths, at the bf16 rate divided
+ * by three (plus one pass that writes the split operands into a per-stream
+ * buffer the library owns).  Not bit-compatible with the exact path;
+ * deterministic run to run.  epi (may be NULL) adds the fused epilogue,
+ * which the exact path refuses.  TC_ERR_DTYPE for non-f32 operands. */
+tc_status_t tc_gemm_f32_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                                const void *B, void *C);
+tc_status_t tc_gemm_f32_relaxed_async(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi,
+                                      const void *A, const void *B, void *C, tc_stream *s);
+
 /* Same GEMM with HOST operands: copies A and B (and C when beta != 0) to the
  * device, runs, copies C back and waits.  Device buffers are cached in the
  * context.  Pinned host memory gives full copy bandwidth. */

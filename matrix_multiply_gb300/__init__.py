@@ -100,6 +100,8 @@ def _load():
         "tc_gemm_epilogue": (st, [vp, D, E, vp, vp, vp]),
         "tc_gemm_epilogue_async": (st, [vp, D, E, vp, vp, vp, vp]),
         "tc_gemm_epilogue_validate": (st, [D, E, vp, vp, vp]),
+        "tc_gemm_f32_relaxed": (st, [vp, D, E, vp, vp, vp]),
+        "tc_gemm_f32_relaxed_async": (st, [vp, D, E, vp, vp, vp, vp]),
         "tc_gemm_host": (st, [vp, D, vp, vp, vp]),
         "tc_gemm_splitk_noalloc": (st, [D, vp, vp, vp, ctypes.c_int, vp]),
         "tc_gemm_validate": (st, [D, vp, vp, vp]),
@@ -124,6 +126,7 @@ EXPORTED = (
     "tc_gemm_validate",
     "tc_gemm_batched_validate", "tc_gemm_plan", "tc_last_kernel", "tc_launch_count",
     "tc_status_string", "tc_gemm_epilogue", "tc_gemm_epilogue_async", "tc_gemm_epilogue_validate",
+    "tc_gemm_f32_relaxed", "tc_gemm_f32_relaxed_async",
 )
 
 
@@ -346,6 +349,25 @@ def tc_gemm_epilogue_validate(d: tc_gemm_desc, bias=None, activation=None, A=1 <
     """Host-only validation status of a fused-epilogue call."""
     e = make_epilogue(bias, activation)
     return int(_lib.tc_gemm_epilogue_validate(ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C)))
+
+
+def tc_gemm_f32_relaxed(ctx: Context, d: tc_gemm_desc, A, B, C, bias=None, activation=None):
+    """fp32 GEMM on the bf16 tensor cores through a two-part bf16 split of
+    each operand (see include/tcgemm.h), synchronously; optional fused
+    epilogue."""
+    _check_capacity(d, A, B, C)
+    _check_bias(d, bias)
+    e = make_epilogue(bias, activation)
+    _check(_lib.tc_gemm_f32_relaxed(ctx.ptr, ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C)),
+           "tc_gemm_f32_relaxed")
+
+
+def tc_gemm_f32_relaxed_async(ctx: Context, d: tc_gemm_desc, A, B, C, stream: Stream, bias=None, activation=None):
+    _check_capacity(d, A, B, C)
+    _check_bias(d, bias)
+    e = make_epilogue(bias, activation)
+    _check(_lib.tc_gemm_f32_relaxed_async(ctx.ptr, ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C),
+                                          stream.ptr), "tc_gemm_f32_relaxed_async")
 
 
 def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):

@@ -31,6 +31,8 @@ struct tc_stream {
     bool owned = false;
     void *ws = nullptr;              // repacked operands + split-K partials
     size_t ws_cap = 0;
+    void *rx = nullptr;              // relaxed fp32: the bf16 split operands
+    size_t rx_cap = 0;
     unsigned *status_host = nullptr; // mapped, pinned: kernels report timeouts here
     unsigned *status_dev = nullptr;
 };
@@ -790,6 +792,82 @@ tc_status_t run(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B
     return enqueue(ctx, d, n, p, A, B, C, s, epi);
 }
 
+// ------------------------------------------------------------ relaxed fp32
+// tessl architecture.md, "GEMM Pipeline & Kernel Selection": a relaxed
+// precision mode beside f32-exact for fp32 operands.  Here each fp32 value
+// x = hi + lo + e (hi = bf16(x), lo = bf16(x - hi), |e| <= 2^-16 |x|), and
+// op(A) op(B) ~= A_hi B_hi + A_hi B_lo + A_lo B_hi is ONE bf16 tensor-core
+// GEMM over K' = 3K of [A_hi | A_hi | A_lo] and [B_hi ; B_lo ; B_hi]: every
+// product is exact in fp32, the dropped terms are below 2^-15 |a b|, so the
+// result meets the 1e-4 * sum|ab| bound of the non-exact paths.
+
+tc_status_t ensure_rx(tc_stream *s, size_t bytes)
+{
+    if (bytes <= s->rx_cap) return TC_OK;
+    const size_t cap = round_up(bytes + bytes / 4, (size_t)1 << 20);
+    if (s->rx) {
+        cudaError_t e = cudaFreeAsync(s->rx, s->st);
+        s->rx = nullptr;
+        s->rx_cap = 0;
+        if (e != cudaSuccess) return TC_ERR_CUDA;
+    }
+    if (cudaMallocAsync(&s->rx, cap, s->st) != cudaSuccess) {
+        s->rx = nullptr;
+        return TC_ERR_CUDA;
+    }
+    s->rx_cap = cap;
+    return TC_OK;
+}
+
+tc_status_t run_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A, const void *B,
+                        void *C, tc_stream *s)
+{
+    if (!ctx || !s) return TC_ERR_NULL;
+    Norm n;
+    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n);
+    if (st != TC_OK) return st;
+    if (d->a_dtype != TC_F32) return TC_ERR_DTYPE;
+    if (epi) {
+        if (epi->activation != TC_ACT_NONE && epi->activation != TC_ACT_GELU_TANH) return TC_ERR_EPILOGUE;
+        if (epi->bias && ranges_overlap(epi->bias, (int64_t)d->N * 4, C, n.c_bytes)) return TC_ERR_OVERLAP;
+    }
+    if ((int64_t)d->K * 3 > INT32_MAX) return TC_ERR_OVERFLOW;
+    // the split copies: the K dimension (A's columns unless transposed, B's
+    // rows unless transposed) tripled, rows padded to 64 elements
+    const bool a_kcols = !d->transpose_a, b_kcols = d->transpose_b;
+    const int64_t a_rows = a_kcols ? n.a_rows : 3 * n.a_rows, a_cols = a_kcols ? 3 * n.a_cols : n.a_cols;
+    const int64_t b_rows = b_kcols ? n.b_rows : 3 * n.b_rows, b_cols = b_kcols ? 3 * n.b_cols : n.b_cols;
+    const int64_t lda2 = (int64_t)round_up((size_t)a_cols, 64), ldb2 = (int64_t)round_up((size_t)b_cols, 64);
+    if (lda2 > INT32_MAX || ldb2 > INT32_MAX) return TC_ERR_OVERFLOW;
+    const size_t a_bytes = round_up((size_t)(a_rows * lda2 * 2), 256), b_bytes = (size_t)(b_rows * ldb2 * 2);
+
+    tc_gemm_desc d2 = *d;
+    d2.a_dtype = d2.b_dtype = TC_BF16;
+    d2.K = 3 * d->K;
+    d2.lda = (int32_t)lda2;
+    d2.ldb = (int32_t)ldb2;
+    d2.ldc = (int32_t)n.ldc;
+    tc_epilogue e2{};
+    if (epi) e2 = *epi;
+
+    std::lock_guard<std::mutex> g(ctx->mu);
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    if ((st = ensure_rx(s, a_bytes + b_bytes)) != TC_OK) return st;
+    uint16_t *A2 = static_cast<uint16_t *>(s->rx);
+    uint16_t *B2 = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(s->rx) + a_bytes);
+    Norm n2;
+    if ((st = validate(&d2, A2, B2, C, 1, 0, 0, 0, &n2)) != TC_OK) return st;
+    Plan p2;
+    if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p2)) != TC_OK) return st;
+    const SplitArgs sa{static_cast<const float *>(A), A2, n.a_rows, n.a_cols, n.lda, lda2, a_kcols ? 1 : 0, {0, 0, 1}};
+    const SplitArgs sb{static_cast<const float *>(B), B2, n.b_rows, n.b_cols, n.ldb, ldb2, b_kcols ? 1 : 0, {0, 1, 0}};
+    if (launch_split(sa, s->st) != cudaSuccess || launch_split(sb, s->st) != cudaSuccess) return TC_ERR_CUDA;
+    ctx->launches += 2;
+    st = enqueue(ctx, &d2, n2, p2, A2, B2, C, s, epi ? &e2 : nullptr);
+    if (st == TC_OK) ctx->last = "relaxed_f32_3xbf16_" + ctx->last;
+    return st;
+}
+
 tc_status_t stream_init(tc_ctx *ctx, tc_stream *s)
 {
     s->ctx = ctx;
@@ -807,6 +885,7 @@ void stream_free(tc_stream *s)
     if (!s) return;
     if (s->st) cudaStreamSynchronize(s->st);
     if (s->ws) cudaFree(s->ws);
+    if (s->rx) cudaFree(s->rx);
     if (s->status_host) cudaFreeHost(s->status_host);
     if (s->owned && s->st) cudaStreamDestroy(s->st);
     delete s;
@@ -960,6 +1039,21 @@ tc_status_t tc_gemm_epilogue(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilog
 {
     if (!ctx) return TC_ERR_NULL;
     tc_status_t st = tc_gemm_epilogue_async(ctx, d, epi, A, B, C, ctx->def);
+    if (st != TC_OK) return st;
+    return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_f32_relaxed_async(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                                      const void *B, void *C, tc_stream *s)
+{
+    return run_relaxed(ctx, d, epi, A, B, C, s);
+}
+
+tc_status_t tc_gemm_f32_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi, const void *A,
+                                const void *B, void *C)
+{
+    if (!ctx) return TC_ERR_NULL;
+    tc_status_t st = run_relaxed(ctx, d, epi, A, B, C, ctx->def);
     if (st != TC_OK) return st;
     return tc_stream_sync(ctx->def);
 }

@@ -159,6 +159,20 @@ struct FfmaArgs {
 enum FfmaTile { FFMA_SMALL = 0, FFMA_LARGE = 1, FFMA_PANEL = 2 };
 cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st);
 
+// Relaxed fp32: a stored fp32 matrix (rows x cols, leading dimension ld_src)
+// becomes three bf16 copies placed side by side along its K dimension (the
+// columns when k_along_cols, else the rows), part j = hi or lo per
+// parts[j] (0 = hi = bf16(x), 1 = lo = bf16(x - hi)), in a buffer with
+// leading dimension ld_dst (a multiple of 64) and a 256-byte aligned base.
+struct SplitArgs {
+    const float *src;
+    uint16_t *dst;
+    long long rows, cols, ld_src, ld_dst;
+    int k_along_cols;
+    int parts[3];
+};
+cudaError_t launch_split(const SplitArgs &a, cudaStream_t st);
+
 // Copy a strided batch of 16-bit matrices (rows x cols, leading dimension
 // ld_src) into a buffer with leading dimension ld_dst (a multiple of 64) and
 // a 256-byte aligned base, so that TMA can read it.

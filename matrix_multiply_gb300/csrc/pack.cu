@@ -14,6 +14,10 @@
 // the CTAs are split between the operands by a prefix table.
 #include "internal.h"
 
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
 namespace tc {
 namespace {
 
@@ -109,7 +113,37 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const __grid_constan
         if (dst[k]) *reinterpret_cast<uint4 *>(dst[k]) = window16(q0[k], q1[k], off[k]);
 }
 
+// Relaxed fp32 (split into bf16 parts): x = hi + lo + e with hi = bf16(x),
+// lo = bf16(x - hi) (x - hi is exact in fp32), |e| <= 2^-16 |x|.  One thread
+// per element; consecutive threads take consecutive columns, so the fp32
+// loads and the three bf16 stores are contiguous across a warp.
+__global__ void __launch_bounds__(256) split_kernel(const SplitArgs a)
+{
+    const long long total = a.rows * a.cols;
+    for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
+        const long long r = i / a.cols, c = i - r * a.cols;
+        const float x = __ldg(a.src + r * a.ld_src + c);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+        const uint16_t part[2] = {__bfloat16_as_ushort(hi), __bfloat16_as_ushort(lo)};
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const long long off = a.k_along_cols ? r * a.ld_dst + j * a.cols + c : (j * a.rows + r) * a.ld_dst + c;
+            a.dst[off] = part[a.parts[j]];
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_split(const SplitArgs &a, cudaStream_t st)
+{
+    if (a.rows < 1 || a.cols < 1) return cudaErrorInvalidValue;
+    const long long total = a.rows * a.cols;
+    const long long grid = std::min<long long>((total + 255) / 256, 152LL * 16);
+    split_kernel<<<(unsigned)grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(PackBatch &pb, cudaStream_t st)
 {

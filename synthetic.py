@@ -177,3 +177,9 @@ def f16_decode(M: int, N: int, K: int, seed: int = 6) -> Problem:
     """fp16 x[M, K] @ W[N, K]^T, fp16 out, normal(0,1) from a fresh generator."""
     return make_problem(M, N, K, "f16", "f16", transpose_b=True, seed=seed, dist="normal")
 
+
+def fp32_nn_4096() -> Problem:
+    """fp32 NN 4096^3, fp32 out, uniform[-1,1] from a fresh seed-7 generator
+    (the exact and the relaxed fp32 paths at the headline size)."""
+    return make_problem(4096, 4096, 4096, "f32", "f32", seed=7, dist="uniform")
+
