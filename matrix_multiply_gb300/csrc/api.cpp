@@ -46,6 +46,7 @@ struct tc_ctx {
     uint64_t launches = 0;
     void *dbuf[3] = {nullptr, nullptr, nullptr};  // device copies for tc_gemm_host
     size_t dcap[3] = {0, 0, 0};
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;   // tc_gemm_host's copy streams
     int max_pairs[2] = {-1, -1};                   // resident CTA pairs (BN 128, 256), queried once
     std::mutex mu;
 };
@@ -965,6 +966,8 @@ void tc_ctx_destroy(tc_ctx *ctx)
     stream_free(ctx->def);
     for (int i = 0; i < 3; ++i)
         if (ctx->dbuf[i]) cudaFree(ctx->dbuf[i]);
+    if (ctx->copy_in) cudaStreamDestroy(ctx->copy_in);
+    if (ctx->copy_out) cudaStreamDestroy(ctx->copy_out);
     delete ctx;
 }
 
@@ -1121,19 +1124,79 @@ tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
                 ctx->dcap[i] = bytes[i];
             }
         }
+        if ((!ctx->copy_in && cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking) != cudaSuccess) ||
+            (!ctx->copy_out && cudaStreamCreateWithFlags(&ctx->copy_out, cudaStreamNonBlocking) != cudaSuccess))
+            return TC_ERR_CUDA;
     }
-    cudaStream_t st0 = ctx->def->st;
-    if (cudaMemcpyAsync(ctx->dbuf[0], A_host, bytes[0], cudaMemcpyHostToDevice, st0) != cudaSuccess ||
-        cudaMemcpyAsync(ctx->dbuf[1], B_host, bytes[1], cudaMemcpyHostToDevice, st0) != cudaSuccess)
-        return TC_ERR_CUDA;
-    if (d->beta != 0.0f &&
-        cudaMemcpyAsync(ctx->dbuf[2], C_host, bytes[2], cudaMemcpyHostToDevice, st0) != cudaSuccess)
-        return TC_ERR_CUDA;
-    st = run(ctx, d, ctx->dbuf[0], ctx->dbuf[1], ctx->dbuf[2], 1, 0, 0, 0, ctx->def);
-    if (st != TC_OK) return st;
-    if (cudaMemcpyAsync(C_host, ctx->dbuf[2], bytes[2], cudaMemcpyDeviceToHost, st0) != cudaSuccess)
-        return TC_ERR_CUDA;
-    return tc_stream_sync(ctx->def);
+    // The device copies keep the host layouts (same leading dimensions).  A
+    // is moved in bands of op(A) rows and C in the same bands, so that the
+    // GEMM of band i runs while band i + 1 arrives and band i - 1 returns:
+    // B (needed whole) first, then band by band on the copy-in stream; each
+    // band's GEMM on the context's stream once its band has landed; each
+    // band of C back on the copy-out stream once its GEMM is done.
+    // (Host-device copies run at one rate per direction whatever the number
+    // of streams; the two directions overlap.)
+    const int64_t es_a = (int64_t)elem_size(d->a_dtype), es_c = (int64_t)elem_size(d->c_dtype);
+    const int64_t band = d->M <= 1536 ? d->M : std::max<int64_t>(1024, (int64_t)round_up((size_t)cdiv(d->M, 4), 256));
+    const int nb = (int)cdiv(d->M, band);
+    uint8_t *dA = static_cast<uint8_t *>(ctx->dbuf[0]), *dB = static_cast<uint8_t *>(ctx->dbuf[1]);
+    uint8_t *dC = static_cast<uint8_t *>(ctx->dbuf[2]);
+    const uint8_t *hA = static_cast<const uint8_t *>(A_host);
+    uint8_t *hC = static_cast<uint8_t *>(C_host);
+    cudaStream_t comp = ctx->def->st;
+    std::vector<cudaEvent_t> ev;
+    auto event = [&](cudaEvent_t *e) {
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+        ev.push_back(*e);
+        return true;
+    };
+    auto finish = [&](tc_status_t result) {
+        cudaStreamSynchronize(ctx->copy_in);
+        cudaStreamSynchronize(ctx->copy_out);
+        tc_status_t s2 = tc_stream_sync(ctx->def);
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+        return result != TC_OK ? result : s2;
+    };
+    // one band of op(A) rows [m0, m1): rows of A, or columns of A stored [K, M]
+    auto copy_a = [&](int64_t m0, int64_t m1) {
+        if (!d->transpose_a)
+            return cudaMemcpy2DAsync(dA + m0 * n.lda * es_a, n.lda * es_a, hA + m0 * n.lda * es_a, n.lda * es_a,
+                                     n.a_cols * es_a, m1 - m0, cudaMemcpyHostToDevice, ctx->copy_in);
+        return cudaMemcpy2DAsync(dA + m0 * es_a, n.lda * es_a, hA + m0 * es_a, n.lda * es_a, (m1 - m0) * es_a,
+                                 n.a_rows, cudaMemcpyHostToDevice, ctx->copy_in);
+    };
+    auto copy_c = [&](int64_t m0, int64_t m1, cudaMemcpyKind kind, cudaStream_t str) {
+        uint8_t *dst = kind == cudaMemcpyHostToDevice ? dC + m0 * n.ldc * es_c : hC + m0 * n.ldc * es_c;
+        const uint8_t *src = kind == cudaMemcpyHostToDevice ? hC + m0 * n.ldc * es_c : dC + m0 * n.ldc * es_c;
+        return cudaMemcpy2DAsync(dst, n.ldc * es_c, src, n.ldc * es_c, d->N * es_c, m1 - m0, kind, str);
+    };
+    cudaEvent_t ev_b;
+    if (!event(&ev_b) ||
+        cudaMemcpy2DAsync(dB, n.ldb * es_a, B_host, n.ldb * es_a, n.b_cols * es_a, n.b_rows, cudaMemcpyHostToDevice,
+                          ctx->copy_in) != cudaSuccess ||
+        cudaEventRecord(ev_b, ctx->copy_in) != cudaSuccess || cudaStreamWaitEvent(comp, ev_b, 0) != cudaSuccess)
+        return finish(TC_ERR_CUDA);
+    for (int i = 0; i < nb; ++i) {
+        const int64_t m0 = (int64_t)i * band, m1 = std::min<int64_t>(d->M, m0 + band);
+        cudaEvent_t ev_in, ev_done;
+        if (!event(&ev_in) || !event(&ev_done) || copy_a(m0, m1) != cudaSuccess ||
+            (d->beta != 0.0f && copy_c(m0, m1, cudaMemcpyHostToDevice, ctx->copy_in) != cudaSuccess) ||
+            cudaEventRecord(ev_in, ctx->copy_in) != cudaSuccess || cudaStreamWaitEvent(comp, ev_in, 0) != cudaSuccess)
+            return finish(TC_ERR_CUDA);
+        tc_gemm_desc db = *d;
+        db.M = (int32_t)(m1 - m0);
+        db.lda = (int32_t)n.lda;
+        db.ldb = (int32_t)n.ldb;
+        db.ldc = (int32_t)n.ldc;
+        const void *Ab = d->transpose_a ? static_cast<const void *>(dA + m0 * es_a)
+                                        : static_cast<const void *>(dA + m0 * n.lda * es_a);
+        st = run(ctx, &db, Ab, dB, dC + m0 * n.ldc * es_c, 1, 0, 0, 0, ctx->def);
+        if (st != TC_OK) return finish(st);
+        if (cudaEventRecord(ev_done, comp) != cudaSuccess || cudaStreamWaitEvent(ctx->copy_out, ev_done, 0) != cudaSuccess ||
+            copy_c(m0, m1, cudaMemcpyDeviceToHost, ctx->copy_out) != cudaSuccess)
+            return finish(TC_ERR_CUDA);
+    }
+    return finish(TC_OK);
 }
 
 tc_status_t tc_gemm_validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C)

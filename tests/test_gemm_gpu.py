@@ -409,6 +409,23 @@ def test_host_buffers(ctx):
     parity.check(C.numpy(), R, T, "f32", what="host buffers")
 
 
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_host_buffers_banded(ctx, ta, tb):
+    """M large enough for the host call to move A and C in row bands (the
+    last one ragged), with C read (beta != 0) and padded leading dims."""
+    M, N, K = 5000, 300, 256
+    p = synthetic.make_problem(M, N, K, "bf16", "f32", transpose_a=ta, transpose_b=tb, alpha=0.5, beta=1.0,
+                               seed=80, dist="normal", c_fill="uniform", lda=(M if ta else K) + 8,
+                               ldb=(K if tb else N) + 3, ldc=N + 5)
+    A, B, C = p.A.pin_memory(), p.B.pin_memory(), p.C.clone().pin_memory()
+    d = tg.make_desc(M, N, K, "bf16", "f32", transpose_a=ta, transpose_b=tb, alpha=0.5, beta=1.0,
+                     lda=A.shape[1], ldb=B.shape[1], ldc=C.shape[1])
+    tg.tc_gemm_host(ctx, d, A, B, C)
+    R, T = oracle.gemm(p)
+    parity.check(C.numpy()[:, :N], R, T, "f32", what=f"host banded {p.layout} {ctx.last_kernel}")
+    assert torch.equal(C[:, N:], p.C[:, N:])       # the padding of C is not written
+
+
 # ----------------------------------------------------- the named workloads
 
 def test_fp32_nn_256(ctx):
