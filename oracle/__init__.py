@@ -36,7 +36,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 
-CODES = {"f16": 1, "bf16": 2, "f32": 3}
+CODES = {"f16": 1, "bf16": 2, "f32": 3, "i8": 4}
 
 
 class _Problem(ctypes.Structure):
@@ -101,7 +101,7 @@ def _ptr(t: torch.Tensor | None) -> int | None:
 
 
 def _dtype_code(t: torch.Tensor) -> int:
-    return {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3}[t.dtype]
+    return {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3, torch.int8: 4}[t.dtype]
 
 
 def _struct(p, lda=None, ldb=None, ldc=None) -> tuple[_Problem, list]:
@@ -221,4 +221,25 @@ def gemm_epilogue_points(p, bias, activation: str, rows, cols, lib=None):
     cols = np.asarray(cols, dtype=np.int64)
     Y = R if bias is None else R + decode(bias, lib=lib).reshape(-1)[cols]
     return apply_activation(Y, activation), T, Y
+
+
+# -------------------------------------------------------------- int8 GEMM
+# tessl architecture.md, "Integer GEMM": int8 x int8 accumulated exactly
+# (an integer; refused for K > 131072, where a full-range sum can leave
+# int32), then per-column dequantisation.  With this library's alpha/beta:
+# C = alpha * (acc[m, n] * scale[n]) + beta * C_old, in fp64.
+
+def gemm_i8_dequant(p, scale, row0: int = 0, row1: int | None = None, lib=None):
+    """Rows [row0,row1) of alpha * acc * scale[None, :] + beta * C_old for
+    int8 operands, with T and the exact integer accumulation: (R, T, ACC)."""
+    import copy
+    q = copy.copy(p)
+    q.alpha, q.beta = 1.0, 0.0
+    ACC, T = gemm(q, row0, row1, lib=lib)
+    sc = decode(scale, lib=lib).reshape(1, -1)[:, : p.N]
+    R = float(np.float32(p.alpha)) * (ACC * sc)
+    if p.beta != 0.0:
+        row1 = p.M if row1 is None else row1
+        R = R + float(np.float32(p.beta)) * decode(p.C, lib=lib)[row0:row1, : p.N]
+    return R, T, ACC
 

@@ -32,8 +32,11 @@
 #include <stdlib.h>
 #include <string.h>
 
-/* element encodings understood by the oracle */
-enum { ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_F32 = 3 };
+/* element encodings understood by the oracle (ORACLE_I8: two's-complement
+ * int8, the operand type of the tessl architecture.md "Integer GEMM"; its
+ * products and their sums for K <= 131072 are integers below 2^53, so the
+ * fp64 k-sum is exact) */
+enum { ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_F32 = 3, ORACLE_I8 = 4 };
 
 typedef struct {
     int64_t M, N, K;
@@ -83,6 +86,7 @@ static double load(const void *p, int32_t dtype, int64_t idx)
     switch (dtype) {
     case ORACLE_F16: return oracle_decode_f16(((const uint16_t *)p)[idx]);
     case ORACLE_BF16: return oracle_decode_bf16(((const uint16_t *)p)[idx]);
+    case ORACLE_I8: return (double)((const int8_t *)p)[idx];
     default: return (double)((const float *)p)[idx];
     }
 }
@@ -187,7 +191,7 @@ int oracle_gemm_points(const oracle_problem *p, int64_t n, const int64_t *rows,
 /* decode n stored elements of the given encoding into doubles */
 int oracle_decode_array(int32_t dtype, int64_t n, const void *src, double *dst)
 {
-    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16 && dtype != ORACLE_F32) return 1;
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16 && dtype != ORACLE_F32 && dtype != ORACLE_I8) return 1;
     for (int64_t t = 0; t < n; ++t) dst[t] = load(src, dtype, t);
     return 0;
 }

@@ -409,3 +409,56 @@ def test_epilogue_points_match_rows():
     ii, jj = np.meshgrid(np.arange(9), np.arange(11), indexing="ij")
     Rp, Tp, Yp = oracle.gemm_epilogue_points(p, bias, "gelu_tanh", ii.ravel(), jj.ravel())
     assert np.array_equal(Rp, R.ravel()) and np.array_equal(Tp, T.ravel()) and np.array_equal(Yp, Y.ravel())
+
+
+# ---------------------------------------------------------------- int8 GEMM
+# tessl architecture.md, "Integer GEMM": exact int8 x int8 accumulation,
+# per-column dequantisation.
+
+def test_i8_decoder_exhaustive():
+    t = torch.arange(-128, 128, dtype=torch.int16).to(torch.int8)
+    assert np.array_equal(oracle.decode(t), t.to(torch.float64).numpy())
+
+
+def _i8_problem(M, N, K, ta, tb, seed, lo=-128, hi=127):
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randint(lo, hi + 1, (K, M) if ta else (M, K), generator=g).to(torch.int8)
+    B = torch.randint(lo, hi + 1, (N, K) if tb else (K, N), generator=g).to(torch.int8)
+    return synthetic.Problem(M, N, K, "i8", "f32", ta, tb, 1.0, 0.0, A, B, torch.zeros(M, N))
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_i8_brute_force(ta, tb):
+    p = _i8_problem(3, 4, 5, ta, tb, seed=9)
+    Ai = [[int(v) for v in row] for row in p.A.tolist()]
+    Bi = [[int(v) for v in row] for row in p.B.tolist()]
+    a = (lambda i, k: Ai[k][i]) if ta else (lambda i, k: Ai[i][k])
+    b = (lambda k, j: Bi[j][k]) if tb else (lambda k, j: Bi[k][j])
+    exact = np.array([[sum(a(i, k) * b(k, j) for k in range(5)) for j in range(4)] for i in range(3)], float)
+    R, T = oracle.gemm(p)
+    assert np.array_equal(R, exact)
+    assert np.array_equal(T, np.array([[sum(abs(a(i, k) * b(k, j)) for k in range(5)) for j in range(4)]
+                                       for i in range(3)], float))
+
+
+def test_i8_full_range_at_the_k_limit():
+    """All -128: every product is 2^14; at K = 131072 the sum is 2^31, one
+    past the int32 range -- the oracle's fp64 sum is exact."""
+    K = 131072
+    p = synthetic.Problem(2, 3, K, "i8", "f32", False, False, 1.0, 0.0, torch.full((2, K), -128, dtype=torch.int8),
+                          torch.full((K, 3), -128, dtype=torch.int8), torch.zeros(2, 3))
+    R, T = oracle.gemm(p)
+    assert (R == 2.0 ** 31).all() and (T == 2.0 ** 31).all()
+
+
+def test_i8_dequant_closed_form():
+    """Identity A: acc = B, so C = alpha * B * scale[n] + beta * C_old."""
+    N = 6
+    B = torch.tensor([[3, -7, 127, -128, 0, 5], [1, 2, 3, 4, 5, 6]], dtype=torch.int8)
+    scale = torch.tensor([0.5, 2.0, 1e-3, -0.25, 7.0, 1.0])
+    Cold = torch.arange(12, dtype=torch.float32).reshape(2, 6)
+    p = synthetic.Problem(2, N, 2, "i8", "f32", False, False, 0.5, 2.0, torch.eye(2, dtype=torch.int8), B, Cold)
+    R, _, ACC = oracle.gemm_i8_dequant(p, scale)
+    want = 0.5 * B.double().numpy() * scale.double().numpy()[None, :] + 2.0 * Cold.double().numpy()
+    assert np.array_equal(ACC, B.double().numpy())
+    assert np.allclose(R, want, rtol=1e-15, atol=0)
