@@ -47,7 +47,8 @@
 extern "C" {
 #endif
 
-typedef enum { TC_F16 = 1, TC_BF16 = 2, TC_F32 = 3 } tc_dtype_t;
+/* TC_I8 / TC_I32: operands and accumulator of tc_gemm_i8_dequant only. */
+typedef enum { TC_F16 = 1, TC_BF16 = 2, TC_F32 = 3, TC_I8 = 4, TC_I32 = 5 } tc_dtype_t;
 
 typedef enum {
     TC_OK = 0,
@@ -168,6 +169,24 @@ tc_status_t tc_gemm_f32_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epi
                                 const void *B, void *C);
 tc_status_t tc_gemm_f32_relaxed_async(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *epi,
                                       const void *A, const void *B, void *C, tc_stream *s);
+
+/* Integer GEMM with per-column dequantisation (tessl architecture.md,
+ * "Integer GEMM"):
+ *   acc[m, n] = sum_k op(A)[m, k] * op(B)[k, n]   (int8 x int8, exact)
+ *   C[m, n]   = alpha * (acc[m, n] * col_scale[n]) + beta * C_old[m, n]
+ * The descriptor has a_dtype == b_dtype == TC_I8, accum_dtype == TC_I32,
+ * c_dtype == TC_F32 (TC_ERR_DTYPE otherwise); col_scale is a DEVICE pointer
+ * to N floats (TC_ERR_NULL if NULL; it must not overlap C).  K > 131072 is
+ * refused (TC_ERR_DIM): past it a full-range sum can leave int32.  The
+ * accumulation is exact: operands are widened to bf16 (exact for int8) in
+ * a per-stream buffer the library owns, the tensor cores sum at most 1024
+ * products per K slice in fp32 (below 2^24, exact), and the slices are
+ * added as 64-bit integers; the result is rounded once to fp32 and once by
+ * the scale (and alpha, beta).  Deterministic run to run. */
+tc_status_t tc_gemm_i8_dequant(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, const void *A,
+                               const void *B, void *C);
+tc_status_t tc_gemm_i8_dequant_async(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale,
+                                     const void *A, const void *B, void *C, tc_stream *s);
 
 /* Same GEMM with HOST operands: copies A and B (and C when beta != 0) to the
  * device, runs, copies C back and waits.  Device buffers are cached in the

@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libtcgemm.so")
 
 # ------------------------------------------------------------------ enums
 
-TC_F16, TC_BF16, TC_F32 = 1, 2, 3
+TC_F16, TC_BF16, TC_F32, TC_I8, TC_I32 = 1, 2, 3, 4, 5
 STATUS = {
     0: "TC_OK", 1: "TC_ERR_NULL", 2: "TC_ERR_DIM", 3: "TC_ERR_LD", 4: "TC_ERR_DTYPE",
     5: "TC_ERR_SCALAR", 6: "TC_ERR_OVERLAP", 7: "TC_ERR_OVERFLOW", 8: "TC_ERR_ALIGN_UNSUPPORTED",
@@ -101,6 +101,8 @@ def _load():
         "tc_gemm_epilogue_async": (st, [vp, D, E, vp, vp, vp, vp]),
         "tc_gemm_epilogue_validate": (st, [D, E, vp, vp, vp]),
         "tc_gemm_f32_relaxed": (st, [vp, D, E, vp, vp, vp]),
+        "tc_gemm_i8_dequant": (st, [vp, D, vp, vp, vp, vp]),
+        "tc_gemm_i8_dequant_async": (st, [vp, D, vp, vp, vp, vp, vp]),
         "tc_gemm_f32_relaxed_async": (st, [vp, D, E, vp, vp, vp, vp]),
         "tc_gemm_host": (st, [vp, D, vp, vp, vp]),
         "tc_gemm_splitk_noalloc": (st, [D, vp, vp, vp, ctypes.c_int, vp]),
@@ -126,7 +128,7 @@ EXPORTED = (
     "tc_gemm_validate",
     "tc_gemm_batched_validate", "tc_gemm_plan", "tc_last_kernel", "tc_launch_count",
     "tc_status_string", "tc_gemm_epilogue", "tc_gemm_epilogue_async", "tc_gemm_epilogue_validate",
-    "tc_gemm_f32_relaxed", "tc_gemm_f32_relaxed_async",
+    "tc_gemm_f32_relaxed", "tc_gemm_f32_relaxed_async", "tc_gemm_i8_dequant", "tc_gemm_i8_dequant_async",
 )
 
 
@@ -142,7 +144,7 @@ def _check(status: int, what: str):
 
 # ------------------------------------------------------------------ helpers
 
-_DT_NAMES = {"f16": TC_F16, "bf16": TC_BF16, "f32": TC_F32}
+_DT_NAMES = {"f16": TC_F16, "bf16": TC_BF16, "f32": TC_F32, "i8": TC_I8}
 
 
 def _torch_dtype_code(t) -> int:
@@ -163,7 +165,8 @@ def make_desc(M, N, K, a_dtype, c_dtype=None, *, transpose_a=False, transpose_b=
               alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0) -> tc_gemm_desc:
     a = _DT_NAMES.get(a_dtype, a_dtype)
     c = _DT_NAMES.get(c_dtype, c_dtype) if c_dtype is not None else a
-    return tc_gemm_desc(M, N, K, a, a, c, TC_F32, bool(transpose_a), bool(transpose_b),
+    accum = TC_I32 if a == TC_I8 else TC_F32       # int8 operands accumulate in int32
+    return tc_gemm_desc(M, N, K, a, a, c, accum, bool(transpose_a), bool(transpose_b),
                         float(alpha), float(beta), lda, ldb, ldc)
 
 
@@ -368,6 +371,22 @@ def tc_gemm_f32_relaxed_async(ctx: Context, d: tc_gemm_desc, A, B, C, stream: St
     e = make_epilogue(bias, activation)
     _check(_lib.tc_gemm_f32_relaxed_async(ctx.ptr, ctypes.byref(d), ctypes.byref(e), _addr(A), _addr(B), _addr(C),
                                           stream.ptr), "tc_gemm_f32_relaxed_async")
+
+
+def tc_gemm_i8_dequant(ctx: Context, d: tc_gemm_desc, A, B, C, col_scale):
+    """int8 x int8 accumulated exactly, then C = alpha * acc * col_scale[n] +
+    beta * C (C fp32; col_scale a CUDA tensor of N floats), synchronously."""
+    _check_capacity(d, A, B, C)
+    _require(col_scale, d.N, "col_scale")
+    _check(_lib.tc_gemm_i8_dequant(ctx.ptr, ctypes.byref(d), _addr(col_scale), _addr(A), _addr(B), _addr(C)),
+           "tc_gemm_i8_dequant")
+
+
+def tc_gemm_i8_dequant_async(ctx: Context, d: tc_gemm_desc, A, B, C, col_scale, stream: Stream):
+    _check_capacity(d, A, B, C)
+    _require(col_scale, d.N, "col_scale")
+    _check(_lib.tc_gemm_i8_dequant_async(ctx.ptr, ctypes.byref(d), _addr(col_scale), _addr(A), _addr(B), _addr(C),
+                                         stream.ptr), "tc_gemm_i8_dequant_async")
 
 
 def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):

@@ -53,7 +53,7 @@ struct tc_ctx {
 
 namespace {
 
-size_t elem_size(tc_dtype_t t) { return t == TC_F32 ? 4 : 2; }
+size_t elem_size(tc_dtype_t t) { return t == TC_F32 ? 4 : t == TC_I8 ? 1 : 2; }
 
 bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
 bool add_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_add_overflow(a, b, out); }
@@ -86,15 +86,22 @@ bool ranges_overlap(const void *p, int64_t pb, const void *q, int64_t qb)
     return a0 < b1 && b0 < a1;
 }
 
+// int8 operands (accumulated in int32, written as fp32) only where allow_i8:
+// the integer GEMM has its own entry point.
 tc_status_t validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C, int64_t batch,
-                     int64_t sa, int64_t sb, int64_t sc, Norm *n)
+                     int64_t sa, int64_t sb, int64_t sc, Norm *n, bool allow_i8 = false)
 {
     if (!d || !A || !B || !C) return TC_ERR_NULL;
     if (d->M < 1 || d->N < 1 || d->K < 1 || batch < 1) return TC_ERR_DIM;
-    const bool ab_ok = d->a_dtype == TC_F16 || d->a_dtype == TC_BF16 || d->a_dtype == TC_F32;
-    if (!ab_ok || d->b_dtype != d->a_dtype || d->accum_dtype != TC_F32 ||
-        (d->c_dtype != d->a_dtype && d->c_dtype != TC_F32))
-        return TC_ERR_DTYPE;
+    if (d->a_dtype == TC_I8) {
+        if (!allow_i8 || d->b_dtype != TC_I8 || d->accum_dtype != TC_I32 || d->c_dtype != TC_F32)
+            return TC_ERR_DTYPE;
+    } else {
+        const bool ab_ok = d->a_dtype == TC_F16 || d->a_dtype == TC_BF16 || d->a_dtype == TC_F32;
+        if (!ab_ok || d->b_dtype != d->a_dtype || d->accum_dtype != TC_F32 ||
+            (d->c_dtype != d->a_dtype && d->c_dtype != TC_F32))
+            return TC_ERR_DTYPE;
+    }
     if (d->lda < 0 || d->ldb < 0 || d->ldc < 0) return TC_ERR_LD;
     if (sa < 0 || sb < 0 || sc < 0) return TC_ERR_STRIDE;
 
@@ -385,8 +392,11 @@ tc_status_t read_status(tc_stream *s)
 
 // Enqueue one validated, planned problem on stream s (epi: the fused
 // bias/activation epilogue, or null).
+// col_scale: the int8 path's per-column dequantisation (its K slices then
+// hold integers and are added as such), or null.
 tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Plan &p, const void *A,
-                    const void *B, void *C, tc_stream *s, const tc_epilogue *epi = nullptr)
+                    const void *B, void *C, tc_stream *s, const tc_epilogue *epi = nullptr,
+                    const float *col_scale = nullptr)
 {
     cudaError_t e;
     if (p.ffma) {
@@ -503,6 +513,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.status = s->status_dev;
     a.bias = epi ? epi->bias : nullptr;
     a.act = epi ? (int)epi->activation : (int)TC_ACT_NONE;
+    a.col_scale = col_scale;
     const int64_t kb_per_unit = a.num_kb;
     a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
     {
@@ -559,6 +570,8 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         r.c_vec_ok = aligned16(C) && n.ldc % 4 == 0 && a.stride_c % 4 == 0;   // 4-element vectors
         r.bias = a.bias;
         r.act = a.act;
+        r.col_scale = col_scale;
+        r.int_sum = col_scale != nullptr;
         const int64_t work = (int64_t)r.ntiles * rows_per_tile * (p.bn / 4);
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), (int64_t)ctx->num_sms * 8));
         if ((e = launch_reduce(r, grid, s->st)) != cudaSuccess) return TC_ERR_CUDA;
@@ -869,6 +882,71 @@ tc_status_t run_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *e
     return st;
 }
 
+// ---------------------------------------------------------------- int8 GEMM
+// tessl architecture.md, "Integer GEMM": int8 x int8 summed exactly, then
+// per-column dequantisation.  Both operands are widened to bf16 (exact for
+// int8) and run through the bf16 tensor-core kernel with K cut into slices
+// of at most 16 K blocks (1024 products, |sum| <= 2^24: exact in the fp32
+// accumulator); the reduction kernel adds the slices as 64-bit integers,
+// rounds once to fp32, scales by the column's factor, then alpha/beta.
+constexpr int I8_K_MAX = 131072;
+constexpr int I8_SLICE_KB = 16;
+
+tc_status_t run_i8(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, const void *A, const void *B,
+                   void *C, tc_stream *s)
+{
+    if (!ctx || !s) return TC_ERR_NULL;
+    Norm n;
+    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n, true);
+    if (st != TC_OK) return st;
+    if (d->a_dtype != TC_I8) return TC_ERR_DTYPE;
+    if (!col_scale) return TC_ERR_NULL;
+    if (d->K > I8_K_MAX) return TC_ERR_DIM;
+    if (ranges_overlap(col_scale, (int64_t)d->N * 4, C, n.c_bytes)) return TC_ERR_OVERLAP;
+    const int64_t lda2 = (int64_t)round_up((size_t)n.a_cols, 64), ldb2 = (int64_t)round_up((size_t)n.b_cols, 64);
+    const size_t a_bytes = round_up((size_t)(n.a_rows * lda2 * 2), 256), b_bytes = (size_t)(n.b_rows * ldb2 * 2);
+    tc_gemm_desc d2 = *d;
+    d2.a_dtype = d2.b_dtype = TC_BF16;
+    d2.accum_dtype = TC_F32;
+    d2.lda = (int32_t)lda2;
+    d2.ldb = (int32_t)ldb2;
+    d2.ldc = (int32_t)n.ldc;
+
+    std::lock_guard<std::mutex> g(ctx->mu);
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    if ((st = ensure_rx(s, a_bytes + b_bytes)) != TC_OK) return st;
+    uint16_t *A2 = static_cast<uint16_t *>(s->rx);
+    uint16_t *B2 = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(s->rx) + a_bytes);
+    Norm n2;
+    if ((st = validate(&d2, A2, B2, C, 1, 0, 0, 0, &n2)) != TC_OK) return st;
+    Plan p;
+    if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p)) != TC_OK) return st;
+    // every tile in the same K slices of at most I8_SLICE_KB blocks (the
+    // plan's own tail split would add its slices in fp32)
+    const int64_t num_kb = cdiv(d->K, BK);
+    const int S = (int)cdiv(num_kb, I8_SLICE_KB);
+    const int64_t tiles = cdiv(d->M, BM * p.cg) * cdiv(d->N, p.bn);
+    p.tiles = tiles;
+    p.seg0_tiles = tiles;
+    p.seg0_split = S;
+    p.seg1_split = 1;
+    p.split_base = 0;
+    p.units = tiles * S;
+    p.split = S > 1 ? 2 : 1;
+    if (p.units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
+    const int workers = p.cg == 2 ? std::max(ctx->num_sms / 2, 1) : ctx->num_sms;
+    p.grid = (int)std::min<int64_t>(p.units, workers) * p.cg;
+    char buf[32];
+    std::snprintf(buf, sizeof buf, "_i8s%d", S);
+    const WidenArgs wa{static_cast<const int8_t *>(A), A2, n.a_rows, n.a_cols, n.lda, lda2};
+    const WidenArgs wb{static_cast<const int8_t *>(B), B2, n.b_rows, n.b_cols, n.ldb, ldb2};
+    if (launch_widen(wa, s->st) != cudaSuccess || launch_widen(wb, s->st) != cudaSuccess) return TC_ERR_CUDA;
+    ctx->launches += 2;
+    st = enqueue(ctx, &d2, n2, p, A2, B2, C, s, nullptr, col_scale);
+    if (st == TC_OK) ctx->last = "i8_dequant_" + ctx->last.substr(0, ctx->last.find("_tail")) + buf;
+    return st;
+}
+
 tc_status_t stream_init(tc_ctx *ctx, tc_stream *s)
 {
     s->ctx = ctx;
@@ -1057,6 +1135,21 @@ tc_status_t tc_gemm_f32_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epi
 {
     if (!ctx) return TC_ERR_NULL;
     tc_status_t st = run_relaxed(ctx, d, epi, A, B, C, ctx->def);
+    if (st != TC_OK) return st;
+    return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_i8_dequant_async(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, const void *A,
+                                     const void *B, void *C, tc_stream *s)
+{
+    return run_i8(ctx, d, col_scale, A, B, C, s);
+}
+
+tc_status_t tc_gemm_i8_dequant(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, const void *A,
+                               const void *B, void *C)
+{
+    if (!ctx) return TC_ERR_NULL;
+    tc_status_t st = run_i8(ctx, d, col_scale, A, B, C, ctx->def);
     if (st != TC_OK) return st;
     return tc_stream_sync(ctx->def);
 }

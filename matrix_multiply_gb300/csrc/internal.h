@@ -71,9 +71,12 @@ struct MmaArgs {
     unsigned long long timeout_ns;
     int debug_drop_tfull;  // test hook: never signal the first tile's accumulator
     // fused epilogue: bias (N values of c_dtype, or null) and activation
-    // (TC_ACT_*) applied after alpha/beta, before the one rounding
+    // (TC_ACT_*) applied after alpha/beta, before the one rounding; a
+    // per-column scale (N floats, or null) applied to the accumulator before
+    // alpha/beta (the int8 path's dequantisation)
     const void *bias;
     int act;
+    const float *col_scale;
 };
 
 struct MmaLaunch {
@@ -130,6 +133,8 @@ struct ReduceArgs {
     int c_dtype, c_vec_ok;
     const void *bias;      // fused epilogue, as in MmaArgs
     int act;
+    const float *col_scale;
+    int int_sum;           // the slices are integers: add them as 64-bit integers
 };
 cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st);
 
@@ -172,6 +177,15 @@ struct SplitArgs {
     int parts[3];
 };
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t st);
+
+// int8 matrix (rows x cols, leading dimension ld_src) -> bf16 (exact) with
+// leading dimension ld_dst (a multiple of 64) and a 256-byte aligned base.
+struct WidenArgs {
+    const int8_t *src;
+    uint16_t *dst;
+    long long rows, cols, ld_src, ld_dst;
+};
+cudaError_t launch_widen(const WidenArgs &a, cudaStream_t st);
 
 // Copy a strided batch of 16-bit matrices (rows x cols, leading dimension
 // ld_src) into a buffer with leading dimension ld_dst (a multiple of 64) and

@@ -1,6 +1,7 @@
-// Operand repacking for inputs that TMA cannot read in place.
+// Operand preparation: repacking of inputs that TMA cannot read in place,
+// and the bf16 copies of the relaxed-fp32 and int8 paths.
 //
-// A TMA tensor copy needs a 16-byte aligned base address and row strides
+// Repacking: a TMA tensor copy needs a 16-byte aligned base address and row strides
 // that are multiples of 16 bytes.  A contiguous f16/bf16 matrix with an odd
 // row length (the ragged shapes of the tessl architecture.md "Edge-Slice
 // Support" discussion) breaks the second rule.  Such an operand is copied
@@ -134,7 +135,39 @@ __global__ void __launch_bounds__(256) split_kernel(const SplitArgs a)
     }
 }
 
+// int8 -> bf16 (every int8 value is exact in bf16), four consecutive
+// columns per thread: four byte loads, one 8-byte store when the row has
+// all four.
+__global__ void __launch_bounds__(256) widen_kernel(const WidenArgs a)
+{
+    const long long groups = (a.cols + 3) / 4, total = a.rows * groups;
+    for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
+        const long long r = i / groups, c = (i - r * groups) * 4;
+        const int8_t *src = a.src + r * a.ld_src + c;
+        uint16_t *dst = a.dst + r * a.ld_dst + c;
+        const int n = (int)min(4LL, a.cols - c);
+        uint16_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) h[j] = j < n ? __bfloat16_as_ushort(__float2bfloat16_rn((float)__ldg(src + j))) : 0;
+        if (n == 4) {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16);
+        } else {
+            for (int j = 0; j < n; ++j) dst[j] = h[j];
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_widen(const WidenArgs &a, cudaStream_t st)
+{
+    if (a.rows < 1 || a.cols < 1 || (a.ld_dst % 64) || (reinterpret_cast<uintptr_t>(a.dst) & 255u))
+        return cudaErrorInvalidValue;
+    const long long total = a.rows * ((a.cols + 3) / 4);
+    const long long grid = std::min<long long>((total + 255) / 256, 152LL * 16);
+    widen_kernel<<<(unsigned)grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t st)
 {

@@ -234,6 +234,16 @@ __device__ __forceinline__ void bias_act(const MmaArgs &a, int lane, long long c
     }
 }
 
+// The int8 path's dequantisation: the warp's chunk (lane = row, v[j] =
+// column col0 + j) times the column's scale, before alpha/beta.
+__device__ __forceinline__ void col_scale_apply(const MmaArgs &a, int lane, long long col0, float (&v)[32])
+{
+    const long long col = col0 + lane;
+    const float sl = (col < a.N) ? a.col_scale[col] : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= __shfl_sync(0xffffffffu, sl, j);
+}
+
 // C[row, col0 .. col0+31] = v with plain stores (C not readable by TMA)
 __device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long row, long long col0,
                                              const float (&v)[32])
@@ -630,11 +640,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             if (!ea.c_tma) {
                 // both staging buffers of this warp serve as one transpose buffer
                 float *xbuf = reinterpret_cast<float *>(my_stage);
+                if constexpr (EPI)
+                    if (ea.col_scale) col_scale_apply(ea, lane, col0, v);
                 apply_alpha_beta_staged(ea, xbuf, lane, b, row - lane, col0, v);
                 if constexpr (EPI) bias_act(ea, lane, col0, v);
                 store_staged(ea, xbuf, lane, b, row - lane, col0, v);
                 return;
             }
+            if constexpr (EPI)
+                if (ea.col_scale) col_scale_apply(ea, lane, col0, v);
             apply_alpha_beta(ea, b, row, col0, v);
             if constexpr (EPI) bias_act(ea, lane, col0, v);
             if (ea.c_tma) {
@@ -818,6 +832,10 @@ int pairs_for()
 // across a warp.  Launched as a programmatic dependent of the GEMM kernel:
 // griddepcontrol.wait returns once that grid has finished and its partial
 // tiles are visible.
+// INT: the int8 path -- the slices hold exact integers, summed in 64 bits,
+// then scaled per column (a template flag, so the fp32 reduction carries
+// none of it).
+template <bool INT>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
 {
     griddep_wait();
@@ -837,15 +855,39 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
         const long long gcol = (long long)tn * r.bn + c4 * 4;
         if (grow >= r.M || gcol >= r.N) continue;
         const float *src = r.ws + (size_t)t * r.S * slice + (size_t)row * r.bn + c4 * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < r.S; ++s) {
-            const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + s * slice));
-            acc.x += p.x;
-            acc.y += p.y;
-            acc.z += p.z;
-            acc.w += p.w;
+        float v[4];
+        if constexpr (INT) {
+            // every slice holds exact integers: their sum, exact in 64 bits,
+            // then one rounding to fp32
+            long long acc[4] = {0, 0, 0, 0};
+            for (int s = 0; s < r.S; ++s) {
+                const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + s * slice));
+                acc[0] += __float2ll_rn(p.x);
+                acc[1] += __float2ll_rn(p.y);
+                acc[2] += __float2ll_rn(p.z);
+                acc[3] += __float2ll_rn(p.w);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __ll2float_rn(acc[j]);
+        } else {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < r.S; ++s) {
+                const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + s * slice));
+                acc.x += p.x;
+                acc.y += p.y;
+                acc.z += p.z;
+                acc.w += p.w;
+            }
+            v[0] = acc.x;
+            v[1] = acc.y;
+            v[2] = acc.z;
+            v[3] = acc.w;
         }
-        float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        if constexpr (INT) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gcol + j < r.N) v[j] *= r.col_scale[gcol + j];
+        }
         const long long base = (long long)b * r.stride_c + grow * r.ldc + gcol;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -885,12 +927,13 @@ cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, r);
+    if (r.int_sum) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true>, r);
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false>, r);
 }
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
-    const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE;
+    const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE || L.args.col_scale != nullptr;
     if (L.cg == 2) {
         switch (L.bn) {
         case 128: return epi ? launch_kernel<128, 2, false, true>(L, st) : launch_kernel<128, 2>(L, st);

@@ -25,7 +25,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32, "i8": torch.int8}
 
 
 @dataclass
@@ -182,4 +182,26 @@ def fp32_nn_4096() -> Problem:
     """fp32 NN 4096^3, fp32 out, uniform[-1,1] from a fresh seed-7 generator
     (the exact and the relaxed fp32 paths at the headline size)."""
     return make_problem(4096, 4096, 4096, "f32", "f32", seed=7, dist="uniform")
+
+
+# The int8 GEMM with per-column dequantisation (tessl architecture.md,
+# "Integer GEMM"): full-range int8 operands, fp32 output.
+
+def i8_problem(M, N, K, *, transpose_a=False, transpose_b=False, alpha=1.0, beta=0.0, seed=0,
+               c_fill="zero") -> Problem:
+    """int8 A and B uniform over [-128, 127] (drawn A then B then C, in their
+    stored shapes), fp32 C."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    A = torch.randint(-128, 128, (K, M) if transpose_a else (M, K), generator=g).to(torch.int8)
+    B = torch.randint(-128, 128, (N, K) if transpose_b else (K, N), generator=g).to(torch.int8)
+    C = torch.zeros(M, N) if c_fill == "zero" else _draw(g, (M, N), "uniform", 1.0)
+    return Problem(M, N, K, "i8", "f32", transpose_a, transpose_b, alpha, beta, A, B, C)
+
+
+def i8_dequant_4096():
+    """int8 NN 4096^3 with per-column scales uniform in [0, 1e-3) drawn after
+    A and B (seed 8).  Returns (problem, scale)."""
+    p = i8_problem(4096, 4096, 4096, seed=8)
+    scale = torch.rand(4096, generator=torch.Generator("cpu").manual_seed(9)) * 1e-3
+    return p, scale
 
