@@ -557,8 +557,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer (even CTA of a pair)
+        // One thread feeds the tensor core, and its work between two MMAs
+        // paces the K loop: rebuilding both shared-memory descriptors per
+        // MMA cost ~3 % of the square bf16 GEMM's time on GB300.  Each
+        // descriptor is built once per unit and then advanced by additions,
+        // and the ring position is stepped rather than divided out.
         if (lane == 0 && rank == 0) {
-            uint32_t it = 0, local = 0;
+            uint32_t stage = 0, ph = 0, local = 0;
             bool ok = true;
             int hint = 0;
             for (int u = cluster; ok && u < args.total_units; u += nclusters, ++local) {
@@ -570,6 +575,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     b_kmajor = gt.info[w.p].b_kmajor;
                     idesc = gt.info[w.p].idesc;
                 }
+                // descriptors of stage 0, K step 0.  A stage adds STAGE bytes
+                // to the start address; a K step of 16 adds 32 bytes along the
+                // swizzled row (K-major) or 16 rows of 128 bytes (MN-major).
+                // Shared addresses stay below 2^18 bytes, so the additions
+                // never carry out of the descriptor's 14-bit address field.
+                const uint32_t s0 = smem_u32(smem);
+                const uint64_t ad0 = a_kmajor ? smem_desc_sw128(s0, 16, 1024) : smem_desc_sw128(s0, 8192, 1024);
+                const uint64_t bd0 = b_kmajor ? smem_desc_sw128(s0 + A_BYTES, 16, 1024)
+                                              : smem_desc_sw128(s0 + A_BYTES, 8192, 1024);
+                const uint64_t astep = a_kmajor ? 2u : 128u, bstep = b_kmajor ? 2u : 128u;
                 const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
                 if (!wait_bar(smem_u32(&tempty_bar[acc]), aph ^ 1u, watch, W_TMEM_EMPTY)) {
                     ok = false;
@@ -578,22 +593,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    const uint32_t stage = it % S, ph = (it / S) & 1u;
                     if (!wait_bar(smem_u32(&full_bar[stage]), ph, watch, W_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * STAGE);
-                    const uint32_t sb = sa + A_BYTES;
+                    const uint64_t soff = (uint64_t)(stage * (STAGE >> 4));
 #pragma unroll
                     for (int k = 0; k < BK / MMA_K; ++k) {
-                        // K-major: advance 32 bytes along the swizzled row;
-                        // MN-major: advance 16 rows of 128 bytes.
-                        const uint64_t ad = a_kmajor ? smem_desc_sw128(sa + 32 * k, 16, 1024)
-                                                     : smem_desc_sw128(sa + 2048 * k, 8192, 1024);
-                        const uint64_t bd = b_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
-                                                     : smem_desc_sw128(sb + 2048 * k, 8192, 1024);
+                        const uint64_t ad = ad0 + soff + k * astep, bd = bd0 + soff + k * bstep;
                         const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
                         if (CG == 1)
                             mma_f16_ss(d_tmem, ad, bd, idesc, accum);
@@ -604,7 +612,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                         mma_commit(smem_u32(&empty_bar[stage]));
                     else
                         mma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
-                    ++it;
+                    if (++stage == (uint32_t)S) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 // test hook: withhold the "accumulator ready" signal of this
