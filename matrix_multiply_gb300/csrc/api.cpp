@@ -157,7 +157,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // group_m=<G> ffma=<small|large|panel> pack=<1> tail=<S> (K slices of the
 // last-wave tiles; 0 or 1 disables) sms=<N> (plan for N SMs) cg=<1|2>
 // (CTAs per tile) store=direct (plain stores of C instead of TMA stores)
-// grouped=0 (a grouped call enqueues its problems one by one).
+// grouped=0 (a grouped call enqueues its problems one by one) chunk=0 (an
+// MN-major operand is read 64 columns per copy instead of one chunked copy).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -166,6 +167,7 @@ struct Force {
     bool direct_store = false;
     int grouped = 1;
     int debug_drop = 0, debug_timeout_ms = 0;
+    int no_chunk = 0;
 };
 
 Force read_force()
@@ -198,6 +200,7 @@ Force read_force()
         else if (k == "grouped") f.grouped = std::atoi(v.c_str());
         else if (k == "debug_drop") f.debug_drop = std::atoi(v.c_str());
         else if (k == "debug_timeout_ms") f.debug_timeout_ms = std::atoi(v.c_str());
+        else if (k == "chunk") f.no_chunk = std::atoi(v.c_str()) == 0;
     }
     return f;
 }
@@ -380,6 +383,28 @@ bool encode_map(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, in
     return r == CUDA_SUCCESS;
 }
 
+// An MN-major operand (K rows of `extent` elements, leading dimension ld)
+// viewed as 64-element rows x K x extent/64 chunks, so that one box of
+// {64, 64, chunks} brings `chunks` adjacent 64-wide slices of one K block,
+// each as a 64 x 64 swizzled tile 8 KB after the previous one -- the layout
+// that separate 64-wide boxes give.  Only for extents that are multiples of
+// 64: no chunk then reaches past a row's last element.
+bool encode_chunked(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, int64_t extent, int64_t k,
+                    int64_t ld_elems, uint32_t chunks)
+{
+    if (extent % 64 != 0) return false;
+    const CUtensorMapDataType t = dt == TC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int64_t es = 2;
+    cuuint64_t dims[3] = {64, (cuuint64_t)k, (cuuint64_t)(extent / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld_elems * es), (cuuint64_t)(64 * es)};
+    cuuint32_t box[3] = {64, 64, chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = ctx->encode(m, t, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 tc_status_t read_status(tc_stream *s)
 {
     volatile unsigned *st = s->status_host;
@@ -524,17 +549,24 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
 
     const int64_t lda_use = p.pack_a ? lda_p : n.lda;
     const int64_t ldb_use = p.pack_b ? ldb_p : n.ldb;
+    const bool chunk_ok = !read_force().no_chunk;
     bool ok;
-    if (a.a_kmajor)
+    if (a.a_kmajor) {
         ok = encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->K, d->M, lda_use, a.a_3d, n.batch, sa, 64, BM);
-    else
-        ok = encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->M, d->K, lda_use, a.a_3d, n.batch, sa, 64, 64);
+    } else {
+        a.a_chunked = chunk_ok && !a.a_3d && encode_chunked(ctx, &L.tmA, d->a_dtype, Ause, d->M, d->K, lda_use, BM / 64);
+        ok = a.a_chunked || encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->M, d->K, lda_use, a.a_3d, n.batch, sa, 64, 64);
+    }
     if (ok) {
-        if (a.b_kmajor)
+        if (a.b_kmajor) {
             ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->K, d->N, ldb_use, a.b_3d, n.batch, sb, 64,
                             (uint32_t)(p.bn / p.cg));
-        else
-            ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, a.b_3d, n.batch, sb, 64, 64);
+        } else {
+            a.b_chunked = chunk_ok && !a.b_3d &&
+                          encode_chunked(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, (uint32_t)(p.bn / p.cg / 64));
+            ok = a.b_chunked ||
+                 encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, a.b_3d, n.batch, sb, 64, 64);
+        }
     }
     if (ok && a.c_tma)
         ok = encode_map(ctx, &L.tmC, d->c_dtype, C, d->N, d->M, n.ldc, a.c_3d, n.batch, a.stride_c, 32, 32,

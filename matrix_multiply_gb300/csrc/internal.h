@@ -58,6 +58,10 @@ struct MmaArgs {
     int group_m;           // rasterisation band height, in tile rows
     int a_kmajor, b_kmajor;
     int a_3d, b_3d;        // 3-D descriptors: the batch index is the third coordinate
+    // MN-major operand read through a chunked 3-D descriptor (64 elements,
+    // K rows, 64-element chunks): one copy brings a CTA's whole share of
+    // the operand for a K block instead of one copy per 64-wide chunk
+    int a_chunked, b_chunked;
     uint32_t idesc;        // tcgen05 instruction descriptor
     float alpha, beta;
     void *C;

@@ -123,6 +123,14 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = in_band / rows_in_band;
 }
 
+// First K block of slice s of S over num_kb blocks: floor(s * num_kb / S),
+// in 32-bit arithmetic whenever the product cannot overflow it.
+__device__ __forceinline__ int kb_split(int num_kb, int s, int S)
+{
+    if (num_kb < 65536) return (int)(((unsigned)s * (unsigned)num_kb) / (unsigned)S);
+    return (int)(((long long)s * num_kb) / S);
+}
+
 __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
 {
     Unit r;
@@ -140,8 +148,8 @@ __device__ __forceinline__ Unit decode_unit(const MmaArgs &a, int u)
     }
     r.ufirst = u - r.s;
     tile_coords(r.tile, a.tiles_m, a.tiles_n, a.tiles_per_batch, a.group_m, r.b, r.tm, r.tn);
-    r.kb0 = (int)(((long long)r.s * a.num_kb) / r.S);
-    r.kb1 = (int)(((long long)(r.s + 1) * a.num_kb) / r.S);
+    r.kb0 = kb_split(a.num_kb, r.s, r.S);
+    r.kb1 = kb_split(a.num_kb, r.s + 1, r.S);
     r.p = 0;
     return r;
 }
@@ -173,6 +181,30 @@ __device__ __forceinline__ Unit decode(const MmaArgs &a, const TableOf<GROUPED> 
         return decode_grouped(g, a.group_m, u, hint);
     else
         return decode_unit(a, u);
+}
+
+// What the MMA thread needs of unit u: its K-block count and (grouped) its
+// problem -- no tile coordinates, and no division for a whole-K unit.  The
+// thread's time between two tiles is time the tensor core stands idle.
+struct MmaUnit {
+    int nkb, p;
+};
+template <bool GROUPED>
+__device__ __forceinline__ MmaUnit mma_unit(const MmaArgs &a, const TableOf<GROUPED> &g, int u, int &hint)
+{
+    if constexpr (GROUPED) {
+        int p = hint;
+        while (p + 1 < g.count && g.info[p + 1].unit_begin <= u) ++p;
+        hint = p;
+        return MmaUnit{g.info[p].num_kb, p};
+    } else {
+        const int seg0_units = a.seg0_tiles * a.seg0_split;
+        const bool seg0 = u < seg0_units;
+        const int S = seg0 ? a.seg0_split : a.seg1_split;
+        if (S == 1) return MmaUnit{a.num_kb, 0};
+        const int s = (seg0 ? u : u - seg0_units) % S;
+        return MmaUnit{kb_split(a.num_kb, s + 1, S) - kb_split(a.num_kb, s, S), 0};
+    }
 }
 
 __device__ __forceinline__ void tma_load(const void *tmap, bool is3d, uint32_t dst, uint32_t bar, int c0,
@@ -497,12 +529,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 const CUtensorMap *mapA = &tmA, *mapB = &tmB;
                 int a_kmajor = args.a_kmajor, b_kmajor = args.b_kmajor;
                 bool a_3d = args.a_3d, b_3d = args.b_3d;
+                bool a_chunked = args.a_chunked, b_chunked = args.b_chunked;
                 if constexpr (GROUPED) {
                     mapA = &gt.tmA[w.p];
                     mapB = &gt.tmB[w.p];
                     a_kmajor = gt.info[w.p].a_kmajor;
                     b_kmajor = gt.info[w.p].b_kmajor;
                     a_3d = b_3d = false;
+                    a_chunked = b_chunked = false;
                 }
                 const int m0 = w.tm * (BM * CG) + (int)rank * BM;
                 const int n0 = w.tn * BN + (int)rank * BNL;
@@ -533,14 +567,25 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                             tma_load_2d_pair(dst, tm, fb, c0, c1);
                         }
                     };
+                    // one 3-D copy of a chunked descriptor: (element, K row, chunk)
+                    auto load_chunks = [&](const CUtensorMap *tm, uint32_t dst, int mn0) {
+                        if (CG == 1)
+                            tma_load_3d(dst, tm, fb, 0, k0, mn0 / 64);
+                        else
+                            tma_load_3d_pair(dst, tm, fb, 0, k0, mn0 / 64);
+                    };
                     if (a_kmajor) {
                         load(mapA, a_3d, sa, k0, m0);
+                    } else if (a_chunked) {
+                        load_chunks(mapA, sa, m0);
                     } else {
                         load(mapA, a_3d, sa, m0, k0);
                         load(mapA, a_3d, sa + 8192, m0 + 64, k0);
                     }
                     if (b_kmajor) {
                         load(mapB, b_3d, sb, k0, n0);
+                    } else if (b_chunked) {
+                        load_chunks(mapB, sb, n0);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BNL / 64; ++j) load(mapB, b_3d, sb + j * 8192, n0 + 64 * j, k0);
@@ -567,7 +612,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             bool ok = true;
             int hint = 0;
             for (int u = cluster; ok && u < args.total_units; u += nclusters, ++local) {
-                const Unit w = decode<GROUPED>(args, gt, u, hint);
+                const MmaUnit w = mma_unit<GROUPED>(args, gt, u, hint);
                 int a_kmajor = args.a_kmajor, b_kmajor = args.b_kmajor;
                 uint32_t idesc = args.idesc;
                 if constexpr (GROUPED) {
@@ -592,7 +637,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int kb = 0; kb < w.nkb; ++kb) {
                     if (!wait_bar(smem_u32(&full_bar[stage]), ph, watch, W_FULL)) {
                         ok = false;
                         break;
@@ -602,7 +647,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / MMA_K; ++k) {
                         const uint64_t ad = ad0 + soff + k * astep, bd = bd0 + soff + k * bstep;
-                        const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
+                        const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
                         if (CG == 1)
                             mma_f16_ss(d_tmem, ad, bd, idesc, accum);
                         else

@@ -164,6 +164,26 @@ def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
     assert np.array_equal(oracle.decode(out), R), ctx.last_kernel
 
 
+@pytest.mark.parametrize("spec", ["", "cg=2 bn=256", "cg=2 bn=128", "cg=1 bn=256", "cg=1 bn=192", "cg=1 bn=64",
+                                  "bn=128 split=3", "cg=2 sms=8 tail=3"])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_chunked_descriptors_bitwise(ctx, force, spec, ta, tb):
+    """An MN-major operand whose extent is a multiple of 64 is read with one
+    3-D copy per K block (64-wide chunks as a third dimension); the result
+    equals that of one copy per chunk bit for bit (same bytes, same MMAs).
+    576 rows and 448 columns end inside a tile, so the last tiles' upper
+    chunks lie past the operand and must read as zeros; K = 1000 is ragged."""
+    p = synthetic.make_problem(576, 448, 1000, "bf16", "f32", transpose_a=ta, transpose_b=tb, alpha=0.75,
+                               beta=0.5, seed=91, dist="normal", c_fill="uniform")
+    force((spec + " chunk=0").strip())
+    ref = run_problem(ctx, p)
+    force(spec)
+    got = run_problem(ctx, p)
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), ctx.last_kernel
+    R, T = oracle.gemm(p)
+    parity.check(oracle.decode(got), R, T, "f32", what=f"{spec} {ctx.last_kernel}")
+
+
 def test_rank_one_exact(ctx):
     for dt in ("f16", "bf16"):
         p = synthetic.make_problem(190, 170, 1, dt, "f32", seed=43, dist="normal")
