@@ -520,10 +520,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
     if (warp == 4) {
         // ------------------------------------------------ TMA producer
+        // Its loop per K block is short too (the copies it issues per K block
+        // pace it): barrier and stage addresses come from bases computed once.
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t stage = 0, ph = 0, issued = 0;
             bool ok = true;
             int hint = 0;
+            const uint32_t s0 = smem_u32(smem);
+            const uint32_t full0 = smem_u32(&full_bar[0]), empty0 = smem_u32(&empty_bar[0]);
+            // the even CTA's barriers count both CTAs' bytes
+            const uint32_t full0_lead = CG == 2 ? mapa_shared(full0, 0) : full0;
             for (int u = cluster; ok && u < args.total_units; u += nclusters) {
                 const Unit w = decode<GROUPED>(args, gt, u, hint);
                 const CUtensorMap *mapA = &tmA, *mapB = &tmB;
@@ -541,21 +547,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 const int m0 = w.tm * (BM * CG) + (int)rank * BM;
                 const int n0 = w.tn * BN + (int)rank * BNL;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    const uint32_t stage = it % S, ph = (it / S) & 1u;
-                    if (!wait_bar(smem_u32(&empty_bar[stage]), ph ^ 1u, watch, W_EMPTY)) {
+                    if (!wait_bar(empty0 + 8 * stage, ph ^ 1u, watch, W_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb_local = smem_u32(&full_bar[stage]);
-                    uint32_t fb = fb_local;
-                    if (CG == 1) {
-                        mbar_arrive_expect_tx(fb_local, STAGE);
-                    } else {
-                        // the even CTA's barrier counts both CTAs' bytes
-                        fb = mapa_shared(fb_local, 0);
-                        if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * STAGE);
-                    }
-                    const uint32_t sa = smem_u32(smem + stage * STAGE);
+                    const uint32_t fb = full0_lead + 8 * stage;
+                    if (CG == 1)
+                        mbar_arrive_expect_tx(full0 + 8 * stage, STAGE);
+                    else if (rank == 0)
+                        mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE);
+                    const uint32_t sa = s0 + stage * STAGE;
                     const uint32_t sb = sa + A_BYTES;
                     const int k0 = kb * BK;
                     auto load = [&](const CUtensorMap *tm, bool is3d, uint32_t dst, int c0, int c1) {
@@ -590,12 +591,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < BNL / 64; ++j) load(mapB, b_3d, sb + j * 8192, n0 + 64 * j, k0);
                     }
-                    ++it;
+                    ++issued;
+                    if (++stage == (uint32_t)S) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (!ok && rank == 0) {
                 // let the copies already issued land before shared memory is released
-                for (uint32_t i = (it > (uint32_t)S ? it - S : 0u); i < it; ++i)
+                for (uint32_t i = (issued > (uint32_t)S ? issued - S : 0u); i < issued; ++i)
                     drain_wait(smem_u32(&full_bar[i % S]), (i / S) & 1u);
             }
         }
@@ -685,6 +690,24 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         uint32_t local = 0, ebuf = 0;
         const int row_in_tile = (int)rank * BM + warp * 32 + lane;
         uint8_t *my_stage = cstage + warp * 2 * EPI_STAGE_BYTES;
+        // The warp's staging is either two buffers that alternate over the
+        // TMA stores actually issued (a buffer is refilled only after one
+        // newer store was committed) or, on the plain-store path, one
+        // transpose buffer.  A grouped launch's problems may switch between
+        // the two: the switch first lets every earlier store finish reading.
+        enum { STG_TMA = 0, STG_XPOSE = 1 };
+        int emode = STG_TMA;
+        auto staging = [&](int mode) -> uint8_t * {
+            if (mode != emode) {
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                emode = mode;
+            }
+            if (mode == STG_XPOSE) return my_stage;
+            uint8_t *buf = my_stage + ebuf * EPI_STAGE_BYTES;
+            ebuf ^= 1u;
+            return buf;
+        };
         // grouped: the launch-wide arguments with the current problem's
         // epilogue fields (M, N, C, ldc, dtype, alpha, beta) swapped in
         MmaArgs ga = args;
@@ -694,8 +717,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         // alpha/beta, then the chunk to C (TMA store when C allows it)
         auto emit = [&](int b, long long row, long long col0, float (&v)[32]) {
             if (!ea.c_tma) {
-                // both staging buffers of this warp serve as one transpose buffer
-                float *xbuf = reinterpret_cast<float *>(my_stage);
+                float *xbuf = reinterpret_cast<float *>(staging(STG_XPOSE));
                 if constexpr (EPI)
                     if (ea.col_scale) col_scale_apply(ea, lane, col0, v);
                 apply_alpha_beta_staged(ea, xbuf, lane, b, row - lane, col0, v);
@@ -708,14 +730,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             apply_alpha_beta(ea, b, row, col0, v);
             if constexpr (EPI) bias_act(ea, lane, col0, v);
             if (ea.c_tma) {
-                // buffers alternate over the stores actually issued, so a
-                // buffer is reused only after one newer store was committed
+                // buffers rotate over the stores actually issued
                 const long long row0 = row - lane;
-                if (row0 < ea.M && col0 < ea.N) {
-                    store_tma(mapC, ea.c_3d, ea.c_dtype, my_stage + ebuf * EPI_STAGE_BYTES, lane, b, row0,
-                              col0, v);
-                    ebuf ^= 1u;
-                }
+                if (row0 < ea.M && col0 < ea.N)
+                    store_tma(mapC, ea.c_3d, ea.c_dtype, staging(STG_TMA), lane, b, row0, col0, v);
             } else {
                 store_direct(ea, b, row, col0, v);
             }
@@ -794,8 +812,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    store_tma(&tmW, false, TC_F32, my_stage + ebuf * EPI_STAGE_BYTES, lane, 0, wrow0, c * 32, v);
-                    ebuf ^= 1u;
+                    store_tma(&tmW, false, TC_F32, staging(STG_TMA), lane, 0, wrow0, c * 32, v);
                 }
             }
         }
