@@ -599,14 +599,12 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         r.ldc = n.ldc;
         r.stride_c = a.stride_c;
         r.c_dtype = d->c_dtype;
-        r.c_vec_ok = aligned16(C) && n.ldc % 4 == 0 && a.stride_c % 4 == 0;   // 4-element vectors
+        r.c_vec_ok = a.c_vec_ok;   // 16-byte vectors of 8 elements (two for fp32)
         r.bias = a.bias;
         r.act = a.act;
         r.col_scale = col_scale;
         r.int_sum = col_scale != nullptr;
-        const int64_t work = (int64_t)r.ntiles * rows_per_tile * (p.bn / 4);
-        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), (int64_t)ctx->num_sms * 8));
-        if ((e = launch_reduce(r, grid, s->st)) != cudaSuccess) return TC_ERR_CUDA;
+        if ((e = launch_reduce(r, s->st)) != cudaSuccess) return TC_ERR_CUDA;
         ++launches;
     }
     ctx->launches += launches;
@@ -1473,10 +1471,8 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
         r.ldc = n.ldc;
         r.stride_c = 0;
         r.c_dtype = d->c_dtype;
-        r.c_vec_ok = aligned16(C) && n.ldc % 4 == 0;   // 4-element vectors
-        const int64_t work = tiles * BM * (bn / 4);
-        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), (int64_t)sms * 8));
-        if (launch_reduce(r, grid, stream) != cudaSuccess) return TC_ERR_CUDA;
+        r.c_vec_ok = a.c_vec_ok;   // 16-byte vectors of 8 elements (two for fp32)
+        if (launch_reduce(r, stream) != cudaSuccess) return TC_ERR_CUDA;
     }
     return TC_OK;
 }

@@ -140,7 +140,9 @@ struct ReduceArgs {
     const float *col_scale;
     int int_sum;           // the slices are integers: add them as 64-bit integers
 };
-cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st);
+// One CTA of bn threads per 8 (or, for small reductions, 4) rows of a tile,
+// 8 (4) columns per thread; c_vec_ok allows 16-byte accesses to C.
+cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st);
 
 // Static scratch of the entry point that allocates nothing: split-K partial
 // tiles (at most NOALLOC_PARTIAL_BYTES) and one status word.

@@ -900,99 +900,129 @@ int pairs_for()
 
 // ---------------------------------------------------------------- split-K reduction
 // C tile = alpha * (p_0 + p_1 + ... + p_{S-1}) + beta * C_old, the slices
-// summed in slice order (deterministic).  Each thread owns four consecutive
-// columns of one tile row: loads of a slice and stores of C are contiguous
-// across a warp.  Launched as a programmatic dependent of the GEMM kernel:
-// griddepcontrol.wait returns once that grid has finished and its partial
-// tiles are visible.
+// summed in slice order (deterministic).  One CTA of bn threads owns COLS
+// rows of one tile (its coordinates are decoded once per CTA); each thread
+// owns COLS consecutive columns of one row, so every slice is read with
+// 16-byte loads and C written with 16-byte (COLS = 8) or 8/16-byte stores,
+// contiguous across a warp.  COLS = 8 unless that leaves few threads (a
+// long split of few tiles), where COLS = 4 doubles them.  Launched as a
+// programmatic dependent of the GEMM kernel: griddepcontrol.wait returns
+// once that grid has finished and its partial tiles are visible.
 // INT: the int8 path -- the slices hold exact integers, summed in 64 bits,
 // then scaled per column (a template flag, so the fp32 reduction carries
 // none of it).
-template <bool INT>
+template <bool INT, int COLS>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
 {
+    static_assert(COLS == 4 || COLS == 8, "whole 16-byte loads");
     griddep_wait();
-    const int groups = r.bn / 4;
-    const long long per_tile = (long long)r.rows_per_tile * groups;
-    const long long total = per_tile * r.ntiles;
+    const int groups = r.bn / COLS;                    // threads per row
+    const int ctas_per_tile = r.rows_per_tile / COLS;  // COLS rows per CTA
+    const int t = blockIdx.x / ctas_per_tile;
+    const int row = (blockIdx.x - t * ctas_per_tile) * COLS + (int)threadIdx.x / groups;
+    const int cc = (int)threadIdx.x % groups;
+    int b, tm, tn;
+    tile_coords(r.first_tile + t, r.tiles_m, r.tiles_n, r.tiles_per_batch, r.group_m, b, tm, tn);
+    const long long grow = (long long)tm * r.rows_per_tile + row;
+    const long long gcol = (long long)tn * r.bn + cc * COLS;
+    if (grow >= r.M || gcol >= r.N) return;
     const size_t slice = (size_t)r.rows_per_tile * r.bn;      // floats per partial tile
-    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total;
-         g += (long long)gridDim.x * blockDim.x) {
-        const int t = (int)(g / per_tile);
-        const long long rem = g - (long long)t * per_tile;
-        const int row = (int)(rem / groups);
-        const int c4 = (int)(rem - (long long)row * groups);
-        int b, tm, tn;
-        tile_coords(r.first_tile + t, r.tiles_m, r.tiles_n, r.tiles_per_batch, r.group_m, b, tm, tn);
-        const long long grow = (long long)tm * r.rows_per_tile + row;
-        const long long gcol = (long long)tn * r.bn + c4 * 4;
-        if (grow >= r.M || gcol >= r.N) continue;
-        const float *src = r.ws + (size_t)t * r.S * slice + (size_t)row * r.bn + c4 * 4;
-        float v[4];
-        if constexpr (INT) {
-            // every slice holds exact integers: their sum, exact in 64 bits,
-            // then one rounding to fp32
-            long long acc[4] = {0, 0, 0, 0};
-            for (int s = 0; s < r.S; ++s) {
-                const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + s * slice));
-                acc[0] += __float2ll_rn(p.x);
-                acc[1] += __float2ll_rn(p.y);
-                acc[2] += __float2ll_rn(p.z);
-                acc[3] += __float2ll_rn(p.w);
-            }
+    const float *src = r.ws + (size_t)t * r.S * slice + (size_t)row * r.bn + cc * COLS;
+    // the thread's COLS columns of slice s
+    auto load = [&](int s, float (&p)[COLS]) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __ll2float_rn(acc[j]);
+        for (int q = 0; q < COLS / 4; ++q) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(src + s * slice) + q);
+            p[4 * q + 0] = x.x;
+            p[4 * q + 1] = x.y;
+            p[4 * q + 2] = x.z;
+            p[4 * q + 3] = x.w;
+        }
+    };
+    // Slices are added one after another in slice order; up to four
+    // slices' loads are issued before their additions, so that a long
+    // split (few threads, many slices) keeps several loads in flight.
+    using Acc = std::conditional_t<INT, long long, float>;
+    Acc acc[COLS] = {};
+    auto add = [&](const float (&p)[COLS]) {
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) {
+            if constexpr (INT)
+                acc[j] += __float2ll_rn(p[j]);     // exact integers: an exact 64-bit sum
+            else
+                acc[j] += p[j];
+        }
+    };
+    int s = 0;
+    for (; s + 4 <= r.S; s += 4) {
+        float p[4][COLS];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) load(s + i, p[i]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) add(p[i]);
+    }
+    for (; s < r.S; ++s) {
+        float p[COLS];
+        load(s, p);
+        add(p);
+    }
+    float v[COLS];
+    if constexpr (INT) {
+        // one rounding of the exact sum to fp32, then the column's scale
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) v[j] = __ll2float_rn(acc[j]);
+#pragma unroll
+        for (int j = 0; j < COLS; ++j)
+            if (gcol + j < r.N) v[j] *= r.col_scale[gcol + j];
+    } else {
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) v[j] = acc[j];
+    }
+    const long long base = (long long)b * r.stride_c + grow * r.ldc + gcol;
+#pragma unroll
+    for (int j = 0; j < COLS; ++j) {
+        const float c = (r.beta != 0.0f && gcol + j < r.N) ? load_c(r.C, base + j, r.c_dtype) : 0.0f;
+        v[j] = (r.beta != 0.0f) ? fmaf(r.beta, c, r.alpha * v[j]) : r.alpha * v[j];
+        if (r.bias && gcol + j < r.N) v[j] += load_c(r.bias, gcol + j, r.c_dtype);
+        if (r.act == TC_ACT_GELU_TANH) v[j] = gelu_tanh(v[j]);
+    }
+    if (r.c_vec_ok && gcol + COLS <= r.N) {
+        if (r.c_dtype == TC_F32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(r.C) + base);
+#pragma unroll
+            for (int q = 0; q < COLS / 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else if constexpr (COLS == 8) {
+            uint4 w;
+            w.x = pack2(v[0], v[1], r.c_dtype);
+            w.y = pack2(v[2], v[3], r.c_dtype);
+            w.z = pack2(v[4], v[5], r.c_dtype);
+            w.w = pack2(v[6], v[7], r.c_dtype);
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(r.C) + base) = w;
         } else {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < r.S; ++s) {
-                const float4 p = __ldcg(reinterpret_cast<const float4 *>(src + s * slice));
-                acc.x += p.x;
-                acc.y += p.y;
-                acc.z += p.z;
-                acc.w += p.w;
-            }
-            v[0] = acc.x;
-            v[1] = acc.y;
-            v[2] = acc.z;
-            v[3] = acc.w;
+            uint2 w;
+            w.x = pack2(v[0], v[1], r.c_dtype);
+            w.y = pack2(v[2], v[3], r.c_dtype);
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(r.C) + base) = w;
         }
-        if constexpr (INT) {
+    } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (gcol + j < r.N) v[j] *= r.col_scale[gcol + j];
-        }
-        const long long base = (long long)b * r.stride_c + grow * r.ldc + gcol;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float c = (r.beta != 0.0f && gcol + j < r.N) ? load_c(r.C, base + j, r.c_dtype) : 0.0f;
-            v[j] = (r.beta != 0.0f) ? fmaf(r.beta, c, r.alpha * v[j]) : r.alpha * v[j];
-            if (r.bias && gcol + j < r.N) v[j] += load_c(r.bias, gcol + j, r.c_dtype);
-            if (r.act == TC_ACT_GELU_TANH) v[j] = gelu_tanh(v[j]);
-        }
-        if (r.c_vec_ok && gcol + 4 <= r.N) {
-            if (r.c_dtype == TC_F32) {
-                *reinterpret_cast<float4 *>(static_cast<float *>(r.C) + base) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-                uint2 w;
-                w.x = pack2(v[0], v[1], r.c_dtype);
-                w.y = pack2(v[2], v[3], r.c_dtype);
-                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(r.C) + base) = w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (gcol + j < r.N) store_c1(r.C, base + j, v[j], r.c_dtype);
-        }
+        for (int j = 0; j < COLS; ++j)
+            if (gcol + j < r.N) store_c1(r.C, base + j, v[j], r.c_dtype);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st)
+cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st)
 {
+    if (r.bn % 8 != 0 || r.bn > 256 || r.rows_per_tile % 8 != 0 || r.ntiles < 1) return cudaErrorInvalidValue;
+    // 8 columns per thread unless that leaves fewer threads than about one
+    // 256-thread CTA per SM of a GB300
+    const long long threads8 = (long long)r.ntiles * r.rows_per_tile * (r.bn / 8);
+    const int cols = threads8 < 152LL * 256 ? 4 : 8;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.gridDim = dim3((unsigned)r.ntiles * (unsigned)(r.rows_per_tile / cols), 1, 1);
+    cfg.blockDim = dim3((unsigned)r.bn, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1000,8 +1030,11 @@ cudaError_t launch_reduce(const ReduceArgs &r, int grid, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (r.int_sum) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true>, r);
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false>, r);
+    if (r.int_sum)
+        return cols == 4 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true, 4>, r)
+                         : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true, 8>, r);
+    return cols == 4 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false, 4>, r)
+                     : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false, 8>, r);
 }
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
