@@ -16,8 +16,19 @@ constexpr int MMA_K = 16;                       // K of one kind::f16 tcgen05.mm
 constexpr int MMA_THREADS = 192;                // 4 epilogue warps, TMA warp, MMA warp
 constexpr int SMEM_LIMIT = 232448;              // max dynamic shared memory per block
 constexpr int EPI_STAGE_BYTES = 4096;           // one 32 x 32 output chunk (fp32 worst case)
-constexpr int EPI_SMEM = 4 * 2 * EPI_STAGE_BYTES;  // 4 epilogue warps, double buffered
-constexpr int SMEM_RESERVE = 1024 + 256 + EPI_SMEM;  // alignment slack + barriers + epilogue staging
+
+// Epilogue staging per warp: two chunk buffers (one TMA store may still be
+// reading the other), except for the one-CTA 192-wide tile, whose 40 KB
+// stages leave room for a fifth stage only with one buffer (its K loop is
+// bound by the latency the ring covers, its single wave drains once).  The
+// plain-store path's 32 x 33-float transpose buffer fits either way.
+__host__ __device__ constexpr int epi_bufs(int bn, int cg) { return (bn == 192 && cg == 1) ? 1 : 2; }
+__host__ __device__ constexpr int epi_warp_bytes(int bn, int cg) { return epi_bufs(bn, cg) == 1 ? 5120 : 8192; }
+__host__ __device__ constexpr int epi_smem(int bn, int cg) { return 4 * epi_warp_bytes(bn, cg); }   // 4 epilogue warps
+__host__ __device__ constexpr int smem_reserve(int bn, int cg)   // alignment slack + barriers + epilogue staging
+{
+    return 1024 + 256 + epi_smem(bn, cg);
+}
 
 // One pipeline stage of a CTA: its 128 rows of A and its share of B (all BN
 // columns for a single CTA; BN/2 for each CTA of a pair running
@@ -29,13 +40,13 @@ __host__ __device__ constexpr int tmem_cols(int bn)
 }
 __host__ __device__ constexpr int mma_stages(int bn, int cg)
 {
-    return ((SMEM_LIMIT - SMEM_RESERVE) / stage_bytes(bn, cg)) > 8
+    return ((SMEM_LIMIT - smem_reserve(bn, cg)) / stage_bytes(bn, cg)) > 8
                ? 8
-               : ((SMEM_LIMIT - SMEM_RESERVE) / stage_bytes(bn, cg));
+               : ((SMEM_LIMIT - smem_reserve(bn, cg)) / stage_bytes(bn, cg));
 }
 __host__ __device__ constexpr int mma_smem_bytes(int bn, int cg)
 {
-    return mma_stages(bn, cg) * stage_bytes(bn, cg) + SMEM_RESERVE;
+    return mma_stages(bn, cg) * stage_bytes(bn, cg) + smem_reserve(bn, cg);
 }
 
 // Device-side arguments of the tensor-core kernel (the two TMA descriptors

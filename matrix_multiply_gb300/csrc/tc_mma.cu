@@ -394,10 +394,13 @@ __device__ __forceinline__ void store_staged(const MmaArgs &a, float *buf, int l
 // tensor.  fp32 rows are 128 bytes (128-byte swizzle: 16-byte unit q of row
 // r sits at q ^ (r % 8)); 16-bit rows are 64 bytes (64-byte swizzle:
 // q ^ ((r / 2) % 4)).  Either way each group of 8 lanes covers all 32 banks.
+// BUFS: the warp's staging buffers (the stores that may still be reading
+// one of the others: BUFS - 1).
+template <int BUFS>
 __device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int dtype, uint8_t *buf, int lane,
                                           int b, long long row0, long long col0, const float (&v)[32])
 {
-    if (lane == 0) bulk_wait_read<1>();      // this buffer's previous store has read it
+    if (lane == 0) bulk_wait_read<BUFS - 1>();      // this buffer's previous store has read it
     __syncwarp();
     if (dtype == TC_F32) {
 #pragma unroll
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *cstage = smem + S * STAGE;            // epilogue staging, 2 x 4 KB per warp
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + EPI_SMEM);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + epi_smem(BN, CG));
     uint64_t *full_bar = bars;
     uint64_t *empty_bar = bars + S;
     uint64_t *tfull_bar = bars + 2 * S;
@@ -689,11 +692,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         // ------------------------------------------------ epilogue warps 0-3
         uint32_t local = 0, ebuf = 0;
         const int row_in_tile = (int)rank * BM + warp * 32 + lane;
-        uint8_t *my_stage = cstage + warp * 2 * EPI_STAGE_BYTES;
-        // The warp's staging is either two buffers that alternate over the
-        // TMA stores actually issued (a buffer is refilled only after one
-        // newer store was committed) or, on the plain-store path, one
-        // transpose buffer.  A grouped launch's problems may switch between
+        constexpr int EBUFS = epi_bufs(BN, CG);
+        uint8_t *my_stage = cstage + warp * epi_warp_bytes(BN, CG);
+        // The warp's staging is either its TMA chunk buffers (two that
+        // alternate over the stores actually issued, a buffer refilled only
+        // after one newer store was committed; or one, refilled after its
+        // store has read it) or, on the plain-store path, one transpose
+        // buffer.  A grouped launch's problems may switch between
         // the two: the switch first lets every earlier store finish reading.
         enum { STG_TMA = 0, STG_XPOSE = 1 };
         int emode = STG_TMA;
@@ -705,7 +710,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             }
             if (mode == STG_XPOSE) return my_stage;
             uint8_t *buf = my_stage + ebuf * EPI_STAGE_BYTES;
-            ebuf ^= 1u;
+            if (EBUFS == 2) ebuf ^= 1u;
             return buf;
         };
         // grouped: the launch-wide arguments with the current problem's
@@ -733,7 +738,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 // buffers rotate over the stores actually issued
                 const long long row0 = row - lane;
                 if (row0 < ea.M && col0 < ea.N)
-                    store_tma(mapC, ea.c_3d, ea.c_dtype, staging(STG_TMA), lane, b, row0, col0, v);
+                    store_tma<EBUFS>(mapC, ea.c_3d, ea.c_dtype, staging(STG_TMA), lane, b, row0, col0, v);
             } else {
                 store_direct(ea, b, row, col0, v);
             }
@@ -812,7 +817,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    store_tma(&tmW, false, TC_F32, staging(STG_TMA), lane, 0, wrow0, c * 32, v);
+                    store_tma<EBUFS>(&tmW, false, TC_F32, staging(STG_TMA), lane, 0, wrow0, c * 32, v);
                 }
             }
         }
