@@ -184,6 +184,23 @@ def test_chunked_descriptors_bitwise(ctx, force, spec, ta, tb):
     parity.check(oracle.decode(got), R, T, "f32", what=f"{spec} {ctx.last_kernel}")
 
 
+@pytest.mark.parametrize("spec", ["cg=1 bn=192", "cg=1 bn=192 split=3", "cg=1 bn=192 store=direct"])
+@pytest.mark.parametrize("c", ["f16", "f32"])
+def test_single_buffer_epilogue_192(ctx, force, spec, c):
+    """The 128x192 kernel stages its epilogue in one buffer per warp (for a
+    fifth pipeline stage): TMA-stored C, C through the transpose buffer (an
+    odd ldc, beta != 0 so C_old is read back through it too), plain stores,
+    and split-K partials all go through that one buffer."""
+    force(spec)
+    for ldc in (0, 389):
+        p = synthetic.make_problem(700, 384, 1500, "f16", c, transpose_b=True, alpha=0.75, beta=-0.5, seed=93,
+                                   dist="normal", c_fill="uniform", ldc=ldc)
+        out = run_problem(ctx, p, ldc=ldc)
+        assert "128x192" in ctx.last_kernel, ctx.last_kernel
+        R, T = oracle.gemm(p)
+        parity.check(oracle.decode(out)[:, :384], R, T, c, what=f"{spec} ldc={ldc} {ctx.last_kernel}")
+
+
 def test_rank_one_exact(ctx):
     for dt in ("f16", "bf16"):
         p = synthetic.make_problem(190, 170, 1, dt, "f32", seed=43, dist="normal")
