@@ -138,10 +138,18 @@ tc_status_t validate(const tc_gemm_desc *d, const void *A, const void *B, const 
 
 // --------------------------------------------------------------- dispatch
 
+// int8 GEMM limits: K at most I8_K_MAX; K slices of I8_SLICE_KB blocks (1024
+// products, |sum| <= 2^24: exact in an fp32 accumulator); the slices are
+// summed on chip as int32 when K <= I8_ONCHIP_K_MAX (|sum| <= 2^14 K <= 2^30).
+constexpr int I8_K_MAX = 131072;
+constexpr int I8_SLICE_KB = 16;
+constexpr int I8_ONCHIP_K_MAX = 65536;    // int32 running sums: |sum| <= 2^14 K <= 2^30
+
 struct Plan {
     bool ffma = false;
     int ffma_tile = FFMA_SMALL;
     int bn = 256, cg = 1, split = 1, grid = 1, group_m = 8;
+    bool i8acc = false;        // int8: exact K slices summed in TMEM (one unit per tile)
     int64_t seg0_tiles = 0, split_base = 0;
     int seg0_split = 1, seg1_split = 1;
     bool tma_store = true;
@@ -158,7 +166,9 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // last-wave tiles; 0 or 1 disables) sms=<N> (plan for N SMs) cg=<1|2>
 // (CTAs per tile) store=direct (plain stores of C instead of TMA stores)
 // grouped=0 (a grouped call enqueues its problems one by one) chunk=0 (an
-// MN-major operand is read 64 columns per copy instead of one chunked copy).
+// MN-major operand is read 64 columns per copy instead of one chunked copy)
+// i8acc=0 (int8: K slices through memory and the reduction kernel, not
+// summed on chip).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -168,6 +178,7 @@ struct Force {
     int grouped = 1;
     int debug_drop = 0, debug_timeout_ms = 0;
     int no_chunk = 0;
+    int i8acc = -1;
 };
 
 Force read_force()
@@ -201,6 +212,7 @@ Force read_force()
         else if (k == "debug_drop") f.debug_drop = std::atoi(v.c_str());
         else if (k == "debug_timeout_ms") f.debug_timeout_ms = std::atoi(v.c_str());
         else if (k == "chunk") f.no_chunk = std::atoi(v.c_str()) == 0;
+        else if (k == "i8acc") f.i8acc = std::atoi(v.c_str());
     }
     return f;
 }
@@ -489,6 +501,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     MmaLaunch L{};
     L.bn = p.bn;
     L.cg = p.cg;
+    L.i8acc = p.i8acc ? 1 : 0;
     L.grid = p.grid;
     if (p.cg == 2) {
         // no more pairs than can be resident at once (a persistent grid)
@@ -539,6 +552,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.bias = epi ? epi->bias : nullptr;
     a.act = epi ? (int)epi->activation : (int)TC_ACT_NONE;
     a.col_scale = col_scale;
+    a.slice_kb = p.i8acc ? I8_SLICE_KB : 0;
     const int64_t kb_per_unit = a.num_kb;
     a.timeout_ns = 4000000000ull + (unsigned long long)kb_per_unit * 20000ull;
     {
@@ -919,8 +933,6 @@ tc_status_t run_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *e
 // of at most 16 K blocks (1024 products, |sum| <= 2^24: exact in the fp32
 // accumulator); the reduction kernel adds the slices as 64-bit integers,
 // rounds once to fp32, scales by the column's factor, then alpha/beta.
-constexpr int I8_K_MAX = 131072;
-constexpr int I8_SLICE_KB = 16;
 
 tc_status_t run_i8(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, const void *A, const void *B,
                    void *C, tc_stream *s)
@@ -951,23 +963,44 @@ tc_status_t run_i8(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, c
     if ((st = validate(&d2, A2, B2, C, 1, 0, 0, 0, &n2)) != TC_OK) return st;
     Plan p;
     if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p)) != TC_OK) return st;
-    // every tile in the same K slices of at most I8_SLICE_KB blocks (the
-    // plan's own tail split would add its slices in fp32)
     const int64_t num_kb = cdiv(d->K, BK);
     const int S = (int)cdiv(num_kb, I8_SLICE_KB);
-    const int64_t tiles = cdiv(d->M, BM * p.cg) * cdiv(d->N, p.bn);
-    p.tiles = tiles;
-    p.seg0_tiles = tiles;
-    p.seg0_split = S;
-    p.seg1_split = 1;
-    p.split_base = 0;
-    p.units = tiles * S;
-    p.split = S > 1 ? 2 : 1;
+    char buf[48];
+    const Force f = read_force();
+    if (d->K <= I8_ONCHIP_K_MAX && f.i8acc != 0) {
+        // one unit per tile, its K slices summed as int32 in TMEM (|sum| <=
+        // 2^14 K <= 2^30): 128-wide tiles (two accumulators and the sums
+        // fit in TMEM), CTA pairs unless that leaves half the SMs idle
+        const int64_t tiles2 = cdiv(d->M, 2 * BM) * cdiv(d->N, 128);
+        p.cg = (tiles2 * 2 >= ctx->num_sms) ? 2 : 1;
+        p.bn = 128;
+        p.i8acc = true;
+        const int64_t tiles = cdiv(d->M, BM * p.cg) * cdiv(d->N, 128);
+        p.tiles = p.seg0_tiles = tiles;
+        p.seg0_split = p.seg1_split = 1;
+        p.split_base = tiles;
+        p.units = tiles;
+        p.split = 1;
+        std::snprintf(buf, sizeof buf, "_i8acc_s%d", S);
+        p.name = std::string("tcgen05_") + (d->transpose_a ? (d->transpose_b ? "tt" : "tn") : (d->transpose_b ? "nt" : "nn")) +
+                 "_bf16_" + (d->c_dtype == TC_F32 ? "f32" : d->c_dtype == TC_BF16 ? "bf16" : "f16") +
+                 (p.cg == 2 ? "_256x128_pair" : "_128x128");
+    } else {
+        // every tile in the same K slices of at most I8_SLICE_KB blocks (the
+        // plan's own tail split would add its slices in fp32)
+        const int64_t tiles = cdiv(d->M, BM * p.cg) * cdiv(d->N, p.bn);
+        p.tiles = tiles;
+        p.seg0_tiles = tiles;
+        p.seg0_split = S;
+        p.seg1_split = 1;
+        p.split_base = 0;
+        p.units = tiles * S;
+        p.split = S > 1 ? 2 : 1;
+        std::snprintf(buf, sizeof buf, "_i8s%d", S);
+    }
     if (p.units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
     const int workers = p.cg == 2 ? std::max(ctx->num_sms / 2, 1) : ctx->num_sms;
     p.grid = (int)std::min<int64_t>(p.units, workers) * p.cg;
-    char buf[32];
-    std::snprintf(buf, sizeof buf, "_i8s%d", S);
     const WidenArgs wa{static_cast<const int8_t *>(A), A2, n.a_rows, n.a_cols, n.lda, lda2};
     const WidenArgs wb{static_cast<const int8_t *>(B), B2, n.b_rows, n.b_cols, n.ldb, ldb2};
     if (launch_widen(wa, s->st) != cudaSuccess || launch_widen(wb, s->st) != cudaSuccess) return TC_ERR_CUDA;

@@ -92,11 +92,13 @@ struct MmaArgs {
     const void *bias;
     int act;
     const float *col_scale;
+    int slice_kb;          // on-chip int8 accumulation: K blocks per exact slice
 };
 
 struct MmaLaunch {
     int bn;
     int cg;      // CTAs per tile: 1, or 2 for a CTA pair (cluster of two)
+    int i8acc;   // int8 slices summed in TMEM (BN = 128 only; args.slice_kb, col_scale)
     int grid;    // CTAs (a multiple of cg)
     CUtensorMap tmA, tmB, tmC, tmW;   // A, B, C and the split-K workspace
     MmaArgs args;

@@ -446,7 +446,16 @@ __device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int
 //
 // EPI: the fused bias/activation epilogue is compiled in (the plain GEMM
 // kernels carry none of its code).
-template <int BN, int CG, bool GROUPED, bool EPI>
+//
+// I8ACC: the int8 path's exact accumulation on chip.  A unit is a whole
+// tile; its K range is cut into slices of args.slice_kb blocks (at most 1024
+// products of int8 values, so each slice's fp32 accumulator holds exact
+// integers), each slice accumulated from zero in one of the two TMEM
+// buffers, and the epilogue adds every slice as int32 to running sums kept
+// in a third TMEM region.  The split-K path writes each slice to memory and
+// adds them in a second kernel instead; the integer sums, their one rounding
+// and everything after are the same.
+template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -456,8 +465,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     constexpr int STAGE = stage_bytes(BN, CG);
     constexpr int A_BYTES = BM * BK * 2;
     constexpr int S = mma_stages(BN, CG);
-    constexpr int TCOLS = tmem_cols(BN);
-    constexpr int ACC_STRIDE = TCOLS / 2;          // TMEM columns between the two accumulators
+    constexpr int TCOLS = I8ACC ? 512 : tmem_cols(BN);
+    constexpr int ACC_STRIDE = I8ACC ? BN : TCOLS / 2;   // TMEM columns between the two accumulators
+    constexpr uint32_t RUN_COL = 2 * BN;           // I8ACC: the running int32 sums
+    static_assert(!I8ACC || (EPI && !GROUPED && 3 * BN <= 512), "on-chip slices: two accumulators and the sums");
     constexpr int CHUNKS = BN / 32;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
     static_assert(BNL % 64 == 0 && BN <= 256, "each CTA's B share must be whole 64-column boxes");
@@ -619,7 +630,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             uint32_t stage = 0, ph = 0, local = 0;
             bool ok = true;
             int hint = 0;
-            for (int u = cluster; ok && u < args.total_units; u += nclusters, ++local) {
+            for (int u = cluster; ok && u < args.total_units; u += nclusters) {
                 const MmaUnit w = mma_unit<GROUPED>(args, gt, u, hint);
                 int a_kmajor = args.a_kmajor, b_kmajor = args.b_kmajor;
                 uint32_t idesc = args.idesc;
@@ -638,46 +649,54 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 const uint64_t bd0 = b_kmajor ? smem_desc_sw128(s0 + A_BYTES, 16, 1024)
                                               : smem_desc_sw128(s0 + A_BYTES, 8192, 1024);
                 const uint64_t astep = a_kmajor ? 2u : 128u, bstep = b_kmajor ? 2u : 128u;
-                const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
-                if (!wait_bar(smem_u32(&tempty_bar[acc]), aph ^ 1u, watch, W_TMEM_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
-                for (int kb = 0; kb < w.nkb; ++kb) {
-                    if (!wait_bar(smem_u32(&full_bar[stage]), ph, watch, W_FULL)) {
+                // Segments of the unit, each accumulated in its own TMEM buffer
+                // from zero: the whole K range, or (I8ACC) K slices of
+                // args.slice_kb blocks that the epilogue adds up on chip.
+                const int seg_kb = I8ACC ? args.slice_kb : w.nkb;
+                for (int k0 = 0; ok && k0 < w.nkb; k0 += seg_kb, ++local) {
+                    const int k1 = min(k0 + seg_kb, w.nkb);
+                    const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+                    if (!wait_bar(smem_u32(&tempty_bar[acc]), aph ^ 1u, watch, W_TMEM_EMPTY)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t soff = (uint64_t)(stage * (STAGE >> 4));
+                    const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+                    for (int kb = k0; kb < k1; ++kb) {
+                        if (!wait_bar(smem_u32(&full_bar[stage]), ph, watch, W_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t soff = (uint64_t)(stage * (STAGE >> 4));
 #pragma unroll
-                    for (int k = 0; k < BK / MMA_K; ++k) {
-                        const uint64_t ad = ad0 + soff + k * astep, bd = bd0 + soff + k * bstep;
-                        const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+                        for (int k = 0; k < BK / MMA_K; ++k) {
+                            const uint64_t ad = ad0 + soff + k * astep, bd = bd0 + soff + k * bstep;
+                            const uint32_t accum = (kb > k0 || k > 0) ? 1u : 0u;
+                            if (CG == 1)
+                                mma_f16_ss(d_tmem, ad, bd, idesc, accum);
+                            else
+                                mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
+                        }
                         if (CG == 1)
-                            mma_f16_ss(d_tmem, ad, bd, idesc, accum);
+                            mma_commit(smem_u32(&empty_bar[stage]));
                         else
-                            mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
+                            mma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
+                        if (++stage == (uint32_t)S) {
+                            stage = 0;
+                            ph ^= 1u;
+                        }
                     }
+                    if (!ok) break;
+                    // test hook: withhold the "accumulator ready" signal of
+                    // this CTA's first segment, so that the epilogue's bounded
+                    // wait expires
+                    if (args.debug_drop_tfull && local == 0) continue;
                     if (CG == 1)
-                        mma_commit(smem_u32(&empty_bar[stage]));
+                        mma_commit(smem_u32(&tfull_bar[acc]));
                     else
-                        mma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
-                    if (++stage == (uint32_t)S) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
+                        mma_commit_pair(smem_u32(&tfull_bar[acc]), (uint16_t)0x3);
                 }
-                if (!ok) break;
-                // test hook: withhold the "accumulator ready" signal of this
-                // CTA's first tile, so that the epilogue's bounded wait expires
-                if (args.debug_drop_tfull && local == 0) continue;
-                if (CG == 1)
-                    mma_commit(smem_u32(&tfull_bar[acc]));
-                else
-                    mma_commit_pair(smem_u32(&tfull_bar[acc]), (uint16_t)0x3);
             }
             if (!ok) {
                 if (CG == 1)
@@ -745,7 +764,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         };
         const uint32_t tempty_leader0 = CG == 2 ? mapa_shared(smem_u32(&tempty_bar[0]), 0) : 0u;
         const uint32_t tempty_leader1 = CG == 2 ? mapa_shared(smem_u32(&tempty_bar[1]), 0) : 0u;
-        for (int u = cluster; u < args.total_units; u += nclusters, ++local) {
+        for (int u = cluster; u < args.total_units; u += nclusters) {
             const Unit w = decode<GROUPED>(args, gt, u, hint);
             if constexpr (GROUPED) {
                 if (w.p != cur_p) {
@@ -765,61 +784,99 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     cur_p = w.p;
                 }
             }
-            const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
-            bool ok = wait_bar(smem_u32(&tfull_bar[acc]), aph, watch, W_TMEM_FULL);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * ACC_STRIDE;
-            const long long row = (long long)w.tm * (BM * CG) + row_in_tile;
-            // accumulator fully read: hand it back to the MMA warp (not after
-            // this CTA's last unit: nothing waits for it then, and the
-            // arrival would sit on the kernel's final critical path)
-            const bool more = u + nclusters < args.total_units;
-            auto release = [&]() {
-                if (!more) return;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (CG == 1)
-                        mbar_arrive(smem_u32(&tempty_bar[acc]));
-                    else
-                        mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
-                }
-            };
+            // segments of the unit (see the MMA warp): one, or the K slices
+            // that I8ACC adds up in TMEM
+            const int nseg = I8ACC ? (w.kb1 - w.kb0 + args.slice_kb - 1) / args.slice_kb : 1;
+            bool ok = true;
+            for (int sg = 0; sg < nseg; ++sg, ++local) {
+                const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+                ok = wait_bar(smem_u32(&tfull_bar[acc]), aph, watch, W_TMEM_FULL);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * ACC_STRIDE;
+                const long long row = (long long)w.tm * (BM * CG) + row_in_tile;
+                // accumulator fully read: hand it back to the MMA warp (not after
+                // this CTA's last segment: nothing waits for it then, and the
+                // arrival would sit on the kernel's final critical path)
+                const bool more = sg + 1 < nseg || u + nclusters < args.total_units;
+                auto release = [&]() {
+                    if (!more) return;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (CG == 1)
+                            mbar_arrive(smem_u32(&tempty_bar[acc]));
+                        else
+                            mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+                    }
+                };
 
-            if (w.S == 1) {
+                if constexpr (I8ACC) {
+                    // This segment's fp32 accumulator holds exact integers (a
+                    // K slice of at most 1024 int8 products); they are added as
+                    // int32 to the running sums in TMEM columns RUN_COL.. of the
+                    // same lanes, and after the last slice the exact sum is
+                    // rounded once to fp32 and goes through the epilogue.
+                    const uint32_t raddr = tmem_base + ((uint32_t)(warp * 32) << 16) + RUN_COL;
+                    const bool first = sg == 0, last = sg + 1 == nseg;
 #pragma unroll 1
-                for (int c = 0; c < CHUNKS; ++c) {
-                    uint32_t r[32];
-                    __syncwarp();
-                    tmem_ld_32x32b_x32(taddr + c * 32, r);
-                    tmem_ld_wait();
-                    if (c == CHUNKS - 1) release();
-                    float v[32];
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        uint32_t r[32], q[32];
+                        __syncwarp();
+                        tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        if (!first) tmem_ld_32x32b_x32(raddr + c * 32, q);
+                        tmem_ld_wait();
+                        if (c == CHUNKS - 1) release();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    emit(w.b, row, (long long)w.tn * BN + c * 32, v);
-                }
-            } else {
-                // K slice: the raw fp32 partial tile goes to its workspace
-                // slot (row-major, (BM * CG) x BN per unit); the reduction
-                // kernel sums the slices in slice order afterwards
-                const long long wrow0 =
-                    (long long)(w.ufirst + w.s - args.split_base) * (BM * CG) + (int)rank * BM + warp * 32;
+                        for (int j = 0; j < 32; ++j) {
+                            const int x = __float2int_rn(__uint_as_float(r[j]));
+                            q[j] = (uint32_t)(first ? x : (int)q[j] + x);
+                        }
+                        if (!last) {
+                            tmem_st_32x32b_x32(raddr + c * 32, q);
+                        } else {
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __int2float_rn((int)q[j]);
+                            emit(w.b, row, (long long)w.tn * BN + c * 32, v);
+                        }
+                    }
+                    if (!last) tmem_st_wait();
+                } else if (w.S == 1) {
 #pragma unroll 1
-                for (int c = 0; c < CHUNKS; ++c) {
-                    uint32_t r[32];
-                    __syncwarp();
-                    tmem_ld_32x32b_x32(taddr + c * 32, r);
-                    tmem_ld_wait();
-                    if (c == CHUNKS - 1) release();
-                    float v[32];
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        uint32_t r[32];
+                        __syncwarp();
+                        tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        tmem_ld_wait();
+                        if (c == CHUNKS - 1) release();
+                        float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    store_tma<EBUFS>(&tmW, false, TC_F32, staging(STG_TMA), lane, 0, wrow0, c * 32, v);
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        emit(w.b, row, (long long)w.tn * BN + c * 32, v);
+                    }
+                } else {
+                    // K slice: the raw fp32 partial tile goes to its workspace
+                    // slot (row-major, (BM * CG) x BN per unit); the reduction
+                    // kernel sums the slices in slice order afterwards
+                    const long long wrow0 =
+                        (long long)(w.ufirst + w.s - args.split_base) * (BM * CG) + (int)rank * BM + warp * 32;
+#pragma unroll 1
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        uint32_t r[32];
+                        __syncwarp();
+                        tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        tmem_ld_wait();
+                        if (c == CHUNKS - 1) release();
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        store_tma<EBUFS>(&tmW, false, TC_F32, staging(STG_TMA), lane, 0, wrow0, c * 32, v);
+                    }
                 }
             }
+            if (!ok) break;
         }
         // every TMA store has read its shared-memory source before the CTA
         // releases it (the global writes complete with the kernel)
@@ -840,7 +897,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
 }
 
-template <int BN, int CG, bool GROUPED = false, bool EPI = false>
+template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false>
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
     constexpr int smem = mma_smem_bytes(BN, CG);
@@ -850,16 +907,16 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (CG == 2) {
-            e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
         configured[dev] = true;
     }
     if (CG == 1) {
-        mma_kernel<BN, CG, GROUPED, EPI><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+        mma_kernel<BN, CG, GROUPED, EPI, I8ACC><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -874,7 +931,7 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG, GROUPED, EPI>, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
 }
 
 template <int BN>
@@ -1045,6 +1102,10 @@ cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st)
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
     const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE || L.args.col_scale != nullptr;
+    if (L.i8acc) {
+        if (L.bn != 128 || L.args.slice_kb < 1 || L.args.col_scale == nullptr) return cudaErrorInvalidValue;
+        return L.cg == 2 ? launch_kernel<128, 2, false, true, true>(L, st) : launch_kernel<128, 1, false, true, true>(L, st);
+    }
     if (L.cg == 2) {
         switch (L.bn) {
         case 128: return epi ? launch_kernel<128, 2, false, true>(L, st) : launch_kernel<128, 2>(L, st);

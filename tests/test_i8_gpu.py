@@ -47,7 +47,52 @@ def test_i8_exact(ctx, ta, tb, K):
     out = run(ctx, p, torch.ones(260))
     _, _, ACC = oracle.gemm_i8_dequant(p, torch.ones(260))
     assert np.array_equal(out.numpy(), ACC.astype(np.float32)), ctx.last_kernel
-    assert ctx.last_kernel.startswith("i8_dequant_tcgen05_") and ctx.last_kernel.endswith(f"_i8s{(K + 1023) // 1024}")
+    assert ctx.last_kernel.startswith("i8_dequant_tcgen05_") and ctx.last_kernel.endswith(f"_i8acc_s{(K + 1023) // 1024}")
+
+
+@pytest.fixture
+def force(monkeypatch):
+    def set_(spec):
+        if spec:
+            monkeypatch.setenv("TC_FORCE_VARIANT", spec)
+        else:
+            monkeypatch.delenv("TC_FORCE_VARIANT", raising=False)
+    return set_
+
+
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("shape", [(300, 260, 1000), (300, 260, 1024), (700, 390, 1025), (1100, 260, 3000),
+                                   (2048, 2048, 2100)])
+def test_i8_on_chip_equals_memory_slices(ctx, force, ta, tb, shape):
+    """K slices summed as int32 in TMEM give the same bits as slices written
+    to memory and added by the reduction kernel: the same exact integer,
+    rounded once, then the same scale and alpha/beta.  Shapes span one slice,
+    a slice boundary, ragged last slices, both CTA shapes (the small ones run
+    128x128 tiles, the 2048^2 one CTA pairs) and ragged M, N."""
+    M, N, K = shape
+    p = synthetic.i8_problem(M, N, K, transpose_a=ta, transpose_b=tb, seed=M + K)
+    p.alpha, p.beta = 0.75, -0.5
+    p.C = (torch.randn(M, N, generator=torch.Generator().manual_seed(K))).float()
+    scale = torch.rand(N, generator=torch.Generator().manual_seed(N)) + 0.5
+    force("i8acc=0")
+    ref = run(ctx, p, scale)
+    k_mem = ctx.last_kernel
+    force("")
+    got = run(ctx, p, scale)
+    assert "_i8acc_" in ctx.last_kernel and "_i8acc_" not in k_mem, (ctx.last_kernel, k_mem)
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), ctx.last_kernel
+
+
+def test_i8_on_chip_largest_sums(ctx):
+    """All -128 at K = 65536, the largest K summed on chip: every int32 sum is
+    2^30, exact."""
+    K = 65536
+    A = torch.full((300, K), -128, dtype=torch.int8)
+    B = torch.full((K, 136), -128, dtype=torch.int8)
+    p = synthetic.Problem(300, 136, K, "i8", "f32", False, False, 1.0, 0.0, A, B, torch.zeros(300, 136))
+    out = run(ctx, p, torch.ones(136))
+    assert "_i8acc_" in ctx.last_kernel, ctx.last_kernel
+    assert (out == 2.0 ** 30).all()
 
 
 def test_i8_full_range_at_the_k_limit(ctx):
