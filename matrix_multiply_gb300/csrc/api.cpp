@@ -168,7 +168,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // grouped=0 (a grouped call enqueues its problems one by one) chunk=0 (an
 // MN-major operand is read 64 columns per copy instead of one chunked copy)
 // i8acc=0 (int8: K slices through memory and the reduction kernel, not
-// summed on chip).
+// summed on chip) shorta=0 (a one-CTA tile copies all 128 rows of A even
+// when A has fewer).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -178,6 +179,7 @@ struct Force {
     int grouped = 1;
     int debug_drop = 0, debug_timeout_ms = 0;
     int no_chunk = 0;
+    int no_short_a = 0;
     int i8acc = -1;
 };
 
@@ -212,6 +214,7 @@ Force read_force()
         else if (k == "debug_drop") f.debug_drop = std::atoi(v.c_str());
         else if (k == "debug_timeout_ms") f.debug_timeout_ms = std::atoi(v.c_str());
         else if (k == "chunk") f.no_chunk = std::atoi(v.c_str()) == 0;
+        else if (k == "shorta") f.no_short_a = std::atoi(v.c_str()) == 0;
         else if (k == "i8acc") f.i8acc = std::atoi(v.c_str());
     }
     return f;
@@ -566,7 +569,12 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     const bool chunk_ok = !read_force().no_chunk;
     bool ok;
     if (a.a_kmajor) {
-        ok = encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->K, d->M, lda_use, a.a_3d, n.batch, sa, 64, BM);
+        // a one-CTA tile taller than A: copy only A's rows (rounded up to 8)
+        const uint32_t rows = (p.cg == 1 && d->M < BM && !read_force().no_short_a)
+                                  ? (uint32_t)round_up((size_t)d->M, 8)
+                                  : (uint32_t)BM;
+        a.a_short_bytes = (int)((BM - rows) * BK * 2);
+        ok = encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->K, d->M, lda_use, a.a_3d, n.batch, sa, 64, rows);
     } else {
         a.a_chunked = chunk_ok && !a.a_3d && encode_chunked(ctx, &L.tmA, d->a_dtype, Ause, d->M, d->K, lda_use, BM / 64);
         ok = a.a_chunked || encode_map(ctx, &L.tmA, d->a_dtype, Ause, d->M, d->K, lda_use, a.a_3d, n.batch, sa, 64, 64);

@@ -93,6 +93,11 @@ struct MmaArgs {
     int act;
     const float *col_scale;
     int slice_kb;          // on-chip int8 accumulation: K blocks per exact slice
+    // one-CTA tiles over fewer than BM rows of a K-major A: its copies carry
+    // only the rows that exist (rounded up to 8) and a stage this many fewer
+    // bytes; the tile's other rows hold stale data, which reaches only
+    // output rows beyond M (never stored)
+    int a_short_bytes;
 };
 
 struct MmaLaunch {

@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     }
                     const uint32_t fb = full0_lead + 8 * stage;
                     if (CG == 1)
-                        mbar_arrive_expect_tx(full0 + 8 * stage, STAGE);
+                        mbar_arrive_expect_tx(full0 + 8 * stage, STAGE - args.a_short_bytes);
                     else if (rank == 0)
                         mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE);
                     const uint32_t sa = s0 + stage * STAGE;

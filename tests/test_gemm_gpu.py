@@ -201,6 +201,25 @@ def test_single_buffer_epilogue_192(ctx, force, spec, c):
         parity.check(oracle.decode(out)[:, :384], R, T, c, what=f"{spec} ldc={ldc} {ctx.last_kernel}")
 
 
+@pytest.mark.parametrize("M", [1, 4, 7, 9, 100, 127])
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+@pytest.mark.parametrize("spec", ["", "cg=1 bn=128", "bn=128 split=4"])
+def test_short_a_copies_bitwise(ctx, force, M, ta, tb, spec):
+    """A one-CTA tile over fewer than 128 rows of a K-major A copies only the
+    rows that exist (rounded up to 8); the tile's other rows hold stale
+    shared memory and feed only output rows beyond M.  The result equals
+    that of full 128-row copies bit for bit."""
+    p = synthetic.make_problem(M, 700, 2100, "bf16", "f32", transpose_a=ta, transpose_b=tb, alpha=0.75, beta=0.5,
+                               seed=M + 95, dist="normal", c_fill="uniform")
+    force((spec + " shorta=0").strip())
+    ref = run_problem(ctx, p)
+    force(spec)
+    got = run_problem(ctx, p)
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), ctx.last_kernel
+    R, T = oracle.gemm(p)
+    parity.check(oracle.decode(got), R, T, "f32", what=f"{spec} M={M} {ctx.last_kernel}")
+
+
 def test_rank_one_exact(ctx):
     for dt in ("f16", "bf16"):
         p = synthetic.make_problem(190, 170, 1, dt, "f32", seed=43, dist="normal")
