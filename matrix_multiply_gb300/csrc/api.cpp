@@ -232,6 +232,11 @@ double tile_rate(int cg, int bn)
     return bn == 256 ? 1.0 : bn == 192 ? 0.87 : bn == 128 ? 0.63 : 0.45;
 }
 
+// Modelled fixed cost of a split-K reduction (its launch, the wait for the
+// GEMM grid, one pass over the partial tiles), in the schedule's time unit:
+// one K block of one 256-wide tile column at tile rate 1, ~1 ns on GB300.
+constexpr double SPLIT_FIXED = 4500.0;
+
 // Persistent schedule of `tiles` output tiles on num_sms CTAs: whole waves
 // of tiles, then the partial last wave.  When the last wave leaves at least
 // half of the SMs idle, its tiles are cut into K slices (reduced in fixed
@@ -298,7 +303,22 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     const int64_t tiles128 = cdiv(d->M, BM) * cdiv(d->N, 128) * n.batch;
     int bn = 0, cg = 1;
     Sched sc{};
-    if ((f.split == 0 && f.cg != 2 && tiles128 * 2 <= num_sms && num_kb >= 16) || f.split > 0) {
+    bool split_k = (f.split == 0 && f.cg != 2 && tiles128 * 2 <= num_sms && num_kb >= 16) || f.split > 0;
+    if (split_k && f.split == 0 && f.bn == 0) {
+        // 64-wide whole-K tiles instead, when they fill at least half the SMs
+        // and the split's reduction would cost more than their lower rate
+        // (e.g. fp16 1024^3 on GB300: 13.8 us against 16.7 us split in two)
+        const int64_t tiles64 = cdiv(d->M, BM) * cdiv(d->N, 64) * n.batch;
+        const int64_t split = std::min<int64_t>(std::max<int64_t>(num_sms / tiles128, 1), num_kb / 4);
+        const double t_split = (double)cdiv(num_kb, split) * 128.0 / tile_rate(1, 128) + SPLIT_FIXED;
+        const double t_64 = (double)cdiv(tiles64, num_sms) * (double)num_kb * 64.0 / tile_rate(1, 64);
+        if (tiles64 * 2 >= num_sms && t_64 < t_split) {
+            split_k = false;
+            bn = 64;
+            sc = schedule(tiles64, num_kb, num_sms, 1, 64, f.tail);
+        }
+    }
+    if (split_k) {
         // split-K: too few output tiles to occupy the SMs and a long K loop
         bn = f.bn ? f.bn : 128;
         const int64_t tiles = cdiv(d->M, BM) * cdiv(d->N, bn) * n.batch;
@@ -306,6 +326,8 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
                                 : (int)std::min<int64_t>(std::max<int64_t>(num_sms / tiles, 1), num_kb / 4);
         split = (int)std::min<int64_t>(std::max(split, 1), num_kb);
         sc = {tiles, tiles, split, 1, 0.0};
+    } else if (bn == 64) {
+        cg = 1;
     } else {
         // the kernel shape (CTAs per tile, tile width) with the least modelled time
         static const int shapes[][2] = {{2, 256}, {1, 256}, {1, 192}, {2, 128}, {1, 128}, {1, 64}};

@@ -160,6 +160,15 @@ def test_plan_split_k_for_tall_k():
     assert 2 <= s <= 152 // 4
 
 
+def test_plan_small_split_gives_way_to_64_wide_tiles():
+    # 1024^2 with a short K: 128 whole-K 128x64 tiles beat a 2-way split and
+    # its reduction; a long K keeps the split, and too few 64-wide tiles
+    # (the skinny shapes) keep it too
+    assert plan(1024, 1024, 1024, "f16", "f16") == "tcgen05_nn_f16_f16_128x64"
+    assert plan(1024, 1024, 8192, "f16", "f16") == "tcgen05_nn_f16_f16_128x128_splitk_s2"
+    assert plan(1, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_splitk")
+
+
 def test_plan_tail_split():
     # 256 tiles of 256x256 on 76 CTA pairs: 3 whole waves, the last 28 tiles in 2 K slices
     assert plan(4096, 4096, 4096, "bf16", "bf16") == "tcgen05_nn_bf16_bf16_256x256_pair_tail28x2"
