@@ -102,11 +102,16 @@ typedef struct {
 typedef struct tc_ctx tc_ctx;
 typedef struct tc_stream tc_stream;
 
-/* Create a context on CUDA device `device` (it becomes current for the
+/* tensorcore gemm.md, "Async, batched, and streams": every call there takes
+ * a `ctx` as its first argument; the page does not print how one is made,
+ * so the constructor and destructor are this library's own.
+ * Create a context on CUDA device `device` (it becomes current for the
  * calling thread).  The context owns the TMA descriptor encoder, a default
  * stream and a device status word.  Returns TC_ERR_CUDA when no usable
  * device exists.  *out is NULL on error. */
 tc_status_t tc_ctx_create(tc_ctx **out, int device);
+/* Waits for the default stream, then frees everything the context owns
+ * (never caller memory).  NULL is a no-op. */
 void tc_ctx_destroy(tc_ctx *ctx);
 
 /* tensorcore gemm.md, "Async, batched, and streams": a stream on which
@@ -124,10 +129,11 @@ tc_status_t tc_stream_sync(tc_stream *s);
 void *tc_stream_handle(tc_stream *s);
 void tc_stream_destroy(tc_stream *s);
 
-/* Synchronous GEMM on the context's default stream (returns when C is
- * written). */
+/* tensorcore gemm.md, "Surface": the synchronous GEMM, on the context's
+ * default stream (returns when C is written). */
 tc_status_t tc_gemm(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B, void *C);
-/* Enqueue the GEMM on stream s and return. */
+/* tensorcore gemm.md, "Async, batched, and streams": enqueue the GEMM on
+ * stream s and return; the work is complete only after tc_stream_sync(s). */
 tc_status_t tc_gemm_async(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B,
                           void *C, tc_stream *s);
 /* Same-shape batch: matrix i is at A + i*stride_a (elements), etc.  One
@@ -136,9 +142,13 @@ tc_status_t tc_gemm_batched(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const v
                             const void *B, void *C);
 tc_status_t tc_gemm_batched_async(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A,
                                   const void *B, void *C, tc_stream *s);
-/* n independent problems (each with its own descriptor and pointers),
- * enqueued on s.  All descriptors are validated before anything is
- * enqueued. */
+/* This library's addition for the ragged batch (no page prints a grouped
+ * call; the tessl architecture.md "GEMM Pipeline & Kernel Selection" chart
+ * routes ragged edges to bounds-checked slices): n independent problems,
+ * each with its own descriptor and device pointers, enqueued on s.  All
+ * descriptors are validated before anything is enqueued; f16/bf16 problems
+ * share one persistent tensor-core launch per 64 problems, f32 problems run
+ * one by one on the exact path. */
 tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d,
                                   const void *const *A, const void *const *B, void *const *C,
                                   tc_stream *s);
@@ -219,14 +229,18 @@ tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
  * (TC_ERR_ALIGN_UNSUPPORTED otherwise: repacking would need scratch sized
  * by the operands).  The call is asynchronous: it clears the array's status
  * word with cudaMemsetAsync and launches on cuda_stream; a device-side wait
- * timeout is not reported by this call.
+ * timeout is not reported by this call, and when one happens the contents of
+ * C are undefined (the reduction kernel then skips C: it may be partly
+ * written by the slices of a single-slice call, or keep its old values).
  *
  * Every call, on any stream, shares the one array and it keeps the last
  * call's contents: calls whose kernels overlap on the GPU race and corrupt
  * each other's results; serialise them (one stream, or events).  The first
  * call on each device performs set-up (it looks up the array's device
  * address and the TMA encoder and sets the kernel's shared-memory limit);
- * make that first call before any stream capture. */
+ * make that first call before any stream capture.  That set-up is kept for
+ * the life of the process: after cudaDeviceReset on a device, this entry
+ * point must not be called again on that device. */
 tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const void *B, void *C, int split,
                                    void *cuda_stream);
 
@@ -246,7 +260,10 @@ tc_status_t tc_gemm_plan(const tc_gemm_desc *d, const void *A, const void *B, co
 /* The variant and configuration of the last kernel this context launched
  * (tensorcore gemm.md "Fallback ladder": which path served the call). */
 const char *tc_last_kernel(tc_ctx *ctx);
-/* Number of kernels this context has launched (0 after any refused call). */
+/* This library's test hook for the tessl architecture.md rule "nothing is
+ * launched on error" (section "The Kernel Library and the nn Boundary"):
+ * the number of kernels this context has launched; a refused call leaves it
+ * unchanged. */
 uint64_t tc_launch_count(tc_ctx *ctx);
 const char *tc_status_string(tc_status_t st);
 

@@ -18,6 +18,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <memory>
 #include <mutex>
 #include <string>
@@ -648,6 +649,9 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         r.act = a.act;
         r.col_scale = col_scale;
         r.int_sum = col_scale != nullptr;
+        // (r.status stays null: the stream's status word is mapped host
+        // memory, and tc_stream_sync reports an expired wait, after which C
+        // is undefined)
         if ((e = launch_reduce(r, s->st)) != cudaSuccess) return TC_ERR_CUDA;
         ++launches;
     }
@@ -1447,16 +1451,27 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
 
     NoallocScratch scratch;
     if (noalloc_scratch(&scratch) != cudaSuccess) return TC_ERR_CUDA;
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 encoder = nullptr;
-    std::call_once(once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            encoder = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
+    // the TMA descriptor encoder, looked up until a lookup succeeds (a
+    // failed first lookup, e.g. before any device was usable, is retried)
+    static std::mutex enc_mu;
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> enc_fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 encoder = enc_fn.load(std::memory_order_acquire);
+    if (!encoder) {
+        std::lock_guard<std::mutex> g(enc_mu);
+        encoder = enc_fn.load(std::memory_order_acquire);
+        if (!encoder) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                    cudaSuccess &&
+                q == cudaDriverEntryPointSuccess && fn) {
+                encoder = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+                enc_fn.store(encoder, std::memory_order_release);
+            } else {
+                cudaGetLastError();
+            }
+        }
+    }
     if (!encoder) return TC_ERR_CUDA;
     tc_ctx enc;                 // carries only the encoder for encode_map; owns nothing
     enc.encode = encoder;
@@ -1535,6 +1550,7 @@ tc_status_t tc_gemm_splitk_noalloc(const tc_gemm_desc *d, const void *A, const v
         r.stride_c = 0;
         r.c_dtype = d->c_dtype;
         r.c_vec_ok = a.c_vec_ok;   // 16-byte vectors of 8 elements (two for fp32)
+        r.status = scratch.status;
         if (launch_reduce(r, stream) != cudaSuccess) return TC_ERR_CUDA;
     }
     return TC_OK;

@@ -14,6 +14,8 @@
 // leading dimension and ragged edges go through bounds-checked loads.
 #include "internal.h"
 
+#include <atomic>
+
 namespace tc {
 namespace {
 
@@ -240,12 +242,15 @@ __global__ void __launch_bounds__(256) ffma_panel_kernel(const FfmaArgs a)
 cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st)
 {
     if (tile == FFMA_PANEL) {
-        static bool configured = false;
-        if (!configured) {
+        static std::atomic<bool> configured[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!configured[dev].load(std::memory_order_acquire)) {
             cudaError_t e =
                 cudaFuncSetAttribute(ffma_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PANEL_SMEM);
             if (e != cudaSuccess) return e;
-            configured = true;
+            configured[dev].store(true, std::memory_order_release);
         }
         const int zb = a.batch < 65535 ? a.batch : 65535;
         const long long ty = ((long long)a.M + PBM - 1) / PBM;

@@ -157,6 +157,10 @@ struct ReduceArgs {
     int act;
     const float *col_scale;
     int int_sum;           // the slices are integers: add them as 64-bit integers
+    // a status word in device memory (or null): nonzero when one of the
+    // GEMM's bounded waits expired, so some partial tiles were never
+    // written; the reduction then leaves C alone
+    const unsigned *status;
 };
 // One CTA of bn threads per 8 (or, for small reductions, 4) rows of a tile,
 // 8 (4) columns per thread; c_vec_ok allows 16-byte accesses to C.

@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -901,11 +902,14 @@ template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = f
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
     constexpr int smem = mma_smem_bytes(BN, CG);
-    static bool configured[64] = {};
+    // per device: the kernel's shared-memory limit is raised once (callers
+    // of the context-free entry point may race here from several threads;
+    // setting the attribute twice is harmless)
+    static std::atomic<bool> configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e =
             cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -913,7 +917,7 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
             e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     if (CG == 1) {
         mma_kernel<BN, CG, GROUPED, EPI, I8ACC><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
@@ -978,6 +982,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
 {
     static_assert(COLS == 4 || COLS == 8, "whole 16-byte loads");
     griddep_wait();
+    // a GEMM wait that expired left partial tiles unwritten: do not sum them
+    if (r.status && *reinterpret_cast<const volatile unsigned *>(r.status) != 0u) return;
     const int groups = r.bn / COLS;                    // threads per row
     const int ctas_per_tile = r.rows_per_tile / COLS;  // COLS rows per CTA
     const int t = blockIdx.x / ctas_per_tile;
