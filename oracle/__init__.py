@@ -15,6 +15,11 @@ activation(alpha * A@B + beta * C_prev + bias), bias per column, the
 GeluTanh activation) is applied here in fp64 on top of the same R, by
 ``gemm_epilogue`` / ``gemm_epilogue_points``.
 
+The int8-weight product (Foundry metal.md, "Custom Compute Kernels":
+fm_sgemm_q8, Out = X @ (W_q8 * scale[n])^T) is the same k-sum over mixed
+operand types, scaled per output column: ``gemm_q8_weight`` /
+``gemm_q8_weight_points``.
+
 Every function here is pinned by ``tests/test_oracle.py`` against things
 other than itself: exact rational brute force, numpy's float64 matmul on
 operands decoded by PyTorch, the worked 2x2 input of the Foundry metal.md
@@ -243,3 +248,46 @@ def gemm_i8_dequant(p, scale, row0: int = 0, row1: int | None = None, lib=None):
         R = R + float(np.float32(p.beta)) * decode(p.C, lib=lib)[row0:row1, : p.N]
     return R, T, ACC
 
+
+
+# ------------------------------------------------- int8-weight (Q8) product
+# Foundry metal.md, "Custom Compute Kernels": fm_sgemm_q8(X[M,K], W_q8[N,K],
+# scales[N]) -- the activations times the transposed int8 weight, each
+# weight row n dequantised by its own scale: Out[m, n] = sum_k X[m, k] *
+# (W_q8[n, k] * scales[n]).  The tensorcore gemm.md "Kernel variants" table
+# runs the same product as an M <= 4 GEMV with fp16 output.  With this
+# library's alpha/beta: Out = alpha * (acc[m, n] * scale[n]) + beta * C_old,
+# acc = sum_k X[m, k] * W[n, k] (X half precision, W int8: every product is
+# exact, and so is the fp64 sum for the sizes tested).  The tolerance scale
+# is that of the GEMM over the dequantised weight: T = |scale[n]| * sum_k
+# |X[m, k] * W[n, k]|.
+
+def gemm_q8_weight(p, scale, row0: int = 0, row1: int | None = None, lib=None):
+    """Rows [row0,row1) of alpha * acc * scale[None, :] + beta * C_old, for
+    p.A = X (f16/bf16, stored [M,K]) and p.B = W (int8, stored [N,K],
+    transpose_b), with T and the product sum: (R, T, ACC)."""
+    import copy
+    q = copy.copy(p)
+    q.alpha, q.beta = 1.0, 0.0
+    ACC, T0 = gemm(q, row0, row1, lib=lib)
+    sc = decode(scale, lib=lib).reshape(1, -1)[:, : p.N]
+    R = float(np.float32(p.alpha)) * (ACC * sc)
+    if p.beta != 0.0:
+        row1 = p.M if row1 is None else row1
+        R = R + float(np.float32(p.beta)) * decode(p.C, lib=lib)[row0:row1, : p.N]
+    return R, T0 * np.abs(sc), ACC
+
+
+def gemm_q8_weight_points(p, scale, rows, cols, lib=None):
+    """gemm_q8_weight at the listed (row, col) positions (1-D arrays)."""
+    import copy
+    q = copy.copy(p)
+    q.alpha, q.beta = 1.0, 0.0
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    ACC, T0 = gemm_points(q, rows, cols, lib=lib)
+    sc = decode(scale, lib=lib).reshape(-1)[cols]
+    R = float(np.float32(p.alpha)) * (ACC * sc)
+    if p.beta != 0.0:
+        R = R + float(np.float32(p.beta)) * decode(p.C, lib=lib)[rows, cols]
+    return R, T0 * np.abs(sc), ACC

@@ -205,3 +205,33 @@ def i8_dequant_4096():
     scale = torch.rand(4096, generator=torch.Generator("cpu").manual_seed(9)) * 1e-3
     return p, scale
 
+
+
+# The int8-weight product (Foundry metal.md, "Custom Compute Kernels":
+# fm_sgemm_q8(X[M,K], W_q8[N,K], scales[N]); tensorcore gemm.md "Kernel
+# variants": the M <= 4 GEMV over Q8 weights with fp16 output), at the
+# decode shapes above.  The pages give no distributions: the activations are
+# normal(0,1) rounded to the half type, the weights uniform over the full
+# int8 range, and the per-row scales uniform in [0.5e-3, 1.5e-3) (the scale
+# of a row of normal(0,0.02) weights quantised to 127 levels).
+
+def q8_weight_problem(M, N, K, x_dtype="f16", c_dtype="f16", *, alpha=1.0, beta=0.0, seed=10,
+                      c_fill="zero", x_dist="normal", ldx=0, ldw=0):
+    """X [M,K] (x_dtype), W int8 stored [N,K] (transpose_b), then the N
+    scales, then C when pre-filled, drawn in that order from one fresh
+    generator.  Returns (problem, scale); problem.A = X, problem.B = W."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    X = _draw(g, (M, max(K, ldx)), x_dist, 4.0 if x_dist == "int" else 1.0).to(DTYPES[x_dtype])
+    W = torch.randint(-128, 128, (N, max(K, ldw)), generator=g).to(torch.int8)
+    scale = torch.rand(N, generator=g) * 1e-3 + 0.5e-3
+    if c_fill == "zero":
+        C = torch.zeros(M, N, dtype=DTYPES[c_dtype])
+    else:
+        C = _draw(g, (M, N), "uniform", 1.0).to(DTYPES[c_dtype])
+    p = Problem(M, N, K, x_dtype, c_dtype, False, True, alpha, beta, X, W, C)
+    return p, scale
+
+
+def q8_decode(M: int, N: int, K: int, seed: int = 10):
+    """fp16 x[M, K] @ (W_q8[N, K] * scale[n])^T, fp16 out (the decode shapes)."""
+    return q8_weight_problem(M, N, K, "f16", "f16", seed=seed)

@@ -462,3 +462,115 @@ def test_i8_dequant_closed_form():
     want = 0.5 * B.double().numpy() * scale.double().numpy()[None, :] + 2.0 * Cold.double().numpy()
     assert np.array_equal(ACC, B.double().numpy())
     assert np.allclose(R, want, rtol=1e-15, atol=0)
+
+
+# ------------------------------------------------- int8-weight (Q8) product
+# Foundry metal.md, "Custom Compute Kernels": fm_sgemm_q8(X[M,K], W_q8[N,K],
+# scales[N]), Out = X @ (W_q8 * scale[n])^T, with alpha/beta on top.
+
+def _q8_tiny(M, N, K, seed, x_dtype="f16", alpha=1.0, beta=0.0):
+    g = torch.Generator().manual_seed(seed)
+    X = torch.randn(M, K, generator=g).to(synthetic.DTYPES[x_dtype])
+    W = torch.randint(-128, 128, (N, K), generator=g).to(torch.int8)
+    scale = (torch.rand(N, generator=g) * 2 - 1) * 1e-2
+    C = (torch.rand(M, N, generator=g) * 2 - 1)
+    return synthetic.Problem(M, N, K, x_dtype, "f32", False, True, alpha, beta, X, W, C), scale
+
+
+def q8_pins_fail(fn):
+    """Failing pins of an int8-weight product function fn(p, scale) ->
+    (R, T, ACC) (the oracle's own, or planted-mistake copies)."""
+    fails = []
+    # exact rational brute force: alpha * scale[n] * sum_k x w + beta * c
+    for x_dtype in ("f16", "bf16"):
+        p, scale = _q8_tiny(3, 4, 5, seed=21, x_dtype=x_dtype, alpha=0.75, beta=-0.5)
+        X = [[Fraction(float(v)) for v in row] for row in p.A.double().tolist()]
+        W = [[int(v) for v in row] for row in p.B.tolist()]
+        s = [Fraction(float(v)) for v in scale.tolist()]
+        Cf = [[Fraction(float(v)) for v in row] for row in p.C.double().tolist()]
+        a, b = Fraction(float(np.float32(0.75))), Fraction(float(np.float32(-0.5)))
+        exact = np.array([[float(a * s[j] * sum(X[i][k] * W[j][k] for k in range(5)) + b * Cf[i][j])
+                           for j in range(4)] for i in range(3)])
+        t_exact = np.array([[float(abs(s[j]) * sum(abs(X[i][k] * W[j][k]) for k in range(5)))
+                             for j in range(4)] for i in range(3)])
+        R, T, _ = fn(p, scale)
+        if not (np.allclose(R, exact, rtol=1e-14, atol=1e-300) and np.allclose(T, t_exact, rtol=1e-14, atol=0)):
+            fails.append(f"brute force {x_dtype}")
+    # identity weight (N = K): Out = X * scale[n] column by column, exactly
+    N = 6
+    g = torch.Generator().manual_seed(22)
+    X = torch.randn(2, N, generator=g).to(torch.float16)
+    scale = torch.tensor([0.5, -2.0, 1e-3, 0.25, 7.0, 1.0])
+    p = synthetic.Problem(2, N, N, "f16", "f32", False, True, 1.0, 0.0, X, torch.eye(N, dtype=torch.int8),
+                          torch.zeros(2, N))
+    R, _, _ = fn(p, scale)
+    if not np.array_equal(R, X.double().numpy() * scale.double().numpy()[None, :]):
+        fails.append("identity weight")
+    # all-ones activations (M != N): Out[m, n] = scale[n] * sum_k W[n, k] on every row
+    W = torch.tensor([[1, -2, 3], [127, -128, 0], [5, 5, 5], [-1, 0, 1], [9, -8, 7]], dtype=torch.int8)
+    scale = torch.tensor([0.5, 2.0, -1.0, 4.0, 0.125])
+    p = synthetic.Problem(2, 5, 3, "bf16", "f32", False, True, 1.0, 0.0, torch.ones(2, 3, dtype=torch.bfloat16),
+                          W, torch.zeros(2, 5))
+    R, _, _ = fn(p, scale)
+    want = (W.double().sum(1) * scale.double()).numpy()
+    if not (np.array_equal(R[0], want) and np.array_equal(R[1], want)):
+        fails.append("all-ones activations")
+    # integer activations, scale 1: the product sum is an exact integer
+    g = torch.Generator().manual_seed(23)
+    X = torch.randint(-4, 5, (3, 40), generator=g).to(torch.float16)
+    W = torch.randint(-128, 128, (7, 40), generator=g).to(torch.int8)
+    p = synthetic.Problem(3, 7, 40, "f16", "f32", False, True, 1.0, 0.0, X, W, torch.zeros(3, 7))
+    R, _, ACC = fn(p, torch.ones(7))
+    want = X.long() @ W.long().T
+    if not (np.array_equal(R, want.double().numpy()) and np.array_equal(ACC, want.double().numpy())):
+        fails.append("integer activations")
+    return fails
+
+
+def test_q8_pins_pass_on_oracle():
+    assert q8_pins_fail(oracle.gemm_q8_weight) == []
+
+
+def _q8_scale_by_row(p, scale):
+    R, T, ACC = oracle.gemm_q8_weight(p, torch.ones(p.N))
+    sc = np.resize(scale.double().numpy(), p.M)[:, None]
+    return R * sc, T * np.abs(sc), ACC
+
+
+def _q8_weight_not_transposed(p, scale):
+    # the same bytes read as a weight stored [K,N]
+    import copy
+    q = copy.copy(p)
+    q.transpose_b = False
+    q.B = p.B.contiguous().reshape(p.K, p.N)
+    return oracle.gemm_q8_weight(q, scale)
+
+
+def _q8_t_unscaled(p, scale):
+    R, T, ACC = oracle.gemm_q8_weight(p, scale)
+    return R, T / np.abs(np.where(scale.double().numpy() == 0, 1.0, scale.double().numpy()))[None, : p.N], ACC
+
+
+def _q8_scale_divides(p, scale):
+    return oracle.gemm_q8_weight(p, 1.0 / scale)
+
+
+Q8_MUTATIONS = {
+    "scale indexed by row": _q8_scale_by_row,
+    "weight read as stored [K,N]": _q8_weight_not_transposed,
+    "T without the scale": _q8_t_unscaled,
+    "scale divides": _q8_scale_divides,
+}
+
+
+@pytest.mark.parametrize("name", sorted(Q8_MUTATIONS))
+def test_planted_q8_mistake_is_caught(name):
+    assert q8_pins_fail(Q8_MUTATIONS[name]) != [], f"planted mistake {name!r} went unnoticed"
+
+
+def test_q8_points_match_rows():
+    p, scale = _q8_tiny(6, 9, 33, seed=24, alpha=0.5, beta=2.0)
+    R, T, ACC = oracle.gemm_q8_weight(p, scale)
+    ii, jj = np.meshgrid(np.arange(6), np.arange(9), indexing="ij")
+    Rp, Tp, Ap = oracle.gemm_q8_weight_points(p, scale, ii.ravel(), jj.ravel())
+    assert np.array_equal(Rp, R.ravel()) and np.array_equal(Tp, T.ravel()) and np.array_equal(Ap, ACC.ravel())
