@@ -262,9 +262,18 @@ def workload_registry():
     for (m, n, k) in synthetic.EPILOGUE_SHAPES:
         tag = f"{m}" if m == n == k else f"{m}x{n}x{k}"
         reg[f"bf16_bias_gelu_{tag}"] = (lambda s=(m, n, k): epilogue(s))
-    # the small-M decode shape (tensor cores, split-K when the tiles are few)
+    # the small-M decode shape (the skinny-product kernel)
     for (m, n, k) in synthetic.DECODE_SHAPES:
         reg[f"f16_decode_m{m}_{n}x{k}"] = (lambda s=(m, n, k): [synthetic.f16_decode(*s)])
+
+    # the same decode shapes over int8 weights with per-row scales (Foundry
+    # metal.md, "Custom Compute Kernels": fm_sgemm_q8 / fm_matvec_q8)
+    def q8(shape):
+        p, scale = synthetic.q8_decode(*shape)
+        p.q8_scale = scale
+        return [p]
+    for (m, n, k) in synthetic.DECODE_SHAPES:
+        reg[f"q8w_decode_m{m}_{n}x{k}"] = (lambda s=(m, n, k): q8(s))
 
     # fp32 at 4096^3: the exact path and the relaxed (bf16-split) path
     def relaxed():
@@ -294,9 +303,13 @@ def roofline(probs, seconds, sms):
     burst, _sustained, hbm, src = peaks()
     es = {"f16": 2, "bf16": 2, "f32": 4, "i8": 1}
     flops = sum(2.0 * p.M * p.N * p.K for p in probs)
-    nbytes = sum(p.M * p.K * es[p.ab_dtype] + p.K * p.N * es[p.ab_dtype] +
+    # each operand at its own element size (the int8-weight product mixes
+    # half-precision activations with one-byte weights), plus the per-column
+    # bias or scale vectors
+    nbytes = sum(p.M * p.K * p.A.element_size() + p.K * p.N * p.B.element_size() +
                  p.M * p.N * es[p.c_dtype] * (2 if p.beta != 0 else 1) +
-                 (p.N * es[p.c_dtype] if getattr(p, "bias", None) is not None else 0) for p in probs)
+                 (p.N * es[p.c_dtype] if getattr(p, "bias", None) is not None else 0) +
+                 (p.N * 4 if getattr(p, "q8_scale", None) is not None else 0) for p in probs)
     # fp32 operands: the exact path runs on the FFMA lanes; the relaxed path
     # on the bf16 tensor cores at three bf16 products per fp32 product
     relaxed = getattr(probs[0], "precision", None) == "relaxed"
@@ -319,6 +332,11 @@ def roofline(probs, seconds, sms):
             "flops_per_step": flops, "bytes_per_step": nbytes, "peak_source": f"{src}: {what}"}
 
 
+def torch_int8():
+    import torch
+    return torch.int8
+
+
 class Runner:
     """Device-resident operands of one workload and its launch."""
 
@@ -328,7 +346,8 @@ class Runner:
         self.B = [p.B.cuda() for p in probs]
         self.C = [p.C.cuda() for p in probs]
         self.d = [tg.make_desc(p.M, p.N, p.K, p.ab_dtype, p.c_dtype, transpose_a=p.transpose_a,
-                               transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta) for p in probs]
+                               transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta,
+                               b_dtype="i8" if p.B.dtype == torch_int8() else None) for p in probs]
         # a group's arguments are marshalled once; each step is one C call
         self.group = tg.GroupedGemm(self.d, self.A, self.B, self.C) if len(probs) > 1 else None
         # the fused-epilogue workloads carry a bias and an activation
@@ -337,10 +356,14 @@ class Runner:
         self.bias = p0.bias.cuda() if getattr(p0, "bias", None) is not None else None
         self.relaxed = getattr(p0, "precision", None) == "relaxed"
         self.col_scale = p0.col_scale.cuda() if getattr(p0, "col_scale", None) is not None else None
+        self.q8_scale = p0.q8_scale.cuda() if getattr(p0, "q8_scale", None) is not None else None
 
     def step(self):
         tg = self.tg
-        if self.col_scale is not None:
+        if self.q8_scale is not None:
+            tg.tc_gemm_q8_weight_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.q8_scale,
+                                       self.stream)
+        elif self.col_scale is not None:
             tg.tc_gemm_i8_dequant_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.col_scale,
                                         self.stream)
         elif self.relaxed:
@@ -435,7 +458,8 @@ def run_ours(args):
 
     # end to end through the host-buffer ABI call (copies inside the timed region)
     e2e = None
-    if len(probs) == 1 and runner.activation is None and not runner.relaxed and runner.col_scale is None:
+    if (len(probs) == 1 and runner.activation is None and not runner.relaxed and runner.col_scale is None
+            and runner.q8_scale is None):
         # (no host-buffer call carries the epilogue or the relaxed mode)
         p = probs[0]
         Ah, Bh, Ch = p.A.pin_memory(), p.B.pin_memory(), p.C.clone().pin_memory()

@@ -47,7 +47,8 @@
 extern "C" {
 #endif
 
-/* TC_I8 / TC_I32: operands and accumulator of tc_gemm_i8_dequant only. */
+/* TC_I8 / TC_I32: operands and accumulator of tc_gemm_i8_dequant; TC_I8
+ * also the weight type of tc_gemm_q8_weight. */
 typedef enum { TC_F16 = 1, TC_BF16 = 2, TC_F32 = 3, TC_I8 = 4, TC_I32 = 5 } tc_dtype_t;
 
 typedef enum {
@@ -65,7 +66,8 @@ typedef enum {
     TC_ERR_STRIDE = 11,            /* batched: negative stride */
     TC_ERR_VARIANT = 12,           /* a forced variant cannot serve this problem */
     TC_ERR_SCRATCH = 13,           /* tc_gemm_splitk_noalloc: more scratch than its static buffer holds */
-    TC_ERR_EPILOGUE = 14           /* fused epilogue: unknown activation, or f32 operands (see tc_gemm_epilogue) */
+    TC_ERR_EPILOGUE = 14,          /* fused epilogue: unknown activation, or f32 operands (see tc_gemm_epilogue) */
+    TC_ERR_LAYOUT = 15             /* transpose flags the call does not support (tc_gemm_q8_weight) */
 } tc_status_t;
 
 /* tensorcore gemm.md, "Surface": the GEMM descriptor, field for field. */
@@ -197,6 +199,35 @@ tc_status_t tc_gemm_i8_dequant(tc_ctx *ctx, const tc_gemm_desc *d, const float *
                                const void *B, void *C);
 tc_status_t tc_gemm_i8_dequant_async(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale,
                                      const void *A, const void *B, void *C, tc_stream *s);
+
+/* int8-weight product (Foundry metal.md, "Custom Compute Kernels":
+ * fm_sgemm_q8(X[M,K], W_q8[N,K], scales[N]) and its M = 1 form
+ * fm_matvec_q8; tensorcore gemm.md "Kernel variants": the M <= 4 GEMV over
+ * Q8 weights with fp16 output):
+ *   acc[m, n] = sum_k X[m, k] * W[n, k]          (fp32 accumulation)
+ *   C[m, n]   = alpha * (acc[m, n] * scale[n]) + beta * C_old[m, n]
+ * i.e. X times the transpose of the dequantised weight W[n, k] * scale[n],
+ * one scale per weight row (per output column).  The descriptor has
+ * a_dtype = X's type (TC_F16 or TC_BF16), b_dtype = TC_I8, accum_dtype =
+ * TC_F32, c_dtype = a_dtype or TC_F32 (TC_ERR_DTYPE otherwise), and
+ * transpose_a = false, transpose_b = true: X stored [M,K] (lda >= K), W
+ * stored [N,K] (ldb >= K), the pages' layout (TC_ERR_LAYOUT otherwise).
+ * X, W, C and scale (N floats, TC_ERR_NULL if NULL, must not overlap C)
+ * are DEVICE pointers owned by the caller.  Up to 16 rows of X the int8
+ * weights are streamed once and widened in registers (one launch, no
+ * scratch); beyond, they are first widened exactly to X's type in a
+ * per-stream buffer the library owns, then the tensor-core GEMM applies the
+ * scales in its epilogue.  Any alignment and leading dimension; the same
+ * validation, error and determinism rules as tc_gemm.  The Q4_0 / Q4_K
+ * block formats and the Q8_0 block layout are not printed on the pages and
+ * have no entry point. */
+tc_status_t tc_gemm_q8_weight(tc_ctx *ctx, const tc_gemm_desc *d, const float *scale, const void *X,
+                              const void *W, void *C);
+tc_status_t tc_gemm_q8_weight_async(tc_ctx *ctx, const tc_gemm_desc *d, const float *scale, const void *X,
+                                    const void *W, void *C, tc_stream *s);
+/* Host-only: the validation tc_gemm_q8_weight runs first (no device needed). */
+tc_status_t tc_gemm_q8_weight_validate(const tc_gemm_desc *d, const float *scale, const void *X, const void *W,
+                                       const void *C);
 
 /* Same GEMM with HOST operands: copies A and B (and C when beta != 0) to the
  * device, runs, copies C back and waits.  Device buffers are cached in the

@@ -32,7 +32,7 @@ STATUS = {
     0: "TC_OK", 1: "TC_ERR_NULL", 2: "TC_ERR_DIM", 3: "TC_ERR_LD", 4: "TC_ERR_DTYPE",
     5: "TC_ERR_SCALAR", 6: "TC_ERR_OVERLAP", 7: "TC_ERR_OVERFLOW", 8: "TC_ERR_ALIGN_UNSUPPORTED",
     9: "TC_ERR_CUDA", 10: "TC_ERR_DEVICE_TIMEOUT", 11: "TC_ERR_STRIDE", 12: "TC_ERR_VARIANT",
-    13: "TC_ERR_SCRATCH", 14: "TC_ERR_EPILOGUE",
+    13: "TC_ERR_SCRATCH", 14: "TC_ERR_EPILOGUE", 15: "TC_ERR_LAYOUT",
 }
 for _code, _name in STATUS.items():
     globals()[_name] = _code
@@ -103,6 +103,9 @@ def _load():
         "tc_gemm_f32_relaxed": (st, [vp, D, E, vp, vp, vp]),
         "tc_gemm_i8_dequant": (st, [vp, D, vp, vp, vp, vp]),
         "tc_gemm_i8_dequant_async": (st, [vp, D, vp, vp, vp, vp, vp]),
+        "tc_gemm_q8_weight": (st, [vp, D, vp, vp, vp, vp]),
+        "tc_gemm_q8_weight_async": (st, [vp, D, vp, vp, vp, vp, vp]),
+        "tc_gemm_q8_weight_validate": (st, [D, vp, vp, vp, vp]),
         "tc_gemm_f32_relaxed_async": (st, [vp, D, E, vp, vp, vp, vp]),
         "tc_gemm_host": (st, [vp, D, vp, vp, vp]),
         "tc_gemm_splitk_noalloc": (st, [D, vp, vp, vp, ctypes.c_int, vp]),
@@ -129,6 +132,7 @@ EXPORTED = (
     "tc_gemm_batched_validate", "tc_gemm_plan", "tc_last_kernel", "tc_launch_count",
     "tc_status_string", "tc_gemm_epilogue", "tc_gemm_epilogue_async", "tc_gemm_epilogue_validate",
     "tc_gemm_f32_relaxed", "tc_gemm_f32_relaxed_async", "tc_gemm_i8_dequant", "tc_gemm_i8_dequant_async",
+    "tc_gemm_q8_weight", "tc_gemm_q8_weight_async", "tc_gemm_q8_weight_validate",
 )
 
 
@@ -162,11 +166,14 @@ def _addr(x) -> int:
 
 
 def make_desc(M, N, K, a_dtype, c_dtype=None, *, transpose_a=False, transpose_b=False,
-              alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0) -> tc_gemm_desc:
+              alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0, b_dtype=None) -> tc_gemm_desc:
+    """A descriptor; B has A's type unless ``b_dtype`` is given (the
+    int8-weight product: a_dtype "f16"/"bf16", b_dtype "i8")."""
     a = _DT_NAMES.get(a_dtype, a_dtype)
+    b = _DT_NAMES.get(b_dtype, b_dtype) if b_dtype is not None else a
     c = _DT_NAMES.get(c_dtype, c_dtype) if c_dtype is not None else a
-    accum = TC_I32 if a == TC_I8 else TC_F32       # int8 operands accumulate in int32
-    return tc_gemm_desc(M, N, K, a, a, c, accum, bool(transpose_a), bool(transpose_b),
+    accum = TC_I32 if a == TC_I8 else TC_F32       # int8 x int8 accumulates in int32
+    return tc_gemm_desc(M, N, K, a, b, c, accum, bool(transpose_a), bool(transpose_b),
                         float(alpha), float(beta), lda, ldb, ldc)
 
 
@@ -387,6 +394,27 @@ def tc_gemm_i8_dequant_async(ctx: Context, d: tc_gemm_desc, A, B, C, col_scale, 
     _require(col_scale, d.N, "col_scale")
     _check(_lib.tc_gemm_i8_dequant_async(ctx.ptr, ctypes.byref(d), _addr(col_scale), _addr(A), _addr(B), _addr(C),
                                          stream.ptr), "tc_gemm_i8_dequant_async")
+
+
+def tc_gemm_q8_weight(ctx: Context, d: tc_gemm_desc, X, W, C, scale):
+    """Out = alpha * (X @ W^T) * scale[n] + beta * Out, X [M,K] f16/bf16,
+    W [N,K] int8, scale N floats (CUDA tensors), synchronously."""
+    _check_capacity(d, X, W, C)
+    _require(scale, d.N, "scale")
+    _check(_lib.tc_gemm_q8_weight(ctx.ptr, ctypes.byref(d), _addr(scale), _addr(X), _addr(W), _addr(C)),
+           "tc_gemm_q8_weight")
+
+
+def tc_gemm_q8_weight_async(ctx: Context, d: tc_gemm_desc, X, W, C, scale, stream: Stream):
+    _check_capacity(d, X, W, C)
+    _require(scale, d.N, "scale")
+    _check(_lib.tc_gemm_q8_weight_async(ctx.ptr, ctypes.byref(d), _addr(scale), _addr(X), _addr(W), _addr(C),
+                                        stream.ptr), "tc_gemm_q8_weight_async")
+
+
+def tc_gemm_q8_weight_validate(d: tc_gemm_desc, scale=4 << 40, X=1 << 20, W=2 << 40, C=3 << 40) -> int:
+    """Host-only validation status of an int8-weight product."""
+    return int(_lib.tc_gemm_q8_weight_validate(ctypes.byref(d), _addr(scale), _addr(X), _addr(W), _addr(C)))
 
 
 def tc_gemm_host(ctx: Context, d: tc_gemm_desc, A_host, B_host, C_host):

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libtcgemm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]
-SOURCES = ["api.cpp", "tc_mma.cu", "ffma.cu", "pack.cu"]
+SOURCES = ["api.cpp", "tc_mma.cu", "ffma.cu", "pack.cu", "gemv.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "elem.cuh"]
 
 

@@ -49,7 +49,13 @@ struct tc_ctx {
     size_t dcap[3] = {0, 0, 0};
     cudaStream_t copy_in = nullptr, copy_out = nullptr;   // tc_gemm_host's copy streams
     int max_pairs[2] = {-1, -1};                   // resident CTA pairs (BN 128, 256), queried once
+    int csplit_clusters[2][17];                    // resident cluster splits (BN 64, 128; S), -1 = not queried
     std::mutex mu;
+    tc_ctx()
+    {
+        for (auto &row : csplit_clusters)
+            for (int &v : row) v = -1;
+    }
 };
 
 namespace {
@@ -87,15 +93,23 @@ bool ranges_overlap(const void *p, int64_t pb, const void *q, int64_t qb)
     return a0 < b1 && b0 < a1;
 }
 
-// int8 operands (accumulated in int32, written as fp32) only where allow_i8:
-// the integer GEMM has its own entry point.
+// Operand types each entry point accepts: the GEMM (a == b in f16, bf16,
+// f32), the integer GEMM (int8 x int8, int32 accumulation, fp32 C) and the
+// int8-weight product (f16/bf16 activations, int8 weights stored [N,K]).
+enum ValidateMode { V_GEMM = 0, V_I8 = 1, V_Q8W = 2 };
+
 tc_status_t validate(const tc_gemm_desc *d, const void *A, const void *B, const void *C, int64_t batch,
-                     int64_t sa, int64_t sb, int64_t sc, Norm *n, bool allow_i8 = false)
+                     int64_t sa, int64_t sb, int64_t sc, Norm *n, int mode = V_GEMM)
 {
     if (!d || !A || !B || !C) return TC_ERR_NULL;
     if (d->M < 1 || d->N < 1 || d->K < 1 || batch < 1) return TC_ERR_DIM;
-    if (d->a_dtype == TC_I8) {
-        if (!allow_i8 || d->b_dtype != TC_I8 || d->accum_dtype != TC_I32 || d->c_dtype != TC_F32)
+    if (mode == V_Q8W) {
+        if ((d->a_dtype != TC_F16 && d->a_dtype != TC_BF16) || d->b_dtype != TC_I8 || d->accum_dtype != TC_F32 ||
+            (d->c_dtype != d->a_dtype && d->c_dtype != TC_F32))
+            return TC_ERR_DTYPE;
+        if (d->transpose_a || !d->transpose_b) return TC_ERR_LAYOUT;
+    } else if (d->a_dtype == TC_I8) {
+        if (mode != V_I8 || d->b_dtype != TC_I8 || d->accum_dtype != TC_I32 || d->c_dtype != TC_F32)
             return TC_ERR_DTYPE;
     } else {
         const bool ab_ok = d->a_dtype == TC_F16 || d->a_dtype == TC_BF16 || d->a_dtype == TC_F32;
@@ -119,9 +133,10 @@ tc_status_t validate(const tc_gemm_desc *d, const void *A, const void *B, const 
     r.sa = sa;
     r.sb = sb;
     r.sc = sc;
-    const int64_t ea = (int64_t)elem_size(d->a_dtype), ec = (int64_t)elem_size(d->c_dtype);
+    const int64_t ea = (int64_t)elem_size(d->a_dtype), eb = (int64_t)elem_size(d->b_dtype),
+                  ec = (int64_t)elem_size(d->c_dtype);
     if (!extent(r.a_rows, r.a_cols, r.lda, batch, sa, ea, &r.a_bytes) ||
-        !extent(r.b_rows, r.b_cols, r.ldb, batch, sb, ea, &r.b_bytes) ||
+        !extent(r.b_rows, r.b_cols, r.ldb, batch, sb, eb, &r.b_bytes) ||
         !extent(d->M, d->N, r.ldc, batch, sc, ec, &r.c_bytes))
         return TC_ERR_OVERFLOW;
     if (batch > 1) {
@@ -151,6 +166,12 @@ struct Plan {
     int ffma_tile = FFMA_SMALL;
     int bn = 256, cg = 1, split = 1, grid = 1, group_m = 8;
     bool i8acc = false;        // int8: exact K slices summed in TMEM (one unit per tile)
+    bool csplit = false;       // split-K as clusters of K slices reduced on chip (seg0_split CTAs per cluster)
+    // the skinny-product kernel (gemv.cu): X = op(A) and W = B (rows N), or,
+    // when swapped, X = B^T (N rows) and W = A (rows M); K split over a
+    // cluster of gemv_ks CTAs
+    bool gemv = false, gemv_swap = false;
+    int gemv_ks = 1;
     int64_t seg0_tiles = 0, split_base = 0;
     int seg0_split = 1, seg1_split = 1;
     bool tma_store = true;
@@ -170,7 +191,10 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // MN-major operand is read 64 columns per copy instead of one chunked copy)
 // i8acc=0 (int8: K slices through memory and the reduction kernel, not
 // summed on chip) shorta=0 (a one-CTA tile copies all 128 rows of A even
-// when A has fewer).
+// when A has fewer) csplit=0 (split-K slices go through global memory and
+// the reduction kernel instead of a cluster reduction on chip) gemv=0 (a
+// product with at most 16 rows on one side stays on the tensor-core kernel)
+// gemv_ks=<1|2|4|8> (the skinny-product kernel's K split).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -182,6 +206,8 @@ struct Force {
     int no_chunk = 0;
     int no_short_a = 0;
     int i8acc = -1;
+    int csplit = -1;
+    int gemv = -1, gemv_ks = 0;
 };
 
 Force read_force()
@@ -217,6 +243,9 @@ Force read_force()
         else if (k == "chunk") f.no_chunk = std::atoi(v.c_str()) == 0;
         else if (k == "shorta") f.no_short_a = std::atoi(v.c_str()) == 0;
         else if (k == "i8acc") f.i8acc = std::atoi(v.c_str());
+        else if (k == "csplit") f.csplit = std::atoi(v.c_str());
+        else if (k == "gemv") f.gemv = std::atoi(v.c_str());
+        else if (k == "gemv_ks") f.gemv_ks = std::atoi(v.c_str());
     }
     return f;
 }
@@ -237,6 +266,10 @@ double tile_rate(int cg, int bn)
 // GEMM grid, one pass over the partial tiles), in the schedule's time unit:
 // one K block of one 256-wide tile column at tile rate 1, ~1 ns on GB300.
 constexpr double SPLIT_FIXED = 4500.0;
+// The same for a cluster split (two cluster barriers and one pass over the
+// slices' shared memory, inside the GEMM kernel).
+constexpr double CSPLIT_FIXED = 1200.0;
+constexpr int CSPLIT_MAX = 16;      // CTAs per cluster (non-portable size)
 
 // Persistent schedule of `tiles` output tiles on num_sms CTAs: whole waves
 // of tiles, then the partial last wave.  When the last wave leaves at least
@@ -266,8 +299,22 @@ Sched schedule(int64_t tiles, int64_t num_kb, int num_sms, int cg, int bn, int f
     return s;
 }
 
+// K split of the skinny-product kernel: clusters of up to 8 CTAs along K
+// until there are at least two CTAs per SM, keeping at least 32 K steps
+// (4 per warp) per CTA.
+int gemv_ksplit(int64_t rows_w, int64_t K, bool w_i8, int num_sms)
+{
+    const int64_t blocks = cdiv(rows_w, 16);
+    const int64_t steps = cdiv(K, w_i8 ? 64 : 32);
+    int ks = 1;
+    while (ks < 8 && blocks * ks < 2LL * num_sms && steps / (2LL * ks) >= 32) ks *= 2;
+    return ks;
+}
+
+// allow_gemv: the call may take the skinny-product kernel (a plain GEMM:
+// no fused epilogue, no per-column scale).
 tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const void *B, int num_sms,
-                      Plan *out)
+                      Plan *out, bool allow_gemv = true)
 {
     Plan p;
     const Force f = read_force();
@@ -293,6 +340,23 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
         return TC_OK;
     }
 
+    // At most GEMV_MAX_ROWS rows on one side of an NT product (both operands
+    // K-contiguous: the decode shape x[M, K] @ W[N, K]^T): the weight side is
+    // streamed once by the skinny-product kernel instead of padding a
+    // 128-row tensor-core tile.
+    if (allow_gemv && f.gemv != 0 && n.batch == 1 && !d->transpose_a && d->transpose_b &&
+        (d->M <= GEMV_MAX_ROWS || d->N <= GEMV_MAX_ROWS)) {
+        p.gemv = true;
+        p.gemv_swap = d->M > GEMV_MAX_ROWS;
+        const int64_t rows_w = p.gemv_swap ? d->M : d->N, rows_x = p.gemv_swap ? d->N : d->M;
+        p.gemv_ks = f.gemv_ks > 0 ? f.gemv_ks : gemv_ksplit(rows_w, d->K, false, num_sms);
+        std::snprintf(buf, sizeof buf, "gemv_%s_%s_%s_x%d_ks%d%s", lay, dt, ct, (int)rows_x, p.gemv_ks,
+                      p.gemv_swap ? "_swap" : "");
+        p.name = buf;
+        *out = p;
+        return TC_OK;
+    }
+
     // TMA reads an operand in place only with a 16-byte aligned base and
     // 16-byte multiple row (and batch) strides; otherwise it is repacked.
     const bool a3 = n.batch > 1 && n.sa != 0, b3 = n.batch > 1 && n.sb != 0;
@@ -305,13 +369,18 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     int bn = 0, cg = 1;
     Sched sc{};
     bool split_k = (f.split == 0 && f.cg != 2 && tiles128 * 2 <= num_sms && num_kb >= 16) || f.split > 0;
+    // cluster split (slices reduced on chip in one launch) unless disabled or
+    // a forced split is longer than a cluster can be
+    const bool csplit_ok = f.csplit != 0 && f.cg != 2 && (f.split == 0 || f.split <= CSPLIT_MAX);
     if (split_k && f.split == 0 && f.bn == 0) {
         // 64-wide whole-K tiles instead, when they fill at least half the SMs
         // and the split's reduction would cost more than their lower rate
-        // (e.g. fp16 1024^3 on GB300: 13.8 us against 16.7 us split in two)
+        // (e.g. fp16 1024^3 on GB300: 13.8 us against 16.7 us split in two
+        // through memory)
         const int64_t tiles64 = cdiv(d->M, BM) * cdiv(d->N, 64) * n.batch;
         const int64_t split = std::min<int64_t>(std::max<int64_t>(num_sms / tiles128, 1), num_kb / 4);
-        const double t_split = (double)cdiv(num_kb, split) * 128.0 / tile_rate(1, 128) + SPLIT_FIXED;
+        const double t_split = (double)cdiv(num_kb, split) * 128.0 / tile_rate(1, 128) +
+                               (csplit_ok ? CSPLIT_FIXED : SPLIT_FIXED);
         const double t_64 = (double)cdiv(tiles64, num_sms) * (double)num_kb * 64.0 / tile_rate(1, 64);
         if (tiles64 * 2 >= num_sms && t_64 < t_split) {
             split_k = false;
@@ -322,10 +391,41 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     if (split_k) {
         // split-K: too few output tiles to occupy the SMs and a long K loop
         bn = f.bn ? f.bn : 128;
-        const int64_t tiles = cdiv(d->M, BM) * cdiv(d->N, bn) * n.batch;
+        int64_t tiles = cdiv(d->M, BM) * cdiv(d->N, bn) * n.batch;
         int split = f.split > 0 ? f.split
                                 : (int)std::min<int64_t>(std::max<int64_t>(num_sms / tiles, 1), num_kb / 4);
         split = (int)std::min<int64_t>(std::max(split, 1), num_kb);
+        if (csplit_ok && (bn == 64 || bn == 128)) {
+            // Cluster split: at most CSPLIT_MAX slices per tile.  Tile width
+            // 128 or 64, whichever leaves each CTA fewer operand bytes to
+            // load (per CTA: ceil(K blocks / S) stages, times the waves of
+            // clusters), since these shapes are bound by how fast each CTA
+            // pulls its operands, not by the tensor core.
+            int best_bn = 0, best_s = 0;
+            double best_cost = 1e300;
+            for (int b : {128, 64}) {
+                if (f.bn && b != f.bn) continue;
+                const int64_t t = cdiv(d->M, BM) * cdiv(d->N, b) * n.batch;
+                int64_t S = f.split > 0 ? f.split
+                                        : std::min<int64_t>({(int64_t)CSPLIT_MAX, std::max<int64_t>(num_sms / t, 1),
+                                                             num_kb / 4});
+                S = std::min<int64_t>(S, num_kb);
+                if (S < 2) continue;
+                const double waves = std::ceil((double)(t * S) / num_sms);
+                const double cost = waves * (double)cdiv(num_kb, S) * (double)stage_bytes(b, 1);
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    best_bn = b;
+                    best_s = (int)S;
+                }
+            }
+            if (best_bn) {
+                p.csplit = true;
+                bn = best_bn;
+                split = best_s;
+                tiles = cdiv(d->M, BM) * cdiv(d->N, bn) * n.batch;
+            }
+        }
         sc = {tiles, tiles, split, 1, 0.0};
     } else if (bn == 64) {
         cg = 1;
@@ -361,11 +461,13 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     if (p.units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
     p.grid = (int)std::min<int64_t>(p.units, workers);
     if (f.grid > 0) p.grid = (int)std::min<int64_t>(f.grid, p.units);
+    if (p.csplit) p.grid = (int)p.units;           // one CTA per (tile, slice): clusters of slices
     p.grid *= cg;                                  // CTAs
     p.group_m = f.group_m > 0 ? f.group_m : 4;
     p.tma_store = !f.direct_store;
     std::snprintf(buf, sizeof buf, "tcgen05_%s_%s_%s_%dx%d%s%s%s%s", lay, dt, ct, BM * cg, bn,
-                  cg == 2 ? "_pair" : "", sc.seg0_split > 1 ? "_splitk" : "", p.pack_a ? "_packA" : "",
+                  cg == 2 ? "_pair" : "", sc.seg0_split > 1 ? (p.csplit ? "_csplit" : "_splitk") : "",
+                  p.pack_a ? "_packA" : "",
                   p.pack_b ? "_packB" : "");
     p.name = buf;
     if (sc.seg0_split > 1) {
@@ -457,11 +559,67 @@ tc_status_t read_status(tc_stream *s)
 // bias/activation epilogue, or null).
 // col_scale: the int8 path's per-column dequantisation (its K slices then
 // hold integers and are added as such), or null.
-tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Plan &p, const void *A,
+// int_slices: the int8 path -- K slices hold exact integers and are added
+// as integers (through memory only, never a cluster split).
+tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Plan &plan, const void *A,
                     const void *B, void *C, tc_stream *s, const tc_epilogue *epi = nullptr,
-                    const float *col_scale = nullptr)
+                    const float *col_scale = nullptr, bool int_slices = false)
 {
     cudaError_t e;
+    Plan p = plan;
+    if (p.gemv) {
+        GemvArgs g{};
+        g.X = p.gemv_swap ? B : A;
+        g.W = p.gemv_swap ? A : B;
+        g.C = C;
+        g.scale = nullptr;
+        g.rows_x = p.gemv_swap ? d->N : d->M;
+        g.rows_w = p.gemv_swap ? d->M : d->N;
+        g.K = d->K;
+        g.ldx = p.gemv_swap ? n.ldb : n.lda;
+        g.ldw = p.gemv_swap ? n.lda : n.ldb;
+        g.c_sx = p.gemv_swap ? 1 : n.ldc;
+        g.c_sw = p.gemv_swap ? n.ldc : 1;
+        g.c_dtype = d->c_dtype;
+        g.alpha = d->alpha;
+        g.beta = d->beta;
+        g.x_vec = aligned16(g.X) && (g.ldx * 2) % 16 == 0;
+        g.w_vec = aligned16(g.W) && (g.ldw * 2) % 16 == 0;
+        g.w_i8 = 0;
+        g.x_bf16 = d->a_dtype == TC_BF16;
+        g.ksplit = p.gemv_ks;
+        if (launch_gemv(g, s->st) != cudaSuccess) return TC_ERR_CUDA;
+        ctx->launches += 1;
+        ctx->last = p.name;
+        return TC_OK;
+    }
+    if (p.csplit) {
+        // A cluster split needs its clusters of K slices to be schedulable
+        // on this device, and all of them resident at once: a second wave
+        // of clusters doubles the time (on GB300 only 7 clusters of 16 fit,
+        // 8 of 12).  Unless the split was forced, the slice count shrinks
+        // until every tile's cluster is resident; with no schedulable
+        // cluster at all the same slices go through global memory.
+        auto clusters = [&](int S) {
+            int &mc = ctx->csplit_clusters[p.bn == 64 ? 0 : 1][std::min(S, CSPLIT_MAX)];
+            if (mc < 0) mc = max_active_csplit_clusters(p.bn, S);
+            return mc;
+        };
+        int S = p.seg0_split;
+        if (read_force().split == 0)
+            while (S > 2 && clusters(S) < p.tiles) --S;
+        if (clusters(S) < 1 || int_slices) {
+            p.csplit = false;
+            p.grid = (int)std::min<int64_t>(p.units, ctx->num_sms);
+            const std::string::size_type at = p.name.find("_csplit");
+            if (at != std::string::npos) p.name.replace(at, 7, "_splitk");
+        } else if (S != p.seg0_split) {
+            p.seg0_split = S;
+            p.units = p.tiles * S;
+            p.grid = (int)p.units;
+            p.name = p.name.substr(0, p.name.rfind("_s")) + "_s" + std::to_string(S);
+        }
+    }
     if (p.ffma) {
         FfmaArgs a{};
         a.M = d->M;
@@ -496,8 +654,9 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     const int64_t ldb_p = p.pack_b ? (int64_t)round_up((size_t)n.b_cols, 64) : n.ldb;
     const size_t a_pack_bytes = p.pack_a ? round_up((size_t)(n.a_rows * lda_p * a_batch * 2), 256) : 0;
     const size_t b_pack_bytes = p.pack_b ? round_up((size_t)(n.b_rows * ldb_p * b_batch * 2), 256) : 0;
+    const bool partials = p.split > 1 && !p.csplit;     // K slices summed through global memory
     const size_t part_bytes =
-        p.split > 1 ? (size_t)(p.units - p.split_base) * BM * p.cg * p.bn * sizeof(float) : 0;
+        partials ? (size_t)(p.units - p.split_base) * BM * p.cg * p.bn * sizeof(float) : 0;
     tc_status_t st = ensure_ws(s, a_pack_bytes + b_pack_bytes + part_bytes + 256);
     if (st != TC_OK) return st;
     uint8_t *ws = static_cast<uint8_t *>(s->ws);
@@ -528,6 +687,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     L.bn = p.bn;
     L.cg = p.cg;
     L.i8acc = p.i8acc ? 1 : 0;
+    L.csplit = p.csplit ? 1 : 0;
     L.grid = p.grid;
     if (p.cg == 2) {
         // no more pairs than can be resident at once (a persistent grid)
@@ -573,7 +733,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     // C written through TMA stores of 32 x 32 chunks when its layout allows
     a.c_tma = a.c_vec_ok && p.tma_store;
     a.c_3d = n.batch > 1;
-    a.ws = p.split > 1 ? reinterpret_cast<float *>(ws + a_pack_bytes + b_pack_bytes) : nullptr;
+    a.ws = partials ? reinterpret_cast<float *>(ws + a_pack_bytes + b_pack_bytes) : nullptr;
     a.status = s->status_dev;
     a.bias = epi ? epi->bias : nullptr;
     a.act = epi ? (int)epi->activation : (int)TC_ACT_NONE;
@@ -648,7 +808,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         r.bias = a.bias;
         r.act = a.act;
         r.col_scale = col_scale;
-        r.int_sum = col_scale != nullptr;
+        r.int_sum = int_slices ? 1 : 0;
         // (r.status stays null: the stream's status word is mapped host
         // memory, and tc_stream_sync reports an expired wait, after which C
         // is undefined)
@@ -878,7 +1038,7 @@ tc_status_t run(tc_ctx *ctx, const tc_gemm_desc *d, const void *A, const void *B
     if (st != TC_OK) return st;
     if (epi && (st = validate_epilogue(d, n, epi, C)) != TC_OK) return st;
     Plan p;
-    if ((st = make_plan(d, n, A, B, ctx->num_sms, &p)) != TC_OK) return st;
+    if ((st = make_plan(d, n, A, B, ctx->num_sms, &p, epi == nullptr)) != TC_OK) return st;
     std::lock_guard<std::mutex> g(ctx->mu);
     if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
     return enqueue(ctx, d, n, p, A, B, C, s, epi);
@@ -950,7 +1110,7 @@ tc_status_t run_relaxed(tc_ctx *ctx, const tc_gemm_desc *d, const tc_epilogue *e
     Norm n2;
     if ((st = validate(&d2, A2, B2, C, 1, 0, 0, 0, &n2)) != TC_OK) return st;
     Plan p2;
-    if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p2)) != TC_OK) return st;
+    if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p2, false)) != TC_OK) return st;
     const SplitArgs sa{static_cast<const float *>(A), A2, n.a_rows, n.a_cols, n.lda, lda2, a_kcols ? 1 : 0, {0, 0, 1}};
     const SplitArgs sb{static_cast<const float *>(B), B2, n.b_rows, n.b_cols, n.ldb, ldb2, b_kcols ? 1 : 0, {0, 1, 0}};
     if (launch_split(sa, s->st) != cudaSuccess || launch_split(sb, s->st) != cudaSuccess) return TC_ERR_CUDA;
@@ -973,7 +1133,7 @@ tc_status_t run_i8(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, c
 {
     if (!ctx || !s) return TC_ERR_NULL;
     Norm n;
-    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n, true);
+    tc_status_t st = validate(d, A, B, C, 1, 0, 0, 0, &n, V_I8);
     if (st != TC_OK) return st;
     if (d->a_dtype != TC_I8) return TC_ERR_DTYPE;
     if (!col_scale) return TC_ERR_NULL;
@@ -996,7 +1156,8 @@ tc_status_t run_i8(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, c
     Norm n2;
     if ((st = validate(&d2, A2, B2, C, 1, 0, 0, 0, &n2)) != TC_OK) return st;
     Plan p;
-    if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p)) != TC_OK) return st;
+    if ((st = make_plan(&d2, n2, A2, B2, ctx->num_sms, &p, false)) != TC_OK) return st;
+    p.csplit = false;      // integer slices are added through memory (or on chip in TMEM)
     const int64_t num_kb = cdiv(d->K, BK);
     const int S = (int)cdiv(num_kb, I8_SLICE_KB);
     char buf[48];
@@ -1035,12 +1196,88 @@ tc_status_t run_i8(tc_ctx *ctx, const tc_gemm_desc *d, const float *col_scale, c
     if (p.units > INT32_MAX / 2) return TC_ERR_OVERFLOW;
     const int workers = p.cg == 2 ? std::max(ctx->num_sms / 2, 1) : ctx->num_sms;
     p.grid = (int)std::min<int64_t>(p.units, workers) * p.cg;
-    const WidenArgs wa{static_cast<const int8_t *>(A), A2, n.a_rows, n.a_cols, n.lda, lda2};
-    const WidenArgs wb{static_cast<const int8_t *>(B), B2, n.b_rows, n.b_cols, n.ldb, ldb2};
+    const WidenArgs wa{static_cast<const int8_t *>(A), A2, n.a_rows, n.a_cols, n.lda, lda2, 0};
+    const WidenArgs wb{static_cast<const int8_t *>(B), B2, n.b_rows, n.b_cols, n.ldb, ldb2, 0};
     if (launch_widen(wa, s->st) != cudaSuccess || launch_widen(wb, s->st) != cudaSuccess) return TC_ERR_CUDA;
     ctx->launches += 2;
-    st = enqueue(ctx, &d2, n2, p, A2, B2, C, s, nullptr, col_scale);
+    st = enqueue(ctx, &d2, n2, p, A2, B2, C, s, nullptr, col_scale, true);
     if (st == TC_OK) ctx->last = "i8_dequant_" + ctx->last.substr(0, ctx->last.find("_tail")) + buf;
+    return st;
+}
+
+// ---------------------------------------------------- int8-weight product
+// Foundry metal.md, "Custom Compute Kernels" (fm_sgemm_q8, fm_matvec_q8):
+// Out = X @ (W_q8 * scale[n])^T; tensorcore gemm.md "Kernel variants": the
+// M <= 4 GEMV over Q8 weights.  Up to GEMV_MAX_ROWS activation rows the
+// skinny-product kernel streams the int8 weights once and widens them in
+// registers; beyond, the weights are widened once (exactly) to the
+// activations' type and the tensor-core GEMM applies the scales in its
+// epilogue.
+
+tc_status_t run_q8w(tc_ctx *ctx, const tc_gemm_desc *d, const float *scale, const void *X, const void *W, void *C,
+                    tc_stream *s)
+{
+    if (!ctx || !s) return TC_ERR_NULL;
+    Norm n;
+    tc_status_t st = validate(d, X, W, C, 1, 0, 0, 0, &n, V_Q8W);
+    if (st != TC_OK) return st;
+    if (!scale) return TC_ERR_NULL;
+    if (ranges_overlap(scale, (int64_t)d->N * 4, C, n.c_bytes)) return TC_ERR_OVERLAP;
+    const Force f = read_force();
+    const char *dt = d->a_dtype == TC_BF16 ? "bf16" : "f16";
+    const char *ct = d->c_dtype == TC_F32 ? "f32" : dt;
+    char buf[96];
+    if (d->M <= GEMV_MAX_ROWS && f.gemv != 0) {
+        GemvArgs g{};
+        g.X = X;
+        g.W = W;
+        g.C = C;
+        g.scale = scale;
+        g.rows_x = d->M;
+        g.rows_w = d->N;
+        g.K = d->K;
+        g.ldx = n.lda;
+        g.ldw = n.ldb;
+        g.c_sx = n.ldc;
+        g.c_sw = 1;
+        g.c_dtype = d->c_dtype;
+        g.alpha = d->alpha;
+        g.beta = d->beta;
+        g.x_vec = aligned16(X) && (n.lda * 2) % 16 == 0;
+        g.w_vec = aligned16(W) && n.ldb % 16 == 0;
+        g.w_i8 = 1;
+        g.x_bf16 = d->a_dtype == TC_BF16;
+        g.ksplit = f.gemv_ks > 0 ? f.gemv_ks : gemv_ksplit(d->N, d->K, true, ctx->num_sms);
+        std::snprintf(buf, sizeof buf, "gemv_q8w_nt_%s_%s_x%d_ks%d", dt, ct, (int)d->M, g.ksplit);
+        std::lock_guard<std::mutex> lk(ctx->mu);
+        if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+        if (launch_gemv(g, s->st) != cudaSuccess) return TC_ERR_CUDA;
+        ctx->launches += 1;
+        ctx->last = buf;
+        return TC_OK;
+    }
+    // W [N, K] int8 -> the activations' type, rows padded to 64 elements
+    const int64_t ldb2 = (int64_t)round_up((size_t)d->K, 64);
+    if (ldb2 > INT32_MAX) return TC_ERR_OVERFLOW;
+    const size_t w_bytes = (size_t)(d->N * ldb2 * 2);
+    tc_gemm_desc d2 = *d;
+    d2.b_dtype = d->a_dtype;
+    d2.ldb = (int32_t)ldb2;
+    d2.lda = (int32_t)n.lda;
+    d2.ldc = (int32_t)n.ldc;
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
+    if ((st = ensure_rx(s, w_bytes)) != TC_OK) return st;
+    uint16_t *W2 = static_cast<uint16_t *>(s->rx);
+    Norm n2;
+    if ((st = validate(&d2, X, W2, C, 1, 0, 0, 0, &n2)) != TC_OK) return st;
+    Plan p;
+    if ((st = make_plan(&d2, n2, X, W2, ctx->num_sms, &p, false)) != TC_OK) return st;
+    const WidenArgs wa{static_cast<const int8_t *>(W), W2, d->N, d->K, n.ldb, ldb2, d->a_dtype == TC_F16 ? 1 : 0};
+    if (launch_widen(wa, s->st) != cudaSuccess) return TC_ERR_CUDA;
+    ctx->launches += 1;
+    st = enqueue(ctx, &d2, n2, p, X, W2, C, s, nullptr, scale, false);
+    if (st == TC_OK) ctx->last = "q8w_widen_" + ctx->last;
     return st;
 }
 
@@ -1091,6 +1328,7 @@ const char *tc_status_string(tc_status_t st)
     case TC_ERR_VARIANT: return "forced variant cannot serve this problem";
     case TC_ERR_SCRATCH: return "problem needs more scratch than the static buffer of tc_gemm_splitk_noalloc holds";
     case TC_ERR_EPILOGUE: return "fused epilogue refused: unknown activation, or f32 operands (exact-fp32 path)";
+    case TC_ERR_LAYOUT: return "transpose flags this call does not support";
     }
     return "unknown status";
 }
@@ -1249,6 +1487,32 @@ tc_status_t tc_gemm_i8_dequant(tc_ctx *ctx, const tc_gemm_desc *d, const float *
     tc_status_t st = run_i8(ctx, d, col_scale, A, B, C, ctx->def);
     if (st != TC_OK) return st;
     return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_q8_weight_async(tc_ctx *ctx, const tc_gemm_desc *d, const float *scale, const void *X,
+                                    const void *W, void *C, tc_stream *s)
+{
+    return run_q8w(ctx, d, scale, X, W, C, s);
+}
+
+tc_status_t tc_gemm_q8_weight(tc_ctx *ctx, const tc_gemm_desc *d, const float *scale, const void *X, const void *W,
+                              void *C)
+{
+    if (!ctx) return TC_ERR_NULL;
+    tc_status_t st = run_q8w(ctx, d, scale, X, W, C, ctx->def);
+    if (st != TC_OK) return st;
+    return tc_stream_sync(ctx->def);
+}
+
+tc_status_t tc_gemm_q8_weight_validate(const tc_gemm_desc *d, const float *scale, const void *X, const void *W,
+                                       const void *C)
+{
+    Norm n;
+    tc_status_t st = validate(d, X, W, C, 1, 0, 0, 0, &n, V_Q8W);
+    if (st != TC_OK) return st;
+    if (!scale) return TC_ERR_NULL;
+    if (ranges_overlap(scale, (int64_t)d->N * 4, C, n.c_bytes)) return TC_ERR_OVERLAP;
+    return TC_OK;
 }
 
 tc_status_t tc_gemm_batched_async(tc_ctx *ctx, const tc_gemm_batched_desc *bd, const void *A, const void *B,

@@ -1,0 +1,400 @@
+// Skinny products: Out = alpha * (X W^T) (* scale per W row) + beta * Out_old
+// for X with at most 16 rows.  This is the decode shape of the pages: the
+// tensorcore gemm.md "Kernel variants" table's M <= 4 GEMV (fp16 out) and
+// the Foundry metal.md "Custom Compute Kernels" int8-weight products
+// (fm_matvec_q8, fm_sgemm_q8: each weight row scaled by its own factor).
+//
+// Every weight byte is read once, so the product is bound by HBM, not by
+// arithmetic.  The kernel is built around the weight stream:
+//   * a warp owns 16 rows of W; each lane streams 16-byte loads of two rows
+//     (rows g and g + 8 of the warp's 16, g = lane / 4), four lanes covering
+//     64 contiguous bytes of a row per load, and several loads in flight;
+//   * the 8 warps of a CTA interleave along K over the same 16 rows; the CTA
+//     adds their partial sums in warp order through shared memory;
+//   * when there are few row blocks, K is also split across a cluster of up
+//     to 8 CTAs, whose sums are added in rank order through distributed
+//     shared memory (deterministic: a fixed order everywhere).
+// The multiply-adds run on mma.sync m16n8k16 (fp32 accumulation) with W as
+// the 16-row operand and X^T as the 8-column operand: the K order inside one
+// lane's load is remapped the same way for both operands, so the fragments
+// come straight from the loaded registers.  On CUDA cores the same work
+// would need a type conversion and M fused multiply-adds per weight, which
+// for int8 weights at M = 4 comes close to the FFMA peak at HBM speed.
+// int8 weights are widened exactly in registers (byte permutes into the
+// mantissa of a half, then one subtraction).
+#include "elem.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+namespace tc {
+namespace {
+
+constexpr int GV_WARPS = 8;
+constexpr int GV_UNROLL = 4;      // register path: slabs in flight per warp
+constexpr int GV_STAGES = 8;      // copy path: slabs in flight per warp (each lane 2 x 16 bytes)
+constexpr int GV_RING = GV_WARPS * GV_STAGES * 2 * 32 * 16;   // bytes of the copy ring per CTA
+
+// 16 bytes global -> shared without passing through registers (cp.async,
+// L2 only); src_bytes = 0 writes zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// D(16x8, f32) += A(16x16) * B(16x8), A row-major, B column-major
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// 16 bytes of the weight stream: read once, so kept out of L1
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16 bytes of X, re-read by every CTA: through L1
+__device__ __forceinline__ uint4 ld_reuse16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+
+// Elements [k, k + E) of a row of 2-byte or 1-byte elements as 16 bytes,
+// zero beyond `kend`; element by element (an unaligned row or the K tail).
+template <int ESZ>
+__device__ __forceinline__ uint4 ld_partial(const uint8_t *row, long long k, long long kend)
+{
+    constexpr int E = 16 / ESZ;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        if (k + j < kend) {
+            uint32_t v = ESZ == 2 ? (uint32_t)reinterpret_cast<const uint16_t *>(row)[k + j]
+                                  : (uint32_t)(uint8_t)row[k + j];
+            w[(j * ESZ) / 4] |= v << (8 * ((j * ESZ) % 4));
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Four int8 values (one 32-bit word) -> two half2 / bf16x2 words, exactly.
+// half: 0x6400 | (b + 128) is the half 1024 + b + 128; subtracting 1152
+// leaves b.  bf16 has too few mantissa bits for that, so each byte goes
+// through fp32 the same way (0x4B000000 | (b + 128) is 2^23 + b + 128) and
+// the exact small integers are packed to bf16.
+template <bool BF16>
+__device__ __forceinline__ void widen4(uint32_t v, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = v ^ 0x80808080u;          // b + 128 in every byte
+    if constexpr (!BF16) {
+        const uint32_t p0 = __byte_perm(u, 0x64646464u, 0x4140u);
+        const uint32_t p1 = __byte_perm(u, 0x64646464u, 0x4342u);
+        const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480u));   // 1152
+        __half2 h0 = __hsub2(*reinterpret_cast<const __half2 *>(&p0), bias);
+        __half2 h1 = __hsub2(*reinterpret_cast<const __half2 *>(&p1), bias);
+        lo = *reinterpret_cast<uint32_t *>(&h0);
+        hi = *reinterpret_cast<uint32_t *>(&h1);
+    } else {
+        float f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            f[j] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u | (uint32_t)j)) - 8388736.0f;
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(f[0], f[1]);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(f[2], f[3]);
+        lo = *reinterpret_cast<uint32_t *>(&b0);
+        hi = *reinterpret_cast<uint32_t *>(&b1);
+    }
+}
+
+// BF16: X (and W unless W8) are bf16, else f16.  W8: W is int8.  NT: n8
+// tiles of X rows (1: at most 8 rows, 2: at most 16).
+// PIPE (16-byte aligned weight rows): each warp streams its slabs through a
+// ring of GV_STAGES slots in shared memory with cp.async, GV_STAGES - 1
+// slabs ahead of the one it multiplies (64 KB of the weight stream in
+// flight per CTA, two or more CTAs per SM); each lane reads back only the
+// 32 bytes it copied itself, so no synchronisation beyond its own copy
+// groups is needed.  The slab that ends past K goes through registers with
+// element loads.  Without PIPE (unaligned weight rows) every slab does, a
+// few per warp at a time.
+template <bool BF16, bool W8, int NT, bool PIPE>
+__global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a)
+{
+    constexpr int WK = W8 ? 16 : 8;             // weights per 16-byte load
+    constexpr int SLAB = 4 * WK;                // K values per warp step (4 lanes per row)
+    constexpr int XL = W8 ? 2 : 1;              // 16-byte X loads per weight load
+    constexpr int WSZ = W8 ? 1 : 2;
+    constexpr int COLS = NT * 8;                // X rows covered
+    __shared__ float red[GV_WARPS][16][COLS + 1];
+    __shared__ float sums[COLS][16];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int KS = a.ksplit;
+    const int rb = blockIdx.x / KS;
+    const int kr = blockIdx.x - rb * KS;       // rank in the cluster (consecutive CTAs)
+    const long long n0 = (long long)rb * 16;
+    const long long K = a.K;
+    const long long nslab = (K + SLAB - 1) / SLAB;
+    const long long s0 = (long long)kr * nslab / KS, s1 = (long long)(kr + 1) * nslab / KS;
+
+    const uint8_t *W = static_cast<const uint8_t *>(a.W);
+    const uint8_t *X = static_cast<const uint8_t *>(a.X);
+    const bool r0ok = n0 + g < a.rows_w, r1ok = n0 + g + 8 < a.rows_w;
+    const uint8_t *wrow0 = W + (r0ok ? (n0 + g) * a.ldw * WSZ : 0);
+    const uint8_t *wrow1 = W + (r1ok ? (n0 + g + 8) * a.ldw * WSZ : 0);
+    const uint8_t *xrow[NT];
+    bool xok[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        xok[nt] = nt * 8 + g < a.rows_x;
+        xrow[nt] = X + (xok[nt] ? (long long)(nt * 8 + g) * a.ldx * 2 : 0);
+    }
+
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+
+    auto load_w = [&](const uint8_t *row, bool ok, long long k) -> uint4 {
+        if (!ok) return make_uint4(0u, 0u, 0u, 0u);
+        if (a.w_vec && k + WK <= K) return ld_stream16(row + k * WSZ);
+        return ld_partial<WSZ>(row, k, K);
+    };
+    auto load_x = [&](int nt, long long k) -> uint4 {
+        if (!xok[nt]) return make_uint4(0u, 0u, 0u, 0u);
+        if (a.x_vec && k + 8 <= K) return ld_reuse16(xrow[nt] + k * 2);
+        return ld_partial<2>(xrow[nt], k, K);
+    };
+
+    // One slab: lane (g, t) holds K values [k, k + WK) of rows g and g + 8
+    // (w0, w1) and of X rows g (and 8 + g); MMA j takes pairs 4j..4j+1 as
+    // the fragments' columns 2t..2t+1 and pairs 4j+2..4j+3 as columns
+    // 2t+8..2t+9, for W and X alike.  X is read as it is needed (it stays in
+    // L1).  Every lane of the warp calls it.
+    auto mma_slab = [&](const uint4 &w0, const uint4 &w1, long long k) {
+        uint4 xv[NT][XL];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < XL; ++q) xv[nt][q] = load_x(nt, k + 8 * q);
+        uint32_t h0[WK / 2], h1[WK / 2];
+        if constexpr (W8) {
+            const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                widen4<BF16>(r0[q], h0[2 * q], h0[2 * q + 1]);
+                widen4<BF16>(r1[q], h1[2 * q], h1[2 * q + 1]);
+            }
+        } else {
+            h0[0] = w0.x, h0[1] = w0.y, h0[2] = w0.z, h0[3] = w0.w;
+            h1[0] = w1.x, h1[1] = w1.y, h1[2] = w1.z, h1[3] = w1.w;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint32_t x[WK / 2];
+#pragma unroll
+            for (int q = 0; q < XL; ++q) {
+                x[4 * q + 0] = xv[nt][q].x;
+                x[4 * q + 1] = xv[nt][q].y;
+                x[4 * q + 2] = xv[nt][q].z;
+                x[4 * q + 3] = xv[nt][q].w;
+            }
+#pragma unroll
+            for (int j = 0; j < WK / 4; ++j) {
+                const uint32_t afrag[4] = {h0[2 * j], h1[2 * j], h0[2 * j + 1], h1[2 * j + 1]};
+                mma_16816<BF16>(acc[nt], afrag, x[2 * j], x[2 * j + 1]);
+            }
+        }
+    };
+
+    long long s_reg = s0 + warp;        // first slab of this warp left for the register path
+    if constexpr (PIPE) {
+        // slabs wholly inside K go through the ring: slabs s0 + warp + 8i
+        extern __shared__ __align__(16) uint8_t gv_ring[];
+        const long long full_end = min(s1, K / SLAB);
+        const long long first = s0 + warp;
+        const long long nmine = first < full_end ? (full_end - first + GV_WARPS - 1) / GV_WARPS : 0;
+        const uint32_t ring = smem_u32(gv_ring) + (uint32_t)(warp * GV_STAGES * 2 * 32 * 16 + lane * 16);
+        auto issue = [&](long long i) {
+            const long long k = (first + i * GV_WARPS) * SLAB + t * WK;
+            const uint32_t slot = ring + (uint32_t)((i % GV_STAGES) * 2 * 32 * 16);
+            cp_async16(slot, wrow0 + k * WSZ, r0ok ? 16u : 0u);
+            cp_async16(slot + 32 * 16, wrow1 + k * WSZ, r1ok ? 16u : 0u);
+        };
+#pragma unroll
+        for (int i = 0; i < GV_STAGES - 1; ++i) {
+            if (i < nmine) issue(i);
+            cp_async_commit();
+        }
+        for (long long i = 0; i < nmine; ++i) {
+            if (i + GV_STAGES - 1 < nmine) issue(i + GV_STAGES - 1);
+            cp_async_commit();
+            cp_async_wait<GV_STAGES - 1>();         // this lane's copies of slab i have landed
+            const uint32_t slot = ring + (uint32_t)((i % GV_STAGES) * 2 * 32 * 16);
+            uint4 w0, w1;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w)
+                         : "r"(slot));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w1.x), "=r"(w1.y), "=r"(w1.z), "=r"(w1.w)
+                         : "r"(slot + 32 * 16));
+            mma_slab(w0, w1, (first + i * GV_WARPS) * SLAB + t * WK);
+        }
+        cp_async_wait<0>();
+        s_reg = first + nmine * GV_WARPS;
+    }
+    // register path: the remaining slabs (all of them without PIPE), the
+    // weight loads of GV_UNROLL slabs issued before their multiplies
+    for (long long s = s_reg; s < s1; s += (long long)GV_WARPS * GV_UNROLL) {
+        uint4 wv[GV_UNROLL][2];
+#pragma unroll
+        for (int u = 0; u < GV_UNROLL; ++u) {
+            const long long sl = s + (long long)u * GV_WARPS;     // warp-uniform
+            const long long k = sl * SLAB + t * WK;
+            if (sl < s1) {
+                wv[u][0] = load_w(wrow0, r0ok, k);
+                wv[u][1] = load_w(wrow1, r1ok, k);
+            } else {
+                wv[u][0] = wv[u][1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < GV_UNROLL; ++u) {
+            const long long sl = s + (long long)u * GV_WARPS;
+            if (sl >= s1) break;                                     // warp-uniform
+            mma_slab(wv[u][0], wv[u][1], sl * SLAB + t * WK);
+        }
+    }
+
+    // D fragment: acc[nt][e] is (W row g, X row nt*8 + 2t + e), acc[nt][2 + e]
+    // is (W row g + 8, same X row)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        red[warp][g][nt * 8 + 2 * t] = acc[nt][0];
+        red[warp][g][nt * 8 + 2 * t + 1] = acc[nt][1];
+        red[warp][g + 8][nt * 8 + 2 * t] = acc[nt][2];
+        red[warp][g + 8][nt * 8 + 2 * t + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    const int r = threadIdx.x & 15, c = threadIdx.x >> 4;      // W row r, X row c
+    float v = 0.0f;
+    if (c < COLS) {
+#pragma unroll
+        for (int w = 0; w < GV_WARPS; ++w) v += red[w][r][c];
+    }
+    if (KS > 1) {
+        // the cluster's K ranges, added in rank order by rank 0
+        if (c < COLS) sums[c][r] = v;
+        cluster_sync();
+        if (kr == 0 && c < COLS) {
+            const uint32_t off = smem_u32(&sums[c][r]);
+            float part[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < KS) part[q] = ld_shared_cluster_f32(mapa_shared(off, (uint32_t)q));
+            v = part[0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q)
+                if (q < KS) v += part[q];
+        }
+    }
+    const long long n = n0 + r;
+    if (kr == 0 && c < COLS && c < a.rows_x && n < a.rows_w) {
+        if (a.scale) v *= a.scale[n];
+        const long long off = (long long)c * a.c_sx + n * a.c_sw;
+        v = (a.beta != 0.0f) ? fmaf(a.beta, load_c(a.C, off, a.c_dtype), a.alpha * v) : a.alpha * v;
+        store_c1(a.C, off, v, a.c_dtype);
+    }
+    if (KS > 1) cluster_sync();      // peers keep their shared memory until rank 0 has read it
+}
+
+template <bool BF16, bool W8, int NT, bool PIPE>
+cudaError_t launch_one(const GemvArgs &a, cudaStream_t st)
+{
+    constexpr auto kern = gemv_kernel<BF16, W8, NT, PIPE>;
+    constexpr int smem = PIPE ? GV_RING : 0;
+    if constexpr (PIPE) {
+        static std::atomic<bool> configured[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!configured[dev].load(std::memory_order_acquire)) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            configured[dev].store(true, std::memory_order_release);
+        }
+    }
+    const long long blocks = ((long long)a.rows_w + 15) / 16 * a.ksplit;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (a.ksplit == 1) {
+        kern<<<(unsigned)blocks, GV_WARPS * 32, smem, st>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(GV_WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.ksplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t st)
+{
+    if (a.rows_x < 1 || a.rows_x > GEMV_MAX_ROWS || a.rows_w < 1 || a.K < 1) return cudaErrorInvalidValue;
+    if (a.ksplit != 1 && a.ksplit != 2 && a.ksplit != 4 && a.ksplit != 8) return cudaErrorInvalidValue;
+    const int nt = a.rows_x > 8 ? 2 : 1;
+    // the copy ring wants 16-byte aligned weight rows (base and row stride)
+    const int pipe = a.w_vec ? 1 : 0;
+    const int key = (a.x_bf16 ? 8 : 0) | (a.w_i8 ? 4 : 0) | (nt == 2 ? 2 : 0) | pipe;
+    switch (key) {
+    case 0: return launch_one<false, false, 1, false>(a, st);
+    case 1: return launch_one<false, false, 1, true>(a, st);
+    case 2: return launch_one<false, false, 2, false>(a, st);
+    case 3: return launch_one<false, false, 2, true>(a, st);
+    case 4: return launch_one<false, true, 1, false>(a, st);
+    case 5: return launch_one<false, true, 1, true>(a, st);
+    case 6: return launch_one<false, true, 2, false>(a, st);
+    case 7: return launch_one<false, true, 2, true>(a, st);
+    case 8: return launch_one<true, false, 1, false>(a, st);
+    case 9: return launch_one<true, false, 1, true>(a, st);
+    case 10: return launch_one<true, false, 2, false>(a, st);
+    case 11: return launch_one<true, false, 2, true>(a, st);
+    case 12: return launch_one<true, true, 1, false>(a, st);
+    case 13: return launch_one<true, true, 1, true>(a, st);
+    case 14: return launch_one<true, true, 2, false>(a, st);
+    default: return launch_one<true, true, 2, true>(a, st);
+    }
+}
+
+}  // namespace tc

@@ -104,6 +104,10 @@ struct MmaLaunch {
     int bn;
     int cg;      // CTAs per tile: 1, or 2 for a CTA pair (cluster of two)
     int i8acc;   // int8 slices summed in TMEM (BN = 128 only; args.slice_kb, col_scale)
+    // split-K inside one launch: the args.seg0_split K slices of a tile form
+    // one cluster and add their partial tiles through distributed shared
+    // memory (BN 64 or 128, one CTA per unit: grid == args.total_units)
+    int csplit;
     int grid;    // CTAs (a multiple of cg)
     CUtensorMap tmA, tmB, tmC, tmW;   // A, B, C and the split-K workspace
     MmaArgs args;
@@ -139,6 +143,9 @@ cudaError_t launch_mma_grouped(const MmaLaunch &L, const GroupTable &g, cudaStre
 // Largest number of CTA pairs of the BN-wide pair kernel that can be
 // resident at once on the current device (0 if the pair kernel cannot run).
 int max_active_pairs(int bn);
+// Largest number of S-CTA clusters of the BN-wide cluster-split kernel
+// resident at once on the current device (0 if such a cluster cannot run).
+int max_active_csplit_clusters(int bn, int S);
 
 // Split-K reduction: tiles [first_tile, first_tile + ntiles) each have S
 // fp32 partial tiles (rows_per_tile x bn, row-major) at
@@ -178,6 +185,29 @@ struct NoallocScratch {
 // once per device).
 cudaError_t noalloc_scratch(NoallocScratch *out);
 
+// Skinny products (gemv.cu): Out = alpha * (X W^T) (* scale[w row]) +
+// beta * Out_old for X with at most GEMV_MAX_ROWS rows.  X is [rows_x, K]
+// (f16 or bf16, row stride ldx elements), W is [rows_w, K] (X's type, or
+// int8 when w_i8; row stride ldw elements); the output element of (X row
+// i, W row j) is at C + i * c_sx + j * c_sw (elements of c_dtype).  K is
+// split across a cluster of ksplit CTAs (1, 2, 4 or 8) whose sums are added
+// in rank order.
+constexpr int GEMV_MAX_ROWS = 16;
+struct GemvArgs {
+    const void *X, *W;
+    void *C;
+    const float *scale;    // per W row, or null
+    int rows_x, rows_w;
+    long long K, ldx, ldw;
+    long long c_sx, c_sw;
+    int c_dtype;
+    float alpha, beta;
+    int x_vec, w_vec;      // 16-byte loads allowed: 16-byte aligned base and row stride
+    int w_i8, x_bf16;
+    int ksplit;
+};
+cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t st);
+
 // fp32 FFMA kernel (exact fp32, ascending-k fused multiply-add chain)
 struct FfmaArgs {
     int M, N, K;
@@ -206,12 +236,14 @@ struct SplitArgs {
 };
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t st);
 
-// int8 matrix (rows x cols, leading dimension ld_src) -> bf16 (exact) with
-// leading dimension ld_dst (a multiple of 64) and a 256-byte aligned base.
+// int8 matrix (rows x cols, leading dimension ld_src) -> bf16, or f16 when
+// to_f16 (both exact for int8), with leading dimension ld_dst (a multiple
+// of 64) and a 256-byte aligned base.
 struct WidenArgs {
     const int8_t *src;
     uint16_t *dst;
     long long rows, cols, ld_src, ld_dst;
+    int to_f16;
 };
 cudaError_t launch_widen(const WidenArgs &a, cudaStream_t st);
 

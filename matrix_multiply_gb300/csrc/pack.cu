@@ -148,7 +148,10 @@ __global__ void __launch_bounds__(256) widen_kernel(const WidenArgs a)
         const int n = (int)min(4LL, a.cols - c);
         uint16_t h[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) h[j] = j < n ? __bfloat16_as_ushort(__float2bfloat16_rn((float)__ldg(src + j))) : 0;
+        for (int j = 0; j < 4; ++j) {
+            const float x = j < n ? (float)__ldg(src + j) : 0.0f;
+            h[j] = a.to_f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
+        }
         if (n == 4) {
             *reinterpret_cast<uint2 *>(dst) = make_uint2(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16);
         } else {

@@ -216,6 +216,25 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// 16 bytes from the shared memory of a CTA of this cluster, given the
+// shared::cluster address mapa_shared returned for it
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 // arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {

@@ -430,6 +430,107 @@ __device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int
     }
 }
 
+// ---------------------------------------------------------------- cluster split-K
+
+// Rows of BN + 4 floats: with 16-byte stores by 32 lanes that each own one
+// row, every group of 8 lanes covers all 32 banks (row r starts at 16-byte
+// unit 33r, i.e. r mod 8 within a 128-byte line).
+template <int BN>
+__host__ __device__ constexpr int csplit_ld() { return BN + 4; }
+
+// The per-column scale (when present), alpha/beta (C_old read only when
+// beta != 0), then the fused bias and activation, then one rounding: four
+// consecutive columns of one row of C.
+template <bool EPI>
+__device__ __forceinline__ void finish4(const MmaArgs &a, int b, long long grow, long long gcol, float (&v)[4])
+{
+    const long long base = (long long)b * a.stride_c + grow * a.ldc + gcol;
+    const bool whole = a.c_vec_ok && gcol + 4 <= a.N;
+    if constexpr (EPI) {
+        if (a.col_scale) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] *= (gcol + j < a.N) ? a.col_scale[gcol + j] : 0.0f;
+        }
+    }
+    if (a.beta != 0.0f) {
+        float c[4];
+        if (whole && a.c_dtype == TC_F32) {
+            const float4 x = *reinterpret_cast<const float4 *>(static_cast<const float *>(a.C) + base);
+            c[0] = x.x, c[1] = x.y, c[2] = x.z, c[3] = x.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[j] = (gcol + j < a.N) ? load_c(a.C, base + j, a.c_dtype) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = fmaf(a.beta, c[j], a.alpha * v[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = a.alpha * v[j];
+    }
+    if constexpr (EPI) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (a.bias && gcol + j < a.N) v[j] += load_c(a.bias, gcol + j, a.c_dtype);
+            if (a.act == TC_ACT_GELU_TANH) v[j] = gelu_tanh(v[j]);
+        }
+    }
+    if (whole) {
+        if (a.c_dtype == TC_F32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(a.C) + base) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            uint2 w;
+            w.x = pack2(v[0], v[1], a.c_dtype);
+            w.y = pack2(v[2], v[3], a.c_dtype);
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.C) + base) = w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (gcol + j < a.N) store_c1(a.C, base + j, v[j], a.c_dtype);
+    }
+}
+
+// The K slices of one output tile run as one cluster of S CTAs (slice s on
+// the CTA of cluster rank s).  Each CTA has left its slice's fp32 partial
+// tile in its own shared memory (rows of csplit_ld<BN>() floats); here the
+// CTA of rank r sums rows [r * ceil(BM/S), ...) of all S partial tiles,
+// reading its peers' shared memory in slice order (deterministic), and
+// writes those rows of C.  Every thread of the CTA takes part.
+template <int BN, bool EPI>
+__device__ __forceinline__ void csplit_reduce(const MmaArgs &a, const uint8_t *partial)
+{
+    constexpr int LD = csplit_ld<BN>();
+    constexpr int G = BN / 4;                       // 16-byte groups per row
+    constexpr int SMAX = 16;
+    const int S = a.seg0_split;
+    const uint32_t rank = cluster_ctarank();
+    const int rows = (BM + S - 1) / S;
+    const int r0 = min(BM, (int)rank * rows), r1 = min(BM, r0 + rows);
+    const Unit w = decode_unit(a, (int)blockIdx.x);
+    const uint32_t base = smem_u32(partial);
+    for (int g = threadIdx.x; g < (r1 - r0) * G; g += blockDim.x) {
+        const int row = r0 + g / G, c4 = (g % G) * 4;
+        const long long grow = (long long)w.tm * BM + row, gcol = (long long)w.tn * BN + c4;
+        if (grow >= a.M || gcol >= a.N) continue;
+        const uint32_t off = base + (uint32_t)((row * LD + c4) * 4);
+        float4 p[SMAX];
+#pragma unroll
+        for (int q = 0; q < SMAX; ++q)
+            if (q < S) p[q] = ld_shared_cluster_f4(mapa_shared(off, (uint32_t)q));
+        float v[4] = {p[0].x, p[0].y, p[0].z, p[0].w};
+#pragma unroll
+        for (int q = 1; q < SMAX; ++q) {
+            if (q < S) {
+                v[0] += p[q].x;
+                v[1] += p[q].y;
+                v[2] += p[q].z;
+                v[3] += p[q].w;
+            }
+        }
+        finish4<EPI>(a, w.b, grow, gcol, v);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
 // CG = 1: one CTA computes a 128 x BN tile with tcgen05.mma.cta_group::1.
@@ -456,7 +557,13 @@ __device__ __forceinline__ void store_tma(const CUtensorMap *map, bool is3d, int
 // in a third TMEM region.  The split-K path writes each slice to memory and
 // adds them in a second kernel instead; the integer sums, their one rounding
 // and everything after are the same.
-template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false>
+//
+// CSPLIT: split-K inside one launch.  The grid holds one unit per CTA and
+// the S K slices of a tile form one cluster (slice = cluster rank); each
+// slice's partial tile stays in its CTA's shared memory and csplit_reduce
+// adds them across the cluster, so no partial tile goes through global
+// memory and no second kernel runs.
+template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false, bool CSPLIT = false>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -470,6 +577,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     constexpr int ACC_STRIDE = I8ACC ? BN : TCOLS / 2;   // TMEM columns between the two accumulators
     constexpr uint32_t RUN_COL = 2 * BN;           // I8ACC: the running int32 sums
     static_assert(!I8ACC || (EPI && !GROUPED && 3 * BN <= 512), "on-chip slices: two accumulators and the sums");
+    static_assert(!CSPLIT || (CG == 1 && !GROUPED && !I8ACC), "cluster split-K: one CTA per slice");
+    static_assert(!CSPLIT || BM * csplit_ld<BN>() * 4 <= S * STAGE, "the partial tile fits in the idle ring");
     constexpr int CHUNKS = BN / 32;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
     static_assert(BNL % 64 == 0 && BN <= 256, "each CTA's B share must be whole 64-column boxes");
@@ -857,6 +966,25 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                         emit(w.b, row, (long long)w.tn * BN + c * 32, v);
                     }
+                } else if constexpr (CSPLIT) {
+                    // K slice of a cluster split: the partial tile goes to this
+                    // CTA's shared memory.  The ring is idle: every copy into it
+                    // was consumed by an MMA, and every MMA has completed (this
+                    // accumulator's commit).  csplit_reduce adds the slices.
+                    float *red = reinterpret_cast<float *>(smem) + (warp * 32 + lane) * csplit_ld<BN>();
+#pragma unroll 1
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        uint32_t r[32];
+                        __syncwarp();
+                        tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        tmem_ld_wait();
+                        if (c == CHUNKS - 1) release();
+                        float4 *dst = reinterpret_cast<float4 *>(red + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    }
                 } else {
                     // K slice: the raw fp32 partial tile goes to its workspace
                     // slot (row-major, (BM * CG) x BN per unit); the reduction
@@ -888,7 +1016,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (CG == 2) cluster_sync();     // no CTA leaves while its peer may still signal it
+    if constexpr (CSPLIT) {
+        cluster_sync();              // every slice's partial tile is in its CTA's shared memory
+        csplit_reduce<BN, EPI>(args, smem);
+        cluster_sync();              // no CTA releases its shared memory while a peer may read it
+    } else if (CG == 2) {
+        cluster_sync();              // no CTA leaves while its peer may still signal it
+    }
     tc_fence_after();
     if (warp == 0) {
         if (CG == 1)
@@ -898,9 +1032,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
 }
 
-template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false>
+template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false, bool CSPLIT = false>
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
+    constexpr auto kern = mma_kernel<BN, CG, GROUPED, EPI, I8ACC, CSPLIT>;
     constexpr int smem = mma_smem_bytes(BN, CG);
     // per device: the kernel's shared-memory limit is raised once (callers
     // of the context-free entry point may race here from several threads;
@@ -910,17 +1045,20 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev].load(std::memory_order_acquire)) {
-        cudaError_t e =
-            cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        if (CG == 2) {
-            e = cudaFuncSetAttribute(mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (CG == 2 || CSPLIT) {
+            // cluster splits of up to 16 CTAs go beyond the portable 8
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, CSPLIT ? 1 : 0);
             if (e != cudaSuccess) return e;
         }
         configured[dev].store(true, std::memory_order_release);
     }
-    if (CG == 1) {
-        mma_kernel<BN, CG, GROUPED, EPI, I8ACC><<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+    const int cluster = CSPLIT ? L.args.seg0_split : CG;
+    if (CSPLIT && (cluster < 2 || cluster > 16 || L.grid != L.args.total_units || L.grid % cluster != 0))
+        return cudaErrorInvalidValue;
+    if (cluster == 1) {
+        kern<<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -930,12 +1068,43 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<BN, CG, GROUPED, EPI, I8ACC>, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+    return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+}
+
+// Clusters of S CTAs of the BN-wide cluster-split kernel that can be
+// resident at once on the current device (0 when such a cluster cannot run).
+template <int BN>
+int csplit_clusters_for(int S)
+{
+    constexpr auto kern = mma_kernel<BN, 1, false, false, false, true>;
+    constexpr int smem = mma_smem_bytes(BN, 1);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S, 1, 1);
+    cfg.blockDim = dim3(MMA_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 template <int BN>
@@ -1045,6 +1214,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
     } else {
 #pragma unroll
         for (int j = 0; j < COLS; ++j) v[j] = acc[j];
+        if (r.col_scale) {
+            // a per-column scale on float slices (the int8-weight product)
+#pragma unroll
+            for (int j = 0; j < COLS; ++j)
+                if (gcol + j < r.N) v[j] *= r.col_scale[gcol + j];
+        }
     }
     const long long base = (long long)b * r.stride_c + grow * r.ldc + gcol;
 #pragma unroll
@@ -1108,6 +1283,16 @@ cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st)
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
     const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE || L.args.col_scale != nullptr;
+    if (L.csplit) {
+        if (L.cg != 1 || L.i8acc) return cudaErrorInvalidValue;
+        switch (L.bn) {
+        case 64: return epi ? launch_kernel<64, 1, false, true, false, true>(L, st)
+                            : launch_kernel<64, 1, false, false, false, true>(L, st);
+        case 128: return epi ? launch_kernel<128, 1, false, true, false, true>(L, st)
+                             : launch_kernel<128, 1, false, false, false, true>(L, st);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (L.i8acc) {
         if (L.bn != 128 || L.args.slice_kb < 1 || L.args.col_scale == nullptr) return cudaErrorInvalidValue;
         return L.cg == 2 ? launch_kernel<128, 2, false, true, true>(L, st) : launch_kernel<128, 1, false, true, true>(L, st);
@@ -1167,6 +1352,16 @@ cudaError_t noalloc_scratch(NoallocScratch *out)
     out->partials = reinterpret_cast<float *>(base);
     out->status = reinterpret_cast<unsigned *>(base + NOALLOC_PARTIAL_BYTES);
     return cudaSuccess;
+}
+
+int max_active_csplit_clusters(int bn, int S)
+{
+    if (S < 2 || S > 16) return 0;
+    switch (bn) {
+    case 64: return csplit_clusters_for<64>(S);
+    case 128: return csplit_clusters_for<128>(S);
+    default: return 0;
+    }
 }
 
 int max_active_pairs(int bn)

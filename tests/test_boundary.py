@@ -154,10 +154,31 @@ def test_plan_tensor_core_shapes():
 
 
 def test_plan_split_k_for_tall_k():
+    # the slices of a tile form one cluster (at most 16 CTAs) and are reduced
+    # on chip; 64-wide tiles give 8 tiles x 16 slices = 128 CTAs, each with
+    # fewer operand bytes to load than 4 128-wide tiles x 16 slices
     p = plan(256, 256, 16384, "bf16", "f32", ta=True)
-    assert "_splitk" in p and p.startswith("tcgen05_tn_bf16_f32_128x128")
-    s = int(p.rsplit("_s", 1)[1])
+    assert p == "tcgen05_tn_bf16_f32_128x64_csplit_s16"
+    # without the cluster reduction: 128-wide tiles, as many slices as fill the SMs
+    q = plan_forced("csplit=0", 256, 256, 16384, "bf16", "f32", ta=True)
+    assert "_splitk" in q and q.startswith("tcgen05_tn_bf16_f32_128x128")
+    s = int(q.rsplit("_s", 1)[1])
     assert 2 <= s <= 152 // 4
+    # a forced split longer than a cluster goes through memory
+    assert "_splitk_s20" in plan_forced("split=20", 256, 256, 16384, "bf16", "f32", ta=True)
+    assert plan_forced("split=5 bn=128", 256, 256, 16384, "bf16", "f32", ta=True).endswith("128x128_csplit_s5")
+
+
+def plan_forced(spec, *args, **kw):
+    old = os.environ.get("TC_FORCE_VARIANT")
+    os.environ["TC_FORCE_VARIANT"] = spec
+    try:
+        return plan(*args, **kw)
+    finally:
+        if old is None:
+            del os.environ["TC_FORCE_VARIANT"]
+        else:
+            os.environ["TC_FORCE_VARIANT"] = old
 
 
 def test_plan_small_split_gives_way_to_64_wide_tiles():
@@ -165,8 +186,8 @@ def test_plan_small_split_gives_way_to_64_wide_tiles():
     # its reduction; a long K keeps the split, and too few 64-wide tiles
     # (the skinny shapes) keep it too
     assert plan(1024, 1024, 1024, "f16", "f16") == "tcgen05_nn_f16_f16_128x64"
-    assert plan(1024, 1024, 8192, "f16", "f16") == "tcgen05_nn_f16_f16_128x128_splitk_s2"
-    assert plan(1, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_splitk")
+    assert plan(1024, 1024, 8192, "f16", "f16") == "tcgen05_nn_f16_f16_128x128_csplit_s2"
+    assert plan_forced("gemv=0", 1, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_csplit")
 
 
 def test_plan_tail_split():
@@ -206,9 +227,40 @@ def test_epilogue_validation():
 
 
 def test_plan_skinny_products():
-    """M or N <= 8 stay on the tensor-core kernel (split-K when the tiles are
-    few); fp32 stays on the exact path."""
-    assert plan(4, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_splitk")
-    assert plan(1, 32000, 4096, "bf16", "bf16", tb=True).startswith("tcgen05_nt_bf16_bf16_128x")
+    """At most 16 rows on one side of an NT product: the skinny-product
+    kernel (K split over a cluster while there are fewer than two CTAs per
+    SM); other layouts stay on the tensor-core kernel; fp32 on the exact
+    path."""
+    assert plan(4, 11008, 4096, "f16", "f16", tb=True) == "gemv_nt_f16_f16_x4_ks1"
+    assert plan(1, 4096, 4096, "f16", "f16", tb=True) == "gemv_nt_f16_f16_x1_ks2"
+    assert plan(4096, 3, 4096, "bf16", "f32", tb=True) == "gemv_nt_bf16_f32_x3_ks2_swap"
+    assert plan(16, 64, 100000, "bf16", "bf16", tb=True) == "gemv_nt_bf16_bf16_x16_ks8"
+    assert plan(17, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_")
+    assert plan_forced("gemv=0", 4, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_csplit")
+    assert plan(1, 32000, 4096, "bf16", "bf16").startswith("tcgen05_nn_bf16_bf16_128x")
     assert plan(4096, 3, 4096, "bf16", "f32").startswith("tcgen05_nn_bf16_f32_128x")
     assert plan(4, 256, 256, "f32", "f32").startswith("ffma_")
+
+
+def test_q8_weight_validation():
+    """The int8-weight product's own checks, host-only."""
+    def q8(**kw):
+        base = dict(M=4, N=32, K=64, a="f16", c="f16", b="i8", ta=False, tb=True)
+        base.update(kw)
+        return tg.make_desc(base["M"], base["N"], base["K"], base["a"], base["c"], b_dtype=base["b"],
+                            transpose_a=base["ta"], transpose_b=base["tb"])
+    v = tg.tc_gemm_q8_weight_validate
+    assert v(q8()) == tg.TC_OK
+    assert v(q8(a="bf16", c="f32")) == tg.TC_OK
+    assert v(q8(tb=False)) == tg.TC_ERR_LAYOUT
+    assert v(q8(ta=True)) == tg.TC_ERR_LAYOUT
+    assert v(q8(b="f16")) == tg.TC_ERR_DTYPE
+    assert v(q8(a="f32", c="f32")) == tg.TC_ERR_DTYPE
+    assert v(q8(a="f16", c="bf16")) == tg.TC_ERR_DTYPE
+    assert v(q8(M=0)) == tg.TC_ERR_DIM
+    assert v(q8(), scale=0) == tg.TC_ERR_NULL
+    # W's byte range is counted in int8 elements: C right after W's 32 x 64 bytes is fine
+    assert v(q8(), W=1 << 30, C=(1 << 30) + 32 * 64) == tg.TC_OK
+    assert v(q8(), W=1 << 30, C=(1 << 30) + 32 * 64 - 1) == tg.TC_ERR_OVERLAP
+    # the scale must not overlap C (4 x 32 f16 at 3 << 40)
+    assert v(q8(), scale=(3 << 40) + 16) == tg.TC_ERR_OVERLAP

@@ -82,13 +82,15 @@ def test_epilogue_parity(ctx, activation, ab, c, ta, tb, shape):
     assert ctx.last_kernel.endswith(want), ctx.last_kernel
 
 
-@pytest.mark.parametrize("spec", ["", "cg=2", "cg=1 bn=64", "bn=192", "bn=128 split=3", "bn=256 split=5",
+@pytest.mark.parametrize("spec", ["", "cg=2", "cg=1 bn=64", "bn=192", "bn=128 split=3", "bn=128 split=3 csplit=0",
+                                  "bn=64 split=16", "bn=256 split=5",
                                   "sms=5 tail=2", "cg=2 sms=6 tail=2", "store=direct", "pack=1",
                                   "pack=1 split=4", "cg=2 bn=128"])
 @pytest.mark.parametrize("c", ["bf16", "f32"])
 def test_epilogue_every_variant(ctx, force, spec, c):
     """The epilogue in the tensor-core kernel's own store paths (TMA, plain,
-    staged) and in the split-K reduction kernel."""
+    staged), in the on-chip reduction of a cluster split and in the split-K
+    reduction kernel."""
     force(spec)
     p = synthetic.make_problem(333, 470, 1100, "bf16", c, transpose_b=True, alpha=-0.5, beta=1.0, seed=41,
                                dist="normal", c_fill="uniform")
@@ -110,7 +112,7 @@ def test_epilogue_unaligned_c_and_bias(ctx):
 def test_bias_only_integer_exact(ctx, force):
     """No activation, integer data and an integer bias: every value is an
     integer below 2^24, so the result is exact in fp32 on every path."""
-    for spec in ["", "bn=128 split=4", "sms=5 tail=3", "store=direct"]:
+    for spec in ["", "bn=128 split=4", "bn=128 split=4 csplit=0", "sms=5 tail=3", "store=direct"]:
         force(spec)
         p = synthetic.make_problem(200, 136, 1024, "bf16", "f32", alpha=1.0, beta=1.0, seed=45, dist="int",
                                    scale=4.0, c_fill="int")
@@ -135,7 +137,7 @@ def test_gelu_without_bias_and_no_op_epilogue(ctx):
 
 
 def test_epilogue_deterministic(ctx, force):
-    for spec in ["", "bn=128 split=6"]:
+    for spec in ["", "bn=128 split=6", "bn=128 split=6 csplit=0"]:
         force(spec)
         p = synthetic.make_problem(384, 512, 2048, "bf16", "f32", seed=47, dist="normal")
         bias = make_bias(512, "f32", seed=48)

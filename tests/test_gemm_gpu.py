@@ -83,7 +83,11 @@ SHAPES = [(1, 1, 1), (5, 7, 3), (128, 256, 64), (300, 200, 333), (257, 385, 130)
 @pytest.mark.parametrize("ab,c", DT_PAIRS)
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 @pytest.mark.parametrize("shape", SHAPES)
-def test_tensor_core_parity(ctx, ab, c, ta, tb, shape):
+def test_tensor_core_parity(ctx, force, ab, c, ta, tb, shape):
+    """Every layout on the tensor-core kernel (NT products with at most 16
+    rows on one side would otherwise take the skinny-product kernel, which
+    tests/test_skinny_gpu.py covers)."""
+    force("gemv=0")
     M, N, K = shape
     p = synthetic.make_problem(M, N, K, ab, c, transpose_a=ta, transpose_b=tb, seed=M * 7 + K,
                                dist="normal")
@@ -120,6 +124,7 @@ def test_alpha_beta(ctx, alpha, beta, c):
 
 
 @pytest.mark.parametrize("spec", ["bn=64", "bn=128", "bn=192", "bn=256", "bn=128 split=3",
+                                  "bn=128 split=3 csplit=0", "bn=64 split=16 csplit=0",
                                   "bn=256 split=7", "bn=64 split=16", "pack=1", "pack=1 split=5",
                                   "grid=3", "group_m=1", "group_m=3 bn=64", "sms=5 tail=2",
                                   "sms=5 tail=3 bn=64", "sms=7 bn=256 tail=2 pack=1", "cg=2",
@@ -131,6 +136,49 @@ def test_forced_variants(ctx, force, spec, ta, tb):
     p = synthetic.make_problem(333, 470, 1100, "f16", "f32", transpose_a=ta, transpose_b=tb,
                                alpha=0.75, beta=-1.0, seed=23, dist="normal", c_fill="uniform")
     check_full(ctx, p, spec)
+
+
+# ----------------------------------------------------- cluster split-K
+
+CSPLIT_SPECS = ["bn=128 split=2", "bn=128 split=3", "bn=64 split=5", "bn=128 split=8", "bn=64 split=16",
+                "bn=128 split=16"]
+
+
+@pytest.mark.parametrize("spec", CSPLIT_SPECS)
+@pytest.mark.parametrize("ta,tb", LAYOUTS)
+def test_cluster_split_equals_memory_split_bitwise(ctx, force, spec, ta, tb):
+    """The K slices of a tile reduced on chip by their cluster are the same
+    slices, added in the same order, as the partial tiles the reduction
+    kernel adds from memory: the two results are equal bit for bit, and
+    within the parity bound.  M and N end inside a tile; beta != 0."""
+    p = synthetic.make_problem(333, 200, 3000, "bf16", "f32", transpose_a=ta, transpose_b=tb, alpha=0.75,
+                               beta=-0.5, seed=131, dist="normal", c_fill="uniform")
+    force(spec + " csplit=0")
+    ref = run_problem(ctx, p)
+    assert "_splitk" in ctx.last_kernel, ctx.last_kernel
+    force(spec)
+    got = run_problem(ctx, p)
+    assert "_csplit" in ctx.last_kernel, ctx.last_kernel
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), ctx.last_kernel
+    R, T = oracle.gemm(p)
+    parity.check(oracle.decode(got), R, T, "f32", what=f"{spec} {ctx.last_kernel}")
+
+
+@pytest.mark.parametrize("ab,c", DT_PAIRS)
+@pytest.mark.parametrize("ldc_pad", [0, 3])
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_cluster_split_outputs(ctx, force, ab, c, ldc_pad, beta):
+    """Every output type of the on-chip reduction: 16-byte / 8-byte stores of
+    whole column groups, element stores at the ragged right edge and when
+    C's rows are not 16-byte multiples (ldc = N + 3), C_old read or not."""
+    force("bn=64 split=7")
+    N = 190
+    p = synthetic.make_problem(250, N, 2500, ab, c, alpha=1.25, beta=beta, seed=137, dist="normal",
+                               c_fill="uniform", ldc=N + ldc_pad if ldc_pad else 0)
+    out = run_problem(ctx, p, ldc=N + ldc_pad if ldc_pad else 0)
+    assert "_csplit" in ctx.last_kernel and ctx.last_kernel.endswith("_s7"), ctx.last_kernel
+    R, T = oracle.gemm(p)
+    parity.check(oracle.decode(out)[:, :N], R, T, c, what=f"{ctx.last_kernel}")
 
 
 def test_padded_leading_dimensions(ctx):
@@ -150,7 +198,8 @@ def test_padded_leading_dimensions(ctx):
 
 # ----------------------------------------------------- exactness and edges
 
-@pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "pack=1 bn=256 split=2",
+@pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "bn=128 split=4 csplit=0",
+                                  "bn=64 split=16", "pack=1 bn=256 split=2",
                                   "sms=5 tail=3", "cg=2", "cg=2 bn=128 sms=4 tail=2", "store=direct"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
@@ -211,10 +260,11 @@ def test_short_a_copies_bitwise(ctx, force, M, ta, tb, spec):
     that of full 128-row copies bit for bit."""
     p = synthetic.make_problem(M, 700, 2100, "bf16", "f32", transpose_a=ta, transpose_b=tb, alpha=0.75, beta=0.5,
                                seed=M + 95, dist="normal", c_fill="uniform")
-    force((spec + " shorta=0").strip())
+    force(spec + " shorta=0 gemv=0")
     ref = run_problem(ctx, p)
-    force(spec)
+    force(spec + " gemv=0")
     got = run_problem(ctx, p)
+    assert ctx.last_kernel.startswith("tcgen05_"), ctx.last_kernel
     assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), ctx.last_kernel
     R, T = oracle.gemm(p)
     parity.check(oracle.decode(got), R, T, "f32", what=f"{spec} M={M} {ctx.last_kernel}")
@@ -262,7 +312,8 @@ def test_identity_and_permutation(ctx):
     assert torch.equal(out, p.B.float()[perm])
 
 
-@pytest.mark.parametrize("spec", ["", "bn=128 split=6", "sms=9 tail=2", "cg=2 sms=8 tail=2"])
+@pytest.mark.parametrize("spec", ["", "bn=128 split=6", "bn=128 split=6 csplit=0", "bn=64 split=16",
+                                  "sms=9 tail=2", "cg=2 sms=8 tail=2"])
 def test_determinism(ctx, force, spec):
     force(spec)
     p = synthetic.make_problem(384, 512, 4096, "bf16", "f32", transpose_a=True, seed=53, dist="normal")
@@ -500,9 +551,12 @@ def test_bf16_tn_nt_4096x8192(ctx, layout):
     check_sampled(ctx, synthetic.bf16_tn_nt_4096x8192(layout), what=f"bf16 {layout} 4096x4096x8192")
 
 
-def test_bf16_tn_splitk_256x16384(ctx):
+def test_bf16_tn_splitk_256x16384(ctx, force):
     check_full(ctx, synthetic.bf16_tn_splitk_256x16384(), "bf16 TN split-K 256x256x16384")
-    assert "splitk" in ctx.last_kernel
+    assert "_csplit_s" in ctx.last_kernel, ctx.last_kernel
+    force("csplit=0")
+    check_full(ctx, synthetic.bf16_tn_splitk_256x16384(), "bf16 TN split-K 256x256x16384 through memory")
+    assert "_splitk" in ctx.last_kernel, ctx.last_kernel
 
 
 def test_fp16_nn_narrow_8192x384(ctx):

@@ -1,10 +1,12 @@
-"""Skinny products -- GEMMs with M <= 8 or N <= 8, the decode-time GEMV
-shape of the tensorcore gemm.md page ("M <= 4 GEMV") -- against the CPU
-oracle on GB300, under the GEMM bound of tests/parity.py (1e-4 * sum|ab|
-plus one output ulp), bitwise on integer data, and the fused epilogue under
-tests/parity.bound_epilogue.  They run on the tensor-core kernel (M or N
-padded inside a 128-row tile by TMA zero fill, split-K when the tiles are
-few): a dedicated CUDA-core GEMV kernel measured no faster on GB300."""
+"""Skinny products -- GEMMs with at most 16 rows on one side, the
+decode-time GEMV shape of the tensorcore gemm.md page ("M <= 4 GEMV") --
+against the CPU oracle on GB300, under the GEMM bound of tests/parity.py
+(1e-4 * sum|ab| plus one output ulp), bitwise on integer data, and the fused
+epilogue under tests/parity.bound_epilogue.  NT products (both operands
+K-contiguous) run on the skinny-product kernel, which streams the larger
+operand once; every other layout, the fused epilogue and batches run on the
+tensor-core kernel (the short side padded inside a 128-row tile by TMA zero
+fill, split-K when the tiles are few), which gemv=0 also forces for NT."""
 from __future__ import annotations
 
 import numpy as np
@@ -64,10 +66,12 @@ SHAPES = [(1, 1000, 77), (3, 4097, 3000), (8, 300, 1), (8, 2050, 9001), (4000, 5
           (1, 1, 1), (6, 7, 33)]
 
 
+@pytest.mark.parametrize("spec", ["", "gemv=0"])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("ab,c", DT_PAIRS)
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
-def test_skinny_parity(ctx, shape, ab, c, ta, tb):
+def test_skinny_parity(ctx, force, spec, shape, ab, c, ta, tb):
+    force(spec)
     M, N, K = shape
     p = synthetic.make_problem(M, N, K, ab, c, transpose_a=ta, transpose_b=tb, alpha=0.75, beta=0.5,
                                seed=M + 7 * N + K, dist="normal", c_fill="uniform")
@@ -150,3 +154,34 @@ def test_skinny_fused_epilogue(ctx, shape):
 def test_decode_shapes(ctx, shape):
     p = synthetic.f16_decode(*shape)
     check(ctx, p, f"decode {shape}")
+    assert ctx.last_kernel.startswith("gemv_nt_f16_f16_x"), ctx.last_kernel
+
+
+@pytest.mark.parametrize("M", list(range(1, 18)))
+@pytest.mark.parametrize("ab", ["f16", "bf16"])
+def test_gemv_every_row_count(ctx, M, ab):
+    """1 to 16 rows of X (one or two 8-row MMA column tiles, rows beyond M
+    zero), and 17, which goes to the tensor cores; the transposed product
+    (few columns) takes the same kernel with the roles swapped."""
+    p = synthetic.make_problem(M, 300, 2000, ab, "f32", transpose_b=True, alpha=0.5, beta=1.0, seed=M + 90,
+                               dist="normal", c_fill="uniform")
+    check(ctx, p, f"M={M}")
+    assert ctx.last_kernel.startswith("gemv_" if M <= 16 else "tcgen05_"), ctx.last_kernel
+    q = synthetic.make_problem(300, M, 2000, ab, ab, transpose_b=True, seed=M + 91, dist="normal")
+    check(ctx, q, f"N={M}")
+    if M <= 16:
+        assert ctx.last_kernel.endswith("_swap"), ctx.last_kernel
+
+
+@pytest.mark.parametrize("ks", [1, 2, 4, 8])
+def test_gemv_k_split_integer_bitwise(ctx, force, ks):
+    """K cut over a cluster of 1 to 8 CTAs (sums added in rank order):
+    integer data give the exact result whatever the cut."""
+    force(f"gemv_ks={ks}")
+    for (M, N, K) in [(4, 1000, 4096), (16, 33, 9001), (1, 5, 17)]:
+        p = synthetic.make_problem(M, N, K, "f16", "f32", transpose_b=True, beta=1.0, seed=K + ks, dist="int",
+                                   scale=4.0, c_fill="int")
+        out = run(ctx, p)
+        assert ctx.last_kernel.endswith(f"_ks{ks}"), ctx.last_kernel
+        R, _ = oracle.gemm(p)
+        assert np.array_equal(out.numpy().astype(np.float64), R), (M, N, K, ctx.last_kernel)
