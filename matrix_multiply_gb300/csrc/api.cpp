@@ -36,6 +36,11 @@ struct tc_stream {
     size_t rx_cap = 0;
     unsigned *status_host = nullptr; // mapped, pinned: kernels report timeouts here
     unsigned *status_dev = nullptr;
+    // skinny-product kernel: per-block arrival counts (zeroed when allocated)
+    // and the epoch that tags this stream's launches
+    unsigned *gv_ticket = nullptr;
+    size_t gv_ticket_cap = 0;
+    unsigned gv_epoch = 0;
 };
 
 struct tc_ctx {
@@ -194,7 +199,9 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // when A has fewer) csplit=0 (split-K slices go through global memory and
 // the reduction kernel instead of a cluster reduction on chip) gemv=0 (a
 // product with at most 16 rows on one side stays on the tensor-core kernel)
-// gemv_ks=<1|2|4|8> (the skinny-product kernel's K split).
+// gemv_ks=<1..8> (the skinny-product kernel's K split) gemv_tma=1 (its
+// bulk-copy ring instead of the register / cp.async form) pf=<d> (the
+// tensor-core producer prefetches A into L2 d K blocks ahead).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -207,7 +214,8 @@ struct Force {
     int no_short_a = 0;
     int i8acc = -1;
     int csplit = -1;
-    int gemv = -1, gemv_ks = 0;
+    int gemv = -1, gemv_ks = 0, gemv_tma = -1;
+    int pf = -1;
 };
 
 Force read_force()
@@ -246,6 +254,8 @@ Force read_force()
         else if (k == "csplit") f.csplit = std::atoi(v.c_str());
         else if (k == "gemv") f.gemv = std::atoi(v.c_str());
         else if (k == "gemv_ks") f.gemv_ks = std::atoi(v.c_str());
+        else if (k == "gemv_tma") f.gemv_tma = std::atoi(v.c_str());
+        else if (k == "pf") f.pf = std::atoi(v.c_str());
     }
     return f;
 }
@@ -299,6 +309,13 @@ Sched schedule(int64_t tiles, int64_t num_kb, int num_sms, int cg, int bn, int f
     return s;
 }
 
+int pow2_floor(int x)
+{
+    int p = 1;
+    while (p * 2 <= x) p *= 2;
+    return p;
+}
+
 // K split of the skinny-product kernel: clusters of up to 8 CTAs along K
 // until there are at least two CTAs per SM, keeping at least 32 K steps
 // (4 per warp) per CTA.
@@ -309,6 +326,44 @@ int gemv_ksplit(int64_t rows_w, int64_t K, bool w_i8, int num_sms)
     int ks = 1;
     while (ks < 8 && blocks * ks < 2LL * num_sms && steps / (2LL * ks) >= 32) ks *= 2;
     return ks;
+}
+
+// The bulk-copy form of the skinny-product kernel, when every row of X and
+// W starts on a 16-byte boundary and K is a whole number of 16-byte pieces
+// of W: K values per stage, ring depth within the shared-memory budget, and
+// K slices per 16-row block so that the (block, slice) units spread evenly
+// over one persistent CTA per SM.  Returns false when the form does not apply.
+bool plan_gemv_tma(GemvArgs &g, int num_sms, int force_ks)
+{
+    const int wsz = g.w_i8 ? 1 : 2;
+    if (!g.x_vec || !g.w_vec || (g.K * wsz) % 16 != 0 || (g.K * 2) % 16 != 0) return false;
+    const int cols = g.rows_x > 8 ? 16 : 8;
+    g.kc = g.w_i8 ? 1024 : 512;
+    const int stage = 16 * gt_wpitch(g.kc, wsz) + cols * gt_xpitch(g.kc);
+    g.stages = std::min<int>(GT_MAX_STAGES, (SMEM_LIMIT - gt_ring_off(cols)) / stage);
+    if (g.stages < 2) return false;
+    g.nrb = (int)cdiv(g.rows_w, 16);
+    const int64_t nchunk = cdiv(g.K, g.kc);
+    int best = 1;
+    if (force_ks > 0) {
+        best = (int)std::min<int64_t>(force_ks, nchunk);
+    } else {
+        double best_waste = 1e300;
+        for (int ks = 1; ks <= 8 && ks <= nchunk; ++ks) {
+            const double units = (double)g.nrb * ks, per = units / num_sms;
+            const double waste = std::ceil(per) / per;
+            if (waste < best_waste - 0.03) {
+                best_waste = waste;
+                best = ks;
+            }
+        }
+    }
+    g.kslices = std::max(best, 1);
+    g.units = g.nrb * g.kslices;
+    g.grid = std::min(g.units, num_sms);
+    g.tma = 1;
+    g.ksplit = 1;
+    return true;
 }
 
 // allow_gemv: the call may take the skinny-product kernel (a plain GEMM:
@@ -349,9 +404,8 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
         p.gemv = true;
         p.gemv_swap = d->M > GEMV_MAX_ROWS;
         const int64_t rows_w = p.gemv_swap ? d->M : d->N, rows_x = p.gemv_swap ? d->N : d->M;
-        p.gemv_ks = f.gemv_ks > 0 ? f.gemv_ks : gemv_ksplit(rows_w, d->K, false, num_sms);
-        std::snprintf(buf, sizeof buf, "gemv_%s_%s_%s_x%d_ks%d%s", lay, dt, ct, (int)rows_x, p.gemv_ks,
-                      p.gemv_swap ? "_swap" : "");
+        p.gemv_ks = f.gemv_ks > 0 ? pow2_floor(std::min(f.gemv_ks, 8)) : gemv_ksplit(rows_w, d->K, false, num_sms);
+        std::snprintf(buf, sizeof buf, "gemv_%s_%s_%s_x%d%s", lay, dt, ct, (int)rows_x, p.gemv_swap ? "_swap" : "");
         p.name = buf;
         *out = p;
         return TC_OK;
@@ -559,6 +613,45 @@ tc_status_t read_status(tc_stream *s)
 // bias/activation epilogue, or null).
 // col_scale: the int8 path's per-column dequantisation (its K slices then
 // hold integers and are added as such), or null.
+// Launch the skinny-product kernel on stream s: the bulk-copy form when it
+// applies (its slice sums in the stream's workspace, its arrival counts in
+// the stream's zeroed count buffer, a fresh epoch), else the register form.
+tc_status_t enqueue_gemv(tc_ctx *ctx, tc_stream *s, GemvArgs &g, const Force &f, std::string &name)
+{
+    char buf[48];
+    if (f.gemv_tma == 1 && plan_gemv_tma(g, ctx->num_sms, f.gemv_ks)) {
+        if (g.kslices > 1) {
+            tc_status_t st = ensure_ws(s, (size_t)g.nrb * g.kslices * 256 * sizeof(float) + 256);
+            if (st != TC_OK) return st;
+            g.part = static_cast<float *>(s->ws);
+        }
+        const size_t tbytes = (size_t)g.nrb * sizeof(unsigned);
+        if (tbytes > s->gv_ticket_cap) {
+            const size_t cap = round_up(tbytes + tbytes / 2, 4096);
+            if (s->gv_ticket) cudaFreeAsync(s->gv_ticket, s->st);
+            s->gv_ticket = nullptr;
+            s->gv_ticket_cap = 0;
+            if (cudaMallocAsync(reinterpret_cast<void **>(&s->gv_ticket), cap, s->st) != cudaSuccess ||
+                cudaMemsetAsync(s->gv_ticket, 0, cap, s->st) != cudaSuccess)
+                return TC_ERR_CUDA;
+            s->gv_ticket_cap = cap;
+        }
+        g.ticket = s->gv_ticket;
+        s->gv_epoch = s->gv_epoch % 0xFFFFFFu + 1u;      // 1 .. 2^24 - 1
+        g.epoch = s->gv_epoch;
+        g.status = s->status_dev;
+        g.timeout_ns = 4000000000ull + (unsigned long long)cdiv(g.K, g.kc) * 20000ull;
+        std::snprintf(buf, sizeof buf, "_tma_s%d_ks%d", g.stages, g.kslices);
+    } else {
+        g.tma = 0;
+        std::snprintf(buf, sizeof buf, "_ks%d", g.ksplit);
+    }
+    if (launch_gemv(g, s->st) != cudaSuccess) return TC_ERR_CUDA;
+    ctx->launches += 1;
+    name += buf;
+    return TC_OK;
+}
+
 // int_slices: the int8 path -- K slices hold exact integers and are added
 // as integers (through memory only, never a cluster split).
 tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Plan &plan, const void *A,
@@ -588,9 +681,10 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         g.w_i8 = 0;
         g.x_bf16 = d->a_dtype == TC_BF16;
         g.ksplit = p.gemv_ks;
-        if (launch_gemv(g, s->st) != cudaSuccess) return TC_ERR_CUDA;
-        ctx->launches += 1;
-        ctx->last = p.name;
+        std::string name = p.name;
+        const tc_status_t st = enqueue_gemv(ctx, s, g, read_force(), name);
+        if (st != TC_OK) return st;
+        ctx->last = name;
         return TC_OK;
     }
     if (p.csplit) {
@@ -745,6 +839,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         const Force f = read_force();
         if (f.debug_timeout_ms > 0) a.timeout_ns = (unsigned long long)f.debug_timeout_ms * 1000000ull;
         a.debug_drop_tfull = f.debug_drop;
+        a.pf_dist = f.pf > 0 ? f.pf : 0;
     }
 
     const int64_t lda_use = p.pack_a ? lda_p : n.lda;
@@ -1247,13 +1342,13 @@ tc_status_t run_q8w(tc_ctx *ctx, const tc_gemm_desc *d, const float *scale, cons
         g.w_vec = aligned16(W) && n.ldb % 16 == 0;
         g.w_i8 = 1;
         g.x_bf16 = d->a_dtype == TC_BF16;
-        g.ksplit = f.gemv_ks > 0 ? f.gemv_ks : gemv_ksplit(d->N, d->K, true, ctx->num_sms);
-        std::snprintf(buf, sizeof buf, "gemv_q8w_nt_%s_%s_x%d_ks%d", dt, ct, (int)d->M, g.ksplit);
+        g.ksplit = f.gemv_ks > 0 ? pow2_floor(std::min(f.gemv_ks, 8)) : gemv_ksplit(d->N, d->K, true, ctx->num_sms);
+        std::snprintf(buf, sizeof buf, "gemv_q8w_nt_%s_%s_x%d", dt, ct, (int)d->M);
+        std::string name = buf;
         std::lock_guard<std::mutex> lk(ctx->mu);
         if (cudaSetDevice(ctx->device) != cudaSuccess) return TC_ERR_CUDA;
-        if (launch_gemv(g, s->st) != cudaSuccess) return TC_ERR_CUDA;
-        ctx->launches += 1;
-        ctx->last = buf;
+        if ((st = enqueue_gemv(ctx, s, g, f, name)) != TC_OK) return st;
+        ctx->last = name;
         return TC_OK;
     }
     // W [N, K] int8 -> the activations' type, rows padded to 64 elements
@@ -1299,6 +1394,7 @@ void stream_free(tc_stream *s)
     if (s->st) cudaStreamSynchronize(s->st);
     if (s->ws) cudaFree(s->ws);
     if (s->rx) cudaFree(s->rx);
+    if (s->gv_ticket) cudaFree(s->gv_ticket);
     if (s->status_host) cudaFreeHost(s->status_host);
     if (s->owned && s->st) cudaStreamDestroy(s->st);
     delete s;

@@ -144,6 +144,150 @@ __global__ void __launch_bounds__(256) ffma_kernel(const FfmaArgs a)
     }
 }
 
+// Large problems: 128 x 128 tiles, 256 threads, 8 x 8 outputs per thread as
+// a 2 x 2 grid of 4 x 4 blocks (rows 4ty.. and 64 + 4ty.., columns 4tx..
+// and 64 + 4tx..), so that every shared-memory read is one 16-byte load
+// that 16 lanes share (A) or that covers 256 contiguous bytes (B).  The
+// layouts are template parameters (no per-element branches); K steps of 16
+// are fully unrolled; the next K block is loaded into registers (16-byte
+// loads when VEC: aligned bases and leading dimensions that are multiples
+// of 4) while the current one is multiplied.  Per output it is still one
+// fmaf chain in ascending k (zero-filled operands past K add exact zeros).
+template <bool TA, bool TB, bool VEC>
+__global__ void __launch_bounds__(256, 2) ffma128_kernel(const FfmaArgs a)
+{
+    constexpr int BM = 128, BN = 128, BK = 16, LDS = 132;    // 528-byte rows keep 16-byte alignment
+    __shared__ __align__(16) float As[2][BK][LDS];
+    __shared__ __align__(16) float Bs[2][BK][LDS];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const long long n0 = (long long)blockIdx.x * BN;
+    const long long tiles_m = ((long long)a.M + BM - 1) / BM;
+
+    for (int b = blockIdx.z; b < a.batch; b += gridDim.z)
+    for (long long mt = blockIdx.y; mt < tiles_m; mt += gridDim.y) {
+        const long long m0 = mt * BM;
+        const float *A = a.A + (long long)b * a.stride_a;
+        const float *B = a.B + (long long)b * a.stride_b;
+        float *C = a.C + (long long)b * a.stride_c;
+
+        // four consecutive elements of a stored row starting at (r, c),
+        // zero past the matrix (rows >= nr, columns >= nc)
+        auto load4 = [&](const float *P, long long ld, long long r, long long c, long long nr, long long nc) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r >= nr) return v;
+            const float *q = P + r * ld + c;
+            if (VEC && c + 4 <= nc) return __ldg(reinterpret_cast<const float4 *>(q));
+            if (c + 0 < nc) v.x = __ldg(q + 0);
+            if (c + 1 < nc) v.y = __ldg(q + 1);
+            if (c + 2 < nc) v.z = __ldg(q + 2);
+            if (c + 3 < nc) v.w = __ldg(q + 3);
+            return v;
+        };
+        // A tile (128 m x 16 k) and B tile (16 k x 128 n): 512 float4 each,
+        // two per thread, along the stored-contiguous dimension
+        float4 ra[2], rb[2];
+        auto load_tiles = [&](long long k0) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = tid + 256 * i;
+                if (TA) ra[i] = load4(A, a.lda, k0 + e / 32, m0 + (e % 32) * 4, a.K, a.M);   // [K][M]
+                else    ra[i] = load4(A, a.lda, m0 + e / 4, k0 + (e % 4) * 4, a.M, a.K);    // [M][K]
+                if (TB) rb[i] = load4(B, a.ldb, n0 + e / 4, k0 + (e % 4) * 4, a.N, a.K);    // [N][K]
+                else    rb[i] = load4(B, a.ldb, k0 + e / 32, n0 + (e % 32) * 4, a.K, a.N);  // [K][N]
+            }
+        };
+        auto store_tiles = [&](int buf) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = tid + 256 * i;
+                if (TA) {
+                    *reinterpret_cast<float4 *>(&As[buf][e / 32][(e % 32) * 4]) = ra[i];
+                } else {
+                    const int m = e / 4, k = (e % 4) * 4;
+                    As[buf][k + 0][m] = ra[i].x;
+                    As[buf][k + 1][m] = ra[i].y;
+                    As[buf][k + 2][m] = ra[i].z;
+                    As[buf][k + 3][m] = ra[i].w;
+                }
+                if (TB) {
+                    const int n = e / 4, k = (e % 4) * 4;
+                    Bs[buf][k + 0][n] = rb[i].x;
+                    Bs[buf][k + 1][n] = rb[i].y;
+                    Bs[buf][k + 2][n] = rb[i].z;
+                    Bs[buf][k + 3][n] = rb[i].w;
+                } else {
+                    *reinterpret_cast<float4 *>(&Bs[buf][e / 32][(e % 32) * 4]) = rb[i];
+                }
+            }
+        };
+
+        float acc[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+        load_tiles(0);
+        store_tiles(0);
+        __syncthreads();
+        int buf = 0;
+        for (long long k0 = 0; k0 < a.K; k0 += BK) {
+            const bool more = k0 + BK < a.K;
+            if (more) load_tiles(k0 + BK);
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][ty * 4]);
+                const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][64 + ty * 4]);
+                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][tx * 4]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][64 + tx * 4]);
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            }
+            if (more) {
+                store_tiles(buf ^ 1);
+                __syncthreads();
+                buf ^= 1;
+            }
+        }
+
+        // alpha/beta; 16-byte accesses of C where aligned and inside N
+        const bool cvec = VEC && (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const long long gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+            if (gm >= a.M) continue;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const long long gn = n0 + h * 64 + tx * 4;
+                float *c = C + gm * a.ldc + gn;
+                float v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = a.alpha * acc[i][h * 4 + j];
+                if (cvec && gn + 4 <= a.N) {
+                    if (a.beta != 0.0f) {
+                        const float4 o = *reinterpret_cast<const float4 *>(c);
+                        v[0] = fmaf(a.beta, o.x, v[0]);
+                        v[1] = fmaf(a.beta, o.y, v[1]);
+                        v[2] = fmaf(a.beta, o.z, v[2]);
+                        v[3] = fmaf(a.beta, o.w, v[3]);
+                    }
+                    *reinterpret_cast<float4 *>(c) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gn + j < a.N) c[j] = (a.beta != 0.0f) ? fmaf(a.beta, c[j], v[j]) : v[j];
+                }
+            }
+        }
+        __syncthreads();   // the shared tiles are refilled by the next tile
+    }
+}
+
 // Small problems: each CTA stages whole K panels (up to KC columns of A's
 // 16 rows and KC rows of B's 32 columns) into shared memory with every load
 // issued back to back, then runs the chains; one global-load latency per
@@ -262,7 +406,21 @@ cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st)
     if (tile == FFMA_LARGE) {
         const long long ty = ((long long)a.M + 127) / 128;
         dim3 grid((unsigned)(((long long)a.N + 127) / 128), (unsigned)(ty < 65535 ? ty : 65535), zb);
-        ffma_kernel<128, 128, 8, 8, 8><<<grid, 256, 0, st>>>(a);
+        // 16-byte loads need 16-byte aligned bases and row / batch strides
+        const bool vec = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15u) == 0 &&
+                         a.lda % 4 == 0 && a.ldb % 4 == 0 && a.stride_a % 4 == 0 && a.stride_b % 4 == 0 &&
+                         a.stride_c % 4 == 0;
+        const int key = (a.ta ? 4 : 0) | (a.tb ? 2 : 0) | (vec ? 1 : 0);
+        switch (key) {
+        case 0: ffma128_kernel<false, false, false><<<grid, 256, 0, st>>>(a); break;
+        case 1: ffma128_kernel<false, false, true><<<grid, 256, 0, st>>>(a); break;
+        case 2: ffma128_kernel<false, true, false><<<grid, 256, 0, st>>>(a); break;
+        case 3: ffma128_kernel<false, true, true><<<grid, 256, 0, st>>>(a); break;
+        case 4: ffma128_kernel<true, false, false><<<grid, 256, 0, st>>>(a); break;
+        case 5: ffma128_kernel<true, false, true><<<grid, 256, 0, st>>>(a); break;
+        case 6: ffma128_kernel<true, true, false><<<grid, 256, 0, st>>>(a); break;
+        default: ffma128_kernel<true, true, true><<<grid, 256, 0, st>>>(a); break;
+        }
     } else {
         const long long ty = ((long long)a.M + 31) / 32;
         dim3 grid((unsigned)(((long long)a.N + 31) / 32), (unsigned)(ty < 65535 ? ty : 65535), zb);

@@ -128,6 +128,56 @@ __device__ __forceinline__ void widen4(uint32_t v, uint32_t &lo, uint32_t &hi)
     }
 }
 
+// One slab of the product: lane (g, t) holds K values [k, k + WK) of W rows
+// g and g + 8 (w0, w1) and of X rows nt * 8 + g (xv); MMA j takes pairs
+// 4j..4j+1 as the fragments' columns 2t..2t+1 and pairs 4j+2..4j+3 as
+// columns 2t+8..2t+9, for W and X alike.  Every lane of the warp calls it.
+template <bool BF16, bool W8, int NT>
+__device__ __forceinline__ void slab_mma(float (&acc)[NT][4], const uint4 &w0, const uint4 &w1,
+                                         const uint4 (&xv)[NT][W8 ? 2 : 1])
+{
+    constexpr int WK = W8 ? 16 : 8;
+    constexpr int XL = W8 ? 2 : 1;
+    uint32_t h0[WK / 2], h1[WK / 2];
+    if constexpr (W8) {
+        const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
+        const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            widen4<BF16>(r0[q], h0[2 * q], h0[2 * q + 1]);
+            widen4<BF16>(r1[q], h1[2 * q], h1[2 * q + 1]);
+        }
+    } else {
+        h0[0] = w0.x, h0[1] = w0.y, h0[2] = w0.z, h0[3] = w0.w;
+        h1[0] = w1.x, h1[1] = w1.y, h1[2] = w1.z, h1[3] = w1.w;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        uint32_t x[WK / 2];
+#pragma unroll
+        for (int q = 0; q < XL; ++q) {
+            x[4 * q + 0] = xv[nt][q].x;
+            x[4 * q + 1] = xv[nt][q].y;
+            x[4 * q + 2] = xv[nt][q].z;
+            x[4 * q + 3] = xv[nt][q].w;
+        }
+#pragma unroll
+        for (int j = 0; j < WK / 4; ++j) {
+            const uint32_t afrag[4] = {h0[2 * j], h1[2 * j], h0[2 * j + 1], h1[2 * j + 1]};
+            mma_16816<BF16>(acc[nt], afrag, x[2 * j], x[2 * j + 1]);
+        }
+    }
+}
+
+// alpha * (v * scale[n]) + beta * C_old, one rounding, for W row n and X row c
+__device__ __forceinline__ void gemv_out(const GemvArgs &a, long long n, int c, float v)
+{
+    if (a.scale) v *= a.scale[n];
+    const long long off = (long long)c * a.c_sx + n * a.c_sw;
+    v = (a.beta != 0.0f) ? fmaf(a.beta, load_c(a.C, off, a.c_dtype), a.alpha * v) : a.alpha * v;
+    store_c1(a.C, off, v, a.c_dtype);
+}
+
 // BF16: X (and W unless W8) are bf16, else f16.  W8: W is int8.  NT: n8
 // tiles of X rows (1: at most 8 rows, 2: at most 16).
 // PIPE (16-byte aligned weight rows): each warp streams its slabs through a
@@ -198,35 +248,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int q = 0; q < XL; ++q) xv[nt][q] = load_x(nt, k + 8 * q);
-        uint32_t h0[WK / 2], h1[WK / 2];
-        if constexpr (W8) {
-            const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
-            const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                widen4<BF16>(r0[q], h0[2 * q], h0[2 * q + 1]);
-                widen4<BF16>(r1[q], h1[2 * q], h1[2 * q + 1]);
-            }
-        } else {
-            h0[0] = w0.x, h0[1] = w0.y, h0[2] = w0.z, h0[3] = w0.w;
-            h1[0] = w1.x, h1[1] = w1.y, h1[2] = w1.z, h1[3] = w1.w;
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            uint32_t x[WK / 2];
-#pragma unroll
-            for (int q = 0; q < XL; ++q) {
-                x[4 * q + 0] = xv[nt][q].x;
-                x[4 * q + 1] = xv[nt][q].y;
-                x[4 * q + 2] = xv[nt][q].z;
-                x[4 * q + 3] = xv[nt][q].w;
-            }
-#pragma unroll
-            for (int j = 0; j < WK / 4; ++j) {
-                const uint32_t afrag[4] = {h0[2 * j], h1[2 * j], h0[2 * j + 1], h1[2 * j + 1]};
-                mma_16816<BF16>(acc[nt], afrag, x[2 * j], x[2 * j + 1]);
-            }
-        }
+        slab_mma<BF16, W8, NT>(acc, w0, w1, xv);
     };
 
     long long s_reg = s0 + warp;        // first slab of this warp left for the register path
@@ -321,13 +343,253 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a
         }
     }
     const long long n = n0 + r;
-    if (kr == 0 && c < COLS && c < a.rows_x && n < a.rows_w) {
-        if (a.scale) v *= a.scale[n];
-        const long long off = (long long)c * a.c_sx + n * a.c_sw;
-        v = (a.beta != 0.0f) ? fmaf(a.beta, load_c(a.C, off, a.c_dtype), a.alpha * v) : a.alpha * v;
-        store_c1(a.C, off, v, a.c_dtype);
-    }
+    if (kr == 0 && c < COLS && c < a.rows_x && n < a.rows_w) gemv_out(a, n, c, v);
     if (KS > 1) cluster_sync();      // peers keep their shared memory until rank 0 has read it
+}
+
+// ------------------------------------------------------------ bulk-copy path
+// One persistent CTA per SM: warp GT_CONSUMERS's elected lane copies, per
+// stage, the 16 rows of a W block and the X rows over `kc` K values into a
+// ring of a.stages slots with 1-D bulk copies (cp.async.bulk, completion in
+// bytes on the slot's mbarrier); warps 0..GT_CONSUMERS-1 multiply them out
+// of shared memory.  Rows sit 64 bytes past a 128-byte multiple apart, so
+// the 16-byte reads of lanes (g, t) and (g + 1, t) fall in different bank
+// groups.  Work units are (16-row block, K slice), u = block * kslices +
+// slice, walked by CTA blockIdx.x, + gridDim.x, ...; the K slices of a
+// block are added in slice order by the CTA that completes the block (an
+// epoch-tagged arrival count per block), so the result does not depend on
+// which CTA finishes last.  Every wait is bounded; on expiry the CTA
+// records the status, lets its copies land and leaves its outputs unwritten.
+__device__ __noinline__ bool gt_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                          const GemvArgs &a)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > a.timeout_ns) {
+                *abort_flag = 1u;
+                if (a.status) {
+                    *(volatile unsigned *)a.status = 0x200u;
+                    __threadfence_system();
+                }
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool gt_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag, const GemvArgs &a)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return gt_wait_slow(bar, parity, abort_flag, a);
+}
+
+// Arrival number (1, 2, ...) of this CTA at a block's count for this launch:
+// a count tagged with another launch's epoch reads as zero.
+__device__ __forceinline__ unsigned ticket_arrive(unsigned *tk, unsigned epoch)
+{
+    const unsigned tag = epoch << 8;
+    unsigned cur = *reinterpret_cast<volatile unsigned *>(tk);
+    for (;;) {
+        const unsigned base = (cur & 0xffffff00u) == tag ? cur : tag;
+        const unsigned prev = atomicCAS(tk, cur, base + 1u);
+        if (prev == cur) return (base + 1u) & 0xffu;
+        cur = prev;
+    }
+}
+
+__device__ __forceinline__ void named_sync_consumers()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(GT_CONSUMERS * 32) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+template <bool BF16, bool W8, int NT>
+__global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const GemvArgs a)
+{
+    constexpr int WSZ = W8 ? 1 : 2;
+    constexpr int WK = W8 ? 16 : 8;
+    constexpr int SLAB = 4 * WK;
+    constexpr int XL = W8 ? 2 : 1;
+    constexpr int COLS = NT * 8;
+    extern __shared__ __align__(128) uint8_t gt_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(gt_smem);
+    uint64_t *empty = full + GT_MAX_STAGES;
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gt_smem + 2 * GT_MAX_STAGES * 8);
+    volatile uint32_t *last_flag = abort_flag + 1;
+    float(*red)[16][COLS + 1] = reinterpret_cast<float(*)[16][COLS + 1]>(gt_smem + GT_HEAD);
+    const uint32_t ring = smem_u32(gt_smem) + (uint32_t)gt_ring_off(COLS);
+    const int S = a.stages;
+    const int kc = a.kc;
+    const uint32_t wpitch = (uint32_t)gt_wpitch(kc, WSZ), xpitch = (uint32_t)gt_xpitch(kc);
+    const uint32_t stage_bytes = 16 * wpitch + COLS * xpitch;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long K = a.K;
+    const int KS = a.kslices;
+    const long long nchunk = (K + kc - 1) / kc;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), GT_CONSUMERS);
+        }
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == GT_CONSUMERS) {
+        // ---------------------------------------------------- producer
+        if (lane == 0) {
+            const uint8_t *W = static_cast<const uint8_t *>(a.W);
+            const uint8_t *X = static_cast<const uint8_t *>(a.X);
+            uint32_t stage = 0, ph = 0, issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+                const int rb = u / KS, ks = u - rb * KS;
+                const long long c0 = ks * nchunk / KS, c1 = (ks + 1) * nchunk / KS;
+                const int nrows = min(16, a.rows_w - rb * 16);
+                for (long long c = c0; c < c1; ++c) {
+                    if (!gt_wait(smem_u32(&empty[stage]), ph ^ 1u, abort_flag, a)) {
+                        ok = false;
+                        break;
+                    }
+                    const long long k0 = c * kc;
+                    const uint32_t len = (uint32_t)min((long long)kc, K - k0);
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)nrows * len * WSZ + (uint32_t)a.rows_x * len * 2u);
+                    const uint32_t dst = ring + stage * stage_bytes;
+                    for (int r = 0; r < nrows; ++r)
+                        bulk_load(dst + r * wpitch, W + (((long long)rb * 16 + r) * a.ldw + k0) * WSZ, len * WSZ, fb);
+                    for (int x = 0; x < a.rows_x; ++x)
+                        bulk_load(dst + 16 * wpitch + x * xpitch, X + ((long long)x * a.ldx + k0) * 2, len * 2u, fb);
+                    ++issued;
+                    if (++stage == (uint32_t)S) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA leaves
+                for (uint32_t i = (issued > (uint32_t)S ? issued - S : 0u); i < issued; ++i) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(smem_u32(&full[i % S]), (i / S) & 1u))
+                        if (globaltimer_ns() - t0 > 200000000ull) break;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- consumers
+        const int g = lane >> 2, t = lane & 3;
+        const int tid = threadIdx.x;
+        uint32_t stage = 0, ph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+            const int rb = u / KS, ks = u - rb * KS;
+            const long long c0 = ks * nchunk / KS, c1 = (ks + 1) * nchunk / KS;
+            const bool w0ok = rb * 16 + g < a.rows_w, w1ok = rb * 16 + g + 8 < a.rows_w;
+            float acc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+            for (long long c = c0; c < c1; ++c) {
+                // after an expired wait the warp keeps the same barrier
+                // sequence as the others (its numbers are discarded)
+                if (ok) ok = gt_wait(smem_u32(&full[stage]), ph, abort_flag, a);
+                ok = __all_sync(0xffffffffu, ok);
+                const long long k0 = c * kc;
+                const int len = (int)min((long long)kc, K - k0);
+                const uint32_t base = ring + stage * stage_bytes;
+                for (int j = warp; j * SLAB < len; j += GT_CONSUMERS) {     // warp-uniform
+                    const int koff = j * SLAB + t * WK;
+                    const bool kv = koff < len;            // len is a multiple of WK
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 w0 = (kv && w0ok) ? lds128(base + g * wpitch + koff * WSZ) : z;
+                    const uint4 w1 = (kv && w1ok) ? lds128(base + (g + 8) * wpitch + koff * WSZ) : z;
+                    uint4 xv[NT][XL];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int q = 0; q < XL; ++q)
+                            xv[nt][q] = (kv && nt * 8 + g < a.rows_x)
+                                            ? lds128(base + 16 * wpitch + (nt * 8 + g) * xpitch + (koff + 8 * q) * 2)
+                                            : z;
+                    slab_mma<BF16, W8, NT>(acc, w0, w1, xv);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+                if (++stage == (uint32_t)S) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            // the block's sums: warps added in warp order, then (several K
+            // slices) the slices in slice order by the CTA that completes the block
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                red[warp][g][nt * 8 + 2 * t] = acc[nt][0];
+                red[warp][g][nt * 8 + 2 * t + 1] = acc[nt][1];
+                red[warp][g + 8][nt * 8 + 2 * t] = acc[nt][2];
+                red[warp][g + 8][nt * 8 + 2 * t + 1] = acc[nt][3];
+            }
+            named_sync_consumers();
+            const int r = tid & 15, col = tid >> 4;        // W row r, X row col
+            float v = 0.0f;
+            if (col < COLS) {
+#pragma unroll
+                for (int w = 0; w < GT_CONSUMERS; ++w) v += red[w][r][col];
+            }
+            const long long n = (long long)rb * 16 + r;
+            if (KS == 1) {
+                if (!*abort_flag && col < a.rows_x && n < a.rows_w) gemv_out(a, n, col, v);
+            } else {
+                float *part = a.part + ((long long)rb * KS) * 256;
+                if (col < COLS) part[ks * 256 + r * 16 + col] = v;
+                __threadfence();
+                named_sync_consumers();
+                if (tid == 0) *last_flag = (!*abort_flag && ticket_arrive(a.ticket + rb, a.epoch) == (unsigned)KS) ? 1u : 0u;
+                named_sync_consumers();
+                if (*last_flag) {
+                    __threadfence();
+                    if (col < a.rows_x && n < a.rows_w) {
+                        float s = 0.0f;
+                        for (int q = 0; q < KS; ++q) s += __ldcg(part + q * 256 + r * 16 + col);
+                        gemv_out(a, n, col, s);
+                    }
+                }
+            }
+            named_sync_consumers();            // red and last_flag are free again
+        }
+    }
+    __syncthreads();
+}
+
+template <bool BF16, bool W8, int NT>
+cudaError_t launch_tma(const GemvArgs &a, cudaStream_t st)
+{
+    constexpr auto kern = gemv_tma_kernel<BF16, W8, NT>;
+    const int smem = gemv_tma_smem(a.kc, W8 ? 1 : 2, NT * 8, a.stages);
+    if (a.stages < 2 || a.stages > GT_MAX_STAGES || smem > SMEM_LIMIT || a.grid < 1) return cudaErrorInvalidValue;
+    static std::atomic<bool> configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+        if (e != cudaSuccess) return e;
+        configured[dev].store(true, std::memory_order_release);
+    }
+    kern<<<a.grid, GT_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 template <bool BF16, bool W8, int NT, bool PIPE>
@@ -374,6 +636,19 @@ cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t st)
     if (a.rows_x < 1 || a.rows_x > GEMV_MAX_ROWS || a.rows_w < 1 || a.K < 1) return cudaErrorInvalidValue;
     if (a.ksplit != 1 && a.ksplit != 2 && a.ksplit != 4 && a.ksplit != 8) return cudaErrorInvalidValue;
     const int nt = a.rows_x > 8 ? 2 : 1;
+    if (a.tma) {
+        const int key = (a.x_bf16 ? 4 : 0) | (a.w_i8 ? 2 : 0) | (nt == 2 ? 1 : 0);
+        switch (key) {
+        case 0: return launch_tma<false, false, 1>(a, st);
+        case 1: return launch_tma<false, false, 2>(a, st);
+        case 2: return launch_tma<false, true, 1>(a, st);
+        case 3: return launch_tma<false, true, 2>(a, st);
+        case 4: return launch_tma<true, false, 1>(a, st);
+        case 5: return launch_tma<true, false, 2>(a, st);
+        case 6: return launch_tma<true, true, 1>(a, st);
+        default: return launch_tma<true, true, 2>(a, st);
+        }
+    }
     // the copy ring wants 16-byte aligned weight rows (base and row stride)
     const int pipe = a.w_vec ? 1 : 0;
     const int key = (a.x_bf16 ? 8 : 0) | (a.w_i8 ? 4 : 0) | (nt == 2 ? 2 : 0) | pipe;

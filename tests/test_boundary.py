@@ -228,13 +228,12 @@ def test_epilogue_validation():
 
 def test_plan_skinny_products():
     """At most 16 rows on one side of an NT product: the skinny-product
-    kernel (K split over a cluster while there are fewer than two CTAs per
-    SM); other layouts stay on the tensor-core kernel; fp32 on the exact
-    path."""
-    assert plan(4, 11008, 4096, "f16", "f16", tb=True) == "gemv_nt_f16_f16_x4_ks1"
-    assert plan(1, 4096, 4096, "f16", "f16", tb=True) == "gemv_nt_f16_f16_x1_ks2"
-    assert plan(4096, 3, 4096, "bf16", "f32", tb=True) == "gemv_nt_bf16_f32_x3_ks2_swap"
-    assert plan(16, 64, 100000, "bf16", "bf16", tb=True) == "gemv_nt_bf16_bf16_x16_ks8"
+    kernel (its form and K split are chosen at launch); other layouts stay
+    on the tensor-core kernel; fp32 on the exact path."""
+    assert plan(4, 11008, 4096, "f16", "f16", tb=True) == "gemv_nt_f16_f16_x4"
+    assert plan(1, 4096, 4096, "f16", "f16", tb=True) == "gemv_nt_f16_f16_x1"
+    assert plan(4096, 3, 4096, "bf16", "f32", tb=True) == "gemv_nt_bf16_f32_x3_swap"
+    assert plan(16, 64, 100000, "bf16", "bf16", tb=True) == "gemv_nt_bf16_bf16_x16"
     assert plan(17, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_")
     assert plan_forced("gemv=0", 4, 4096, 4096, "f16", "f16", tb=True).startswith("tcgen05_nt_f16_f16_128x128_csplit")
     assert plan(1, 32000, 4096, "bf16", "bf16").startswith("tcgen05_nn_bf16_bf16_128x")
