@@ -36,11 +36,6 @@ struct tc_stream {
     size_t rx_cap = 0;
     unsigned *status_host = nullptr; // mapped, pinned: kernels report timeouts here
     unsigned *status_dev = nullptr;
-    // skinny-product kernel: per-block arrival counts (zeroed when allocated)
-    // and the epoch that tags this stream's launches
-    unsigned *gv_ticket = nullptr;
-    size_t gv_ticket_cap = 0;
-    unsigned gv_epoch = 0;
 };
 
 struct tc_ctx {
@@ -199,9 +194,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // when A has fewer) csplit=0 (split-K slices go through global memory and
 // the reduction kernel instead of a cluster reduction on chip) gemv=0 (a
 // product with at most 16 rows on one side stays on the tensor-core kernel)
-// gemv_ks=<1..8> (the skinny-product kernel's K split) gemv_tma=1 (its
-// bulk-copy ring instead of the register / cp.async form) pf=<d> (the
-// tensor-core producer prefetches A into L2 d K blocks ahead).
+// gemv_ks=<1|2|4|8> (the skinny-product kernel's cluster form with this K
+// split) gemv_rr=0 (its cluster form instead of the row-range form).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -214,8 +208,7 @@ struct Force {
     int no_short_a = 0;
     int i8acc = -1;
     int csplit = -1;
-    int gemv = -1, gemv_ks = 0, gemv_tma = -1;
-    int pf = -1;
+    int gemv = -1, gemv_ks = 0, gemv_rr = -1;
 };
 
 Force read_force()
@@ -254,8 +247,7 @@ Force read_force()
         else if (k == "csplit") f.csplit = std::atoi(v.c_str());
         else if (k == "gemv") f.gemv = std::atoi(v.c_str());
         else if (k == "gemv_ks") f.gemv_ks = std::atoi(v.c_str());
-        else if (k == "gemv_tma") f.gemv_tma = std::atoi(v.c_str());
-        else if (k == "pf") f.pf = std::atoi(v.c_str());
+        else if (k == "gemv_rr") f.gemv_rr = std::atoi(v.c_str());
     }
     return f;
 }
@@ -328,41 +320,15 @@ int gemv_ksplit(int64_t rows_w, int64_t K, bool w_i8, int num_sms)
     return ks;
 }
 
-// The bulk-copy form of the skinny-product kernel, when every row of X and
-// W starts on a 16-byte boundary and K is a whole number of 16-byte pieces
-// of W: K values per stage, ring depth within the shared-memory budget, and
-// K slices per 16-row block so that the (block, slice) units spread evenly
-// over one persistent CTA per SM.  Returns false when the form does not apply.
-bool plan_gemv_tma(GemvArgs &g, int num_sms, int force_ks)
+// The row-range form of the skinny-product kernel applies when every row of
+// X and W starts on a 16-byte boundary and there are at least as many W rows
+// as SMs: two persistent CTAs per SM (fewer when rows are few), each owning
+// an equal share of the rows.
+bool plan_gemv_rr(GemvArgs &g, int num_sms)
 {
-    const int wsz = g.w_i8 ? 1 : 2;
-    if (!g.x_vec || !g.w_vec || (g.K * wsz) % 16 != 0 || (g.K * 2) % 16 != 0) return false;
-    const int cols = g.rows_x > 8 ? 16 : 8;
-    g.kc = g.w_i8 ? 1024 : 512;
-    const int stage = 16 * gt_wpitch(g.kc, wsz) + cols * gt_xpitch(g.kc);
-    g.stages = std::min<int>(GT_MAX_STAGES, (SMEM_LIMIT - gt_ring_off(cols)) / stage);
-    if (g.stages < 2) return false;
-    g.nrb = (int)cdiv(g.rows_w, 16);
-    const int64_t nchunk = cdiv(g.K, g.kc);
-    int best = 1;
-    if (force_ks > 0) {
-        best = (int)std::min<int64_t>(force_ks, nchunk);
-    } else {
-        double best_waste = 1e300;
-        for (int ks = 1; ks <= 8 && ks <= nchunk; ++ks) {
-            const double units = (double)g.nrb * ks, per = units / num_sms;
-            const double waste = std::ceil(per) / per;
-            if (waste < best_waste - 0.03) {
-                best_waste = waste;
-                best = ks;
-            }
-        }
-    }
-    g.kslices = std::max(best, 1);
-    g.units = g.nrb * g.kslices;
-    g.grid = std::min(g.units, num_sms);
-    g.tma = 1;
-    g.ksplit = 1;
+    if (!g.x_vec || !g.w_vec || g.rows_w < num_sms) return false;
+    g.rowrange = 1;
+    g.grid = (int)std::min<int64_t>(2LL * num_sms, g.rows_w);
     return true;
 }
 
@@ -613,37 +579,15 @@ tc_status_t read_status(tc_stream *s)
 // bias/activation epilogue, or null).
 // col_scale: the int8 path's per-column dequantisation (its K slices then
 // hold integers and are added as such), or null.
-// Launch the skinny-product kernel on stream s: the bulk-copy form when it
-// applies (its slice sums in the stream's workspace, its arrival counts in
-// the stream's zeroed count buffer, a fresh epoch), else the register form.
+// Launch the skinny-product kernel on stream s: the row-range form when it
+// applies (and no K split was forced), else the cluster form.
 tc_status_t enqueue_gemv(tc_ctx *ctx, tc_stream *s, GemvArgs &g, const Force &f, std::string &name)
 {
     char buf[48];
-    if (f.gemv_tma == 1 && plan_gemv_tma(g, ctx->num_sms, f.gemv_ks)) {
-        if (g.kslices > 1) {
-            tc_status_t st = ensure_ws(s, (size_t)g.nrb * g.kslices * 256 * sizeof(float) + 256);
-            if (st != TC_OK) return st;
-            g.part = static_cast<float *>(s->ws);
-        }
-        const size_t tbytes = (size_t)g.nrb * sizeof(unsigned);
-        if (tbytes > s->gv_ticket_cap) {
-            const size_t cap = round_up(tbytes + tbytes / 2, 4096);
-            if (s->gv_ticket) cudaFreeAsync(s->gv_ticket, s->st);
-            s->gv_ticket = nullptr;
-            s->gv_ticket_cap = 0;
-            if (cudaMallocAsync(reinterpret_cast<void **>(&s->gv_ticket), cap, s->st) != cudaSuccess ||
-                cudaMemsetAsync(s->gv_ticket, 0, cap, s->st) != cudaSuccess)
-                return TC_ERR_CUDA;
-            s->gv_ticket_cap = cap;
-        }
-        g.ticket = s->gv_ticket;
-        s->gv_epoch = s->gv_epoch % 0xFFFFFFu + 1u;      // 1 .. 2^24 - 1
-        g.epoch = s->gv_epoch;
-        g.status = s->status_dev;
-        g.timeout_ns = 4000000000ull + (unsigned long long)cdiv(g.K, g.kc) * 20000ull;
-        std::snprintf(buf, sizeof buf, "_tma_s%d_ks%d", g.stages, g.kslices);
+    if (f.gemv_rr != 0 && f.gemv_ks == 0 && plan_gemv_rr(g, ctx->num_sms)) {
+        std::snprintf(buf, sizeof buf, "_rr%d", g.grid);
     } else {
-        g.tma = 0;
+        g.rowrange = 0;
         std::snprintf(buf, sizeof buf, "_ks%d", g.ksplit);
     }
     if (launch_gemv(g, s->st) != cudaSuccess) return TC_ERR_CUDA;
@@ -839,7 +783,6 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         const Force f = read_force();
         if (f.debug_timeout_ms > 0) a.timeout_ns = (unsigned long long)f.debug_timeout_ms * 1000000ull;
         a.debug_drop_tfull = f.debug_drop;
-        a.pf_dist = f.pf > 0 ? f.pf : 0;
     }
 
     const int64_t lda_use = p.pack_a ? lda_p : n.lda;
@@ -1394,7 +1337,6 @@ void stream_free(tc_stream *s)
     if (s->st) cudaStreamSynchronize(s->st);
     if (s->ws) cudaFree(s->ws);
     if (s->rx) cudaFree(s->rx);
-    if (s->gv_ticket) cudaFree(s->gv_ticket);
     if (s->status_host) cudaFreeHost(s->status_host);
     if (s->owned && s->st) cudaStreamDestroy(s->st);
     delete s;

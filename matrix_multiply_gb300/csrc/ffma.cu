@@ -288,6 +288,114 @@ __global__ void __launch_bounds__(256, 2) ffma128_kernel(const FfmaArgs a)
     }
 }
 
+// Small NN problems with 16-byte aligned rows (the pages' fp32 256^3 shape):
+// 16 x 32 tiles, 128 threads, one row and four columns per thread.  A and B
+// arrive in K chunks of 64 through a double-buffered cp.async pipeline (bytes
+// past M, N or K read as zeros), so the first multiply-adds start after one
+// chunk rather than after the whole K panel; every shared read is 16 bytes
+// (four k of the thread's A row, four columns of a B row).  Per output one
+// fmaf chain in ascending k.
+constexpr int SBM = 16, SBN = 32, SKC = 64, SLDA = SKC + 4;
+
+__device__ __forceinline__ void cp_async16_f(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(128) ffma_small_nn_kernel(const FfmaArgs a)
+{
+    __shared__ __align__(16) float As[2][SBM][SLDA];
+    __shared__ __align__(16) float Bs[2][SKC][SBN];
+    const int tid = threadIdx.x;
+    const int tx = tid & 7, ty = tid >> 3;
+    const long long n0 = (long long)blockIdx.x * SBN;
+    const long long tiles_m = ((long long)a.M + SBM - 1) / SBM;
+    const long long nchunk = ((long long)a.K + SKC - 1) / SKC;
+    for (int b = blockIdx.z; b < a.batch; b += gridDim.z)
+    for (long long mt = blockIdx.y; mt < tiles_m; mt += gridDim.y) {
+        const long long m0 = mt * SBM;
+        const float *A = a.A + (long long)b * a.stride_a;
+        const float *B = a.B + (long long)b * a.stride_b;
+        float *C = a.C + (long long)b * a.stride_c;
+        // chunk c into buffer c & 1: A 16 x 64 (2 pieces of 16 bytes a
+        // thread), B 64 x 32 (4 pieces a thread)
+        auto issue = [&](long long c) {
+            const long long k0 = c * SKC;
+            const int buf = (int)(c & 1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = tid + 128 * i;
+                const int r = e >> 4, q = (e & 15) * 4;
+                const long long gm = m0 + r, gk = k0 + q;
+                const long long left = (gm < a.M) ? (a.K - gk) : 0;
+                const uint32_t bytes = left >= 4 ? 16u : left > 0 ? (uint32_t)left * 4u : 0u;
+                cp_async16_f((uint32_t)__cvta_generic_to_shared(&As[buf][r][q]), bytes ? A + gm * a.lda + gk : A,
+                             bytes);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = tid + 128 * i;
+                const int r = e >> 3, q = (e & 7) * 4;
+                const long long gk = k0 + r, gn = n0 + q;
+                const long long left = (gk < a.K) ? (a.N - gn) : 0;
+                const uint32_t bytes = left >= 4 ? 16u : left > 0 ? (uint32_t)left * 4u : 0u;
+                cp_async16_f((uint32_t)__cvta_generic_to_shared(&Bs[buf][r][q]), bytes ? B + gk * a.ldb + gn : B,
+                             bytes);
+            }
+        };
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        issue(0);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (nchunk > 1) issue(1);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        for (long long c = 0; c < nchunk; ++c) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");      // chunk c has landed
+            __syncthreads();
+            const int buf = (int)(c & 1);
+#pragma unroll
+            for (int kk = 0; kk < SKC; kk += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(&As[buf][ty][kk]);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[buf][kk + u][tx * 4]);
+                    acc[0] = fmaf(av[u], b4.x, acc[0]);
+                    acc[1] = fmaf(av[u], b4.y, acc[1]);
+                    acc[2] = fmaf(av[u], b4.z, acc[2]);
+                    acc[3] = fmaf(av[u], b4.w, acc[3]);
+                }
+            }
+            __syncthreads();                                           // buffer free again
+            if (c + 2 < nchunk) issue(c + 2);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        const long long gm = m0 + ty, gn = n0 + tx * 4;
+        if (gm < a.M) {
+            float *cp = C + gm * a.ldc + gn;
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = a.alpha * acc[j];
+            const bool vec = gn + 4 <= a.N && (a.ldc % 4) == 0 && ((reinterpret_cast<uintptr_t>(cp) & 15u) == 0);
+            if (vec) {
+                if (a.beta != 0.0f) {
+                    const float4 o = *reinterpret_cast<const float4 *>(cp);
+                    v[0] = fmaf(a.beta, o.x, v[0]);
+                    v[1] = fmaf(a.beta, o.y, v[1]);
+                    v[2] = fmaf(a.beta, o.z, v[2]);
+                    v[3] = fmaf(a.beta, o.w, v[3]);
+                }
+                *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gn + j < a.N) cp[j] = (a.beta != 0.0f) ? fmaf(a.beta, cp[j], v[j]) : v[j];
+            }
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+    }
+}
+
 // Small problems: each CTA stages whole K panels (up to KC columns of A's
 // 16 rows and KC rows of B's 32 columns) into shared memory with every load
 // issued back to back, then runs the chains; one global-load latency per
@@ -385,6 +493,15 @@ __global__ void __launch_bounds__(256) ffma_panel_kernel(const FfmaArgs a)
 
 cudaError_t launch_ffma(const FfmaArgs &a, int tile, cudaStream_t st)
 {
+    if (tile == FFMA_PANEL && !a.ta && !a.tb &&
+        ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15u) == 0 && a.lda % 4 == 0 &&
+        a.ldb % 4 == 0 && a.stride_a % 4 == 0 && a.stride_b % 4 == 0) {
+        const int zb = a.batch < 65535 ? a.batch : 65535;
+        const long long ty = ((long long)a.M + SBM - 1) / SBM;
+        dim3 grid((unsigned)(((long long)a.N + SBN - 1) / SBN), (unsigned)(ty < 65535 ? ty : 65535), zb);
+        ffma_small_nn_kernel<<<grid, 128, 0, st>>>(a);
+        return cudaGetLastError();
+    }
     if (tile == FFMA_PANEL) {
         static std::atomic<bool> configured[64] = {};
         int dev = 0;

@@ -5,18 +5,24 @@
 // (fm_matvec_q8, fm_sgemm_q8: each weight row scaled by its own factor).
 //
 // Every weight byte is read once, so the product is bound by HBM, not by
-// arithmetic.  The kernel is built around the weight stream:
-//   * a warp owns 16 rows of W; each lane streams 16-byte loads of two rows
+// arithmetic.  Both kernels are built around the weight stream:
+//   * a warp owns 16 rows of W; each lane streams 16-byte pieces of two rows
 //     (rows g and g + 8 of the warp's 16, g = lane / 4), four lanes covering
-//     64 contiguous bytes of a row per load, and several loads in flight;
-//   * the 8 warps of a CTA interleave along K over the same 16 rows; the CTA
-//     adds their partial sums in warp order through shared memory;
-//   * when there are few row blocks, K is also split across a cluster of up
-//     to 8 CTAs, whose sums are added in rank order through distributed
-//     shared memory (deterministic: a fixed order everywhere).
+//     64 contiguous bytes of a row per step;
+//   * the 8 warps of a CTA interleave along K over the same rows; the CTA
+//     adds their partial sums in warp order through shared memory.
+// The row-range kernel (aligned rows, enough rows for every CTA): one
+// persistent grid of two CTAs per SM, each owning an equal range of W rows
+// (so no CTA waits on a partial last wave), each warp streaming its pieces
+// of W and of X through a ring of cp.async slots in shared memory several
+// steps ahead of its multiplies.  The cluster kernel (unaligned rows, or too
+// few rows to give every SM some): one CTA per 16-row block and K slice,
+// the slices of a block forming a cluster of up to 8 CTAs whose sums are
+// added in rank order through distributed shared memory.  Fixed orders
+// everywhere, so the result is deterministic.
 // The multiply-adds run on mma.sync m16n8k16 (fp32 accumulation) with W as
 // the 16-row operand and X^T as the 8-column operand: the K order inside one
-// lane's load is remapped the same way for both operands, so the fragments
+// lane's piece is remapped the same way for both operands, so the fragments
 // come straight from the loaded registers.  On CUDA cores the same work
 // would need a type conversion and M fused multiply-adds per weight, which
 // for int8 weights at M = 4 comes close to the FFMA peak at HBM speed.
@@ -35,15 +41,18 @@ namespace tc {
 namespace {
 
 constexpr int GV_WARPS = 8;
-constexpr int GV_UNROLL = 4;      // register path: slabs in flight per warp
-constexpr int GV_STAGES = 8;      // copy path: slabs in flight per warp (each lane 2 x 16 bytes)
-constexpr int GV_RING = GV_WARPS * GV_STAGES * 2 * 32 * 16;   // bytes of the copy ring per CTA
+constexpr int GV_UNROLL = 4;      // cluster kernel: steps in flight per warp
 
 // 16 bytes global -> shared without passing through registers (cp.async,
 // L2 only); src_bytes = 0 writes zeros
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// the same through L1 (X is read by every CTA of the SM: L1 keeps it)
+__device__ __forceinline__ void cp_async16_l1(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -180,15 +189,11 @@ __device__ __forceinline__ void gemv_out(const GemvArgs &a, long long n, int c, 
 
 // BF16: X (and W unless W8) are bf16, else f16.  W8: W is int8.  NT: n8
 // tiles of X rows (1: at most 8 rows, 2: at most 16).
-// PIPE (16-byte aligned weight rows): each warp streams its slabs through a
-// ring of GV_STAGES slots in shared memory with cp.async, GV_STAGES - 1
-// slabs ahead of the one it multiplies (64 KB of the weight stream in
-// flight per CTA, two or more CTAs per SM); each lane reads back only the
-// 32 bytes it copied itself, so no synchronisation beyond its own copy
-// groups is needed.  The slab that ends past K goes through registers with
-// element loads.  Without PIPE (unaligned weight rows) every slab does, a
-// few per warp at a time.
-template <bool BF16, bool W8, int NT, bool PIPE>
+// The cluster kernel: one CTA per (16-row block, K slice), the K slices of a
+// block one cluster of a.ksplit CTAs.  Each warp issues the weight loads of
+// GV_UNROLL steps before their multiplies; unaligned rows and the K tail
+// are read element by element.  Two CTAs per SM (at most 128 registers).
+template <bool BF16, bool W8, int NT>
 __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a)
 {
     constexpr int WK = W8 ? 16 : 8;             // weights per 16-byte load
@@ -251,45 +256,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a
         slab_mma<BF16, W8, NT>(acc, w0, w1, xv);
     };
 
-    long long s_reg = s0 + warp;        // first slab of this warp left for the register path
-    if constexpr (PIPE) {
-        // slabs wholly inside K go through the ring: slabs s0 + warp + 8i
-        extern __shared__ __align__(16) uint8_t gv_ring[];
-        const long long full_end = min(s1, K / SLAB);
-        const long long first = s0 + warp;
-        const long long nmine = first < full_end ? (full_end - first + GV_WARPS - 1) / GV_WARPS : 0;
-        const uint32_t ring = smem_u32(gv_ring) + (uint32_t)(warp * GV_STAGES * 2 * 32 * 16 + lane * 16);
-        auto issue = [&](long long i) {
-            const long long k = (first + i * GV_WARPS) * SLAB + t * WK;
-            const uint32_t slot = ring + (uint32_t)((i % GV_STAGES) * 2 * 32 * 16);
-            cp_async16(slot, wrow0 + k * WSZ, r0ok ? 16u : 0u);
-            cp_async16(slot + 32 * 16, wrow1 + k * WSZ, r1ok ? 16u : 0u);
-        };
-#pragma unroll
-        for (int i = 0; i < GV_STAGES - 1; ++i) {
-            if (i < nmine) issue(i);
-            cp_async_commit();
-        }
-        for (long long i = 0; i < nmine; ++i) {
-            if (i + GV_STAGES - 1 < nmine) issue(i + GV_STAGES - 1);
-            cp_async_commit();
-            cp_async_wait<GV_STAGES - 1>();         // this lane's copies of slab i have landed
-            const uint32_t slot = ring + (uint32_t)((i % GV_STAGES) * 2 * 32 * 16);
-            uint4 w0, w1;
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w)
-                         : "r"(slot));
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(w1.x), "=r"(w1.y), "=r"(w1.z), "=r"(w1.w)
-                         : "r"(slot + 32 * 16));
-            mma_slab(w0, w1, (first + i * GV_WARPS) * SLAB + t * WK);
-        }
-        cp_async_wait<0>();
-        s_reg = first + nmine * GV_WARPS;
-    }
-    // register path: the remaining slabs (all of them without PIPE), the
-    // weight loads of GV_UNROLL slabs issued before their multiplies
-    for (long long s = s_reg; s < s1; s += (long long)GV_WARPS * GV_UNROLL) {
+    for (long long s = s0 + warp; s < s1; s += (long long)GV_WARPS * GV_UNROLL) {
         uint4 wv[GV_UNROLL][2];
 #pragma unroll
         for (int u = 0; u < GV_UNROLL; ++u) {
@@ -347,277 +314,164 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a
     if (KS > 1) cluster_sync();      // peers keep their shared memory until rank 0 has read it
 }
 
-// ------------------------------------------------------------ bulk-copy path
-// One persistent CTA per SM: warp GT_CONSUMERS's elected lane copies, per
-// stage, the 16 rows of a W block and the X rows over `kc` K values into a
-// ring of a.stages slots with 1-D bulk copies (cp.async.bulk, completion in
-// bytes on the slot's mbarrier); warps 0..GT_CONSUMERS-1 multiply them out
-// of shared memory.  Rows sit 64 bytes past a 128-byte multiple apart, so
-// the 16-byte reads of lanes (g, t) and (g + 1, t) fall in different bank
-// groups.  Work units are (16-row block, K slice), u = block * kslices +
-// slice, walked by CTA blockIdx.x, + gridDim.x, ...; the K slices of a
-// block are added in slice order by the CTA that completes the block (an
-// epoch-tagged arrival count per block), so the result does not depend on
-// which CTA finishes last.  Every wait is bounded; on expiry the CTA
-// records the status, lets its copies land and leaves its outputs unwritten.
-__device__ __noinline__ bool gt_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          const GemvArgs &a)
-{
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > a.timeout_ns) {
-                *abort_flag = 1u;
-                if (a.status) {
-                    *(volatile unsigned *)a.status = 0x200u;
-                    __threadfence_system();
-                }
-                return false;
-            }
-        }
-    }
-}
+// ------------------------------------------------------------ row-range kernel
+// gridDim.x persistent CTAs; CTA c owns W rows [c N / G, (c + 1) N / G),
+// taken 16 at a time.  Warp w streams steps w, w + 8, ... of each 16-row
+// block through its own ring of GV_RR_RING bytes: per step and lane one
+// slot holds its 16 bytes of rows g and g + 8 and of X rows nt * 8 + g,
+// copied with cp.async (bytes past K or past the rows read as zeros; X
+// through L1, since every CTA of the SM reads the same X rows) and
+// read back by the same lane only, so a lane needs nothing but its own copy
+// groups.  The ring runs on across block boundaries; after a block's last
+// step the warps' sums are added in warp order and written.
+constexpr int GV_RR_RING = 12 * 1024;      // bytes of ring per warp
 
-__device__ __forceinline__ bool gt_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag, const GemvArgs &a)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    return gt_wait_slow(bar, parity, abort_flag, a);
-}
-
-// Arrival number (1, 2, ...) of this CTA at a block's count for this launch:
-// a count tagged with another launch's epoch reads as zero.
-__device__ __forceinline__ unsigned ticket_arrive(unsigned *tk, unsigned epoch)
-{
-    const unsigned tag = epoch << 8;
-    unsigned cur = *reinterpret_cast<volatile unsigned *>(tk);
-    for (;;) {
-        const unsigned base = (cur & 0xffffff00u) == tag ? cur : tag;
-        const unsigned prev = atomicCAS(tk, cur, base + 1u);
-        if (prev == cur) return (base + 1u) & 0xffu;
-        cur = prev;
-    }
-}
-
-__device__ __forceinline__ void named_sync_consumers()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(GT_CONSUMERS * 32) : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
+template <bool W8, int NT>
+__host__ __device__ constexpr int rr_slot() { return (2 + NT * (W8 ? 2 : 1)) * 32 * 16; }
+template <bool W8, int NT>
+__host__ __device__ constexpr int rr_stages() { return GV_RR_RING / rr_slot<W8, NT>(); }
 
 template <bool BF16, bool W8, int NT>
-__global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const GemvArgs a)
+__global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_rr_kernel(const GemvArgs a)
 {
-    constexpr int WSZ = W8 ? 1 : 2;
     constexpr int WK = W8 ? 16 : 8;
     constexpr int SLAB = 4 * WK;
     constexpr int XL = W8 ? 2 : 1;
+    constexpr int WSZ = W8 ? 1 : 2;
     constexpr int COLS = NT * 8;
-    extern __shared__ __align__(128) uint8_t gt_smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(gt_smem);
-    uint64_t *empty = full + GT_MAX_STAGES;
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gt_smem + 2 * GT_MAX_STAGES * 8);
-    volatile uint32_t *last_flag = abort_flag + 1;
-    float(*red)[16][COLS + 1] = reinterpret_cast<float(*)[16][COLS + 1]>(gt_smem + GT_HEAD);
-    const uint32_t ring = smem_u32(gt_smem) + (uint32_t)gt_ring_off(COLS);
-    const int S = a.stages;
-    const int kc = a.kc;
-    const uint32_t wpitch = (uint32_t)gt_wpitch(kc, WSZ), xpitch = (uint32_t)gt_xpitch(kc);
-    const uint32_t stage_bytes = 16 * wpitch + COLS * xpitch;
+    constexpr int SLOT = rr_slot<W8, NT>();
+    constexpr int S = rr_stages<W8, NT>();
+    static_assert(S >= 3, "ring depth");
+    extern __shared__ __align__(16) uint8_t rr_ring[];
+    __shared__ float red[GV_WARPS][16][COLS + 1];
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
     const long long K = a.K;
-    const int KS = a.kslices;
-    const long long nchunk = (K + kc - 1) / kc;
+    const long long r_lo = (long long)blockIdx.x * a.rows_w / gridDim.x;
+    const long long r_hi = (long long)(blockIdx.x + 1) * a.rows_w / gridDim.x;
+    const long long nblk = (r_hi - r_lo + 15) / 16;
+    const long long nslab = (K + SLAB - 1) / SLAB;
+    const long long per = warp < nslab ? (nslab - warp + GV_WARPS - 1) / GV_WARPS : 0;   // this warp's steps per block
+    const long long items = nblk * per;
+    const uint8_t *W = static_cast<const uint8_t *>(a.W);
+    const uint8_t *X = static_cast<const uint8_t *>(a.X);
+    const uint32_t ring = smem_u32(rr_ring) + (uint32_t)(warp * GV_RR_RING + lane * 16);
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), GT_CONSUMERS);
+    // item i of this warp: block i / per, step warp + 8 (i % per)
+    auto issue = [&](long long i) {
+        const long long blk = i / per;
+        const long long kq = (warp + (long long)GV_WARPS * (i - blk * per)) * SLAB + t * WK;   // this lane's K
+        const long long n0 = r_lo + blk * 16;
+        const uint32_t slot = ring + (uint32_t)((i % S) * SLOT);
+        const long long kb = (K - kq) * WSZ;                       // bytes of the piece inside K
+        const uint32_t wbytes = kb >= 16 ? 16u : kb > 0 ? (uint32_t)kb : 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long n = n0 + g + 8 * h;
+            const bool ok = n < r_hi;
+            cp_async16(slot + h * 512, W + (ok ? (n * a.ldw + kq) * WSZ : 0), ok ? wbytes : 0u);
         }
-        *abort_flag = 0u;
-        fence_barrier_init();
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = nt * 8 + g;
+#pragma unroll
+            for (int q = 0; q < XL; ++q) {
+                const long long kx = kq + 8 * q;
+                const long long xb = (K - kx) * 2;
+                const uint32_t bytes = row < a.rows_x ? (xb >= 16 ? 16u : xb > 0 ? (uint32_t)xb : 0u) : 0u;
+                cp_async16_l1(slot + (2 + nt * XL + q) * 512, X + (bytes ? ((long long)row * a.ldx + kx) * 2 : 0),
+                              bytes);
+            }
+        }
+    };
+
+#pragma unroll
+    for (int q = 0; q < S - 1; ++q) {
+        if (q < items) issue(q);
+        cp_async_commit();
     }
-    __syncthreads();
-
-    if (warp == GT_CONSUMERS) {
-        // ---------------------------------------------------- producer
-        if (lane == 0) {
-            const uint8_t *W = static_cast<const uint8_t *>(a.W);
-            const uint8_t *X = static_cast<const uint8_t *>(a.X);
-            uint32_t stage = 0, ph = 0, issued = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
-                const int rb = u / KS, ks = u - rb * KS;
-                const long long c0 = ks * nchunk / KS, c1 = (ks + 1) * nchunk / KS;
-                const int nrows = min(16, a.rows_w - rb * 16);
-                for (long long c = c0; c < c1; ++c) {
-                    if (!gt_wait(smem_u32(&empty[stage]), ph ^ 1u, abort_flag, a)) {
-                        ok = false;
-                        break;
-                    }
-                    const long long k0 = c * kc;
-                    const uint32_t len = (uint32_t)min((long long)kc, K - k0);
-                    const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)nrows * len * WSZ + (uint32_t)a.rows_x * len * 2u);
-                    const uint32_t dst = ring + stage * stage_bytes;
-                    for (int r = 0; r < nrows; ++r)
-                        bulk_load(dst + r * wpitch, W + (((long long)rb * 16 + r) * a.ldw + k0) * WSZ, len * WSZ, fb);
-                    for (int x = 0; x < a.rows_x; ++x)
-                        bulk_load(dst + 16 * wpitch + x * xpitch, X + ((long long)x * a.ldx + k0) * 2, len * 2u, fb);
-                    ++issued;
-                    if (++stage == (uint32_t)S) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // let the copies already issued land before the CTA leaves
-                for (uint32_t i = (issued > (uint32_t)S ? issued - S : 0u); i < issued; ++i) {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(smem_u32(&full[i % S]), (i / S) & 1u))
-                        if (globaltimer_ns() - t0 > 200000000ull) break;
-                }
-            }
+    for (long long blk = 0; blk < nblk; ++blk) {
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        for (long long j = 0; j < per; ++j) {
+            const long long i = blk * per + j;
+            if (i + S - 1 < items) issue(i + S - 1);
+            cp_async_commit();
+            cp_async_wait<S - 1>();                   // this lane's copies of item i have landed
+            const uint32_t slot = ring + (uint32_t)((i % S) * SLOT);
+            uint4 w0, w1;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w) : "r"(slot));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w1.x), "=r"(w1.y), "=r"(w1.z), "=r"(w1.w) : "r"(slot + 512));
+            uint4 xv[NT][XL];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < XL; ++q)
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(xv[nt][q].x), "=r"(xv[nt][q].y), "=r"(xv[nt][q].z), "=r"(xv[nt][q].w)
+                                 : "r"(slot + (2 + nt * XL + q) * 512));
+            slab_mma<BF16, W8, NT>(acc, w0, w1, xv);
         }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------- consumers
-        const int g = lane >> 2, t = lane & 3;
-        const int tid = threadIdx.x;
-        uint32_t stage = 0, ph = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-            const int rb = u / KS, ks = u - rb * KS;
-            const long long c0 = ks * nchunk / KS, c1 = (ks + 1) * nchunk / KS;
-            const bool w0ok = rb * 16 + g < a.rows_w, w1ok = rb * 16 + g + 8 < a.rows_w;
-            float acc[NT][4];
+        // D fragment: acc[nt][e] is (W row g, X row nt*8 + 2t + e), acc[nt][2 + e]
+        // is (W row g + 8, same X row)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-            for (long long c = c0; c < c1; ++c) {
-                // after an expired wait the warp keeps the same barrier
-                // sequence as the others (its numbers are discarded)
-                if (ok) ok = gt_wait(smem_u32(&full[stage]), ph, abort_flag, a);
-                ok = __all_sync(0xffffffffu, ok);
-                const long long k0 = c * kc;
-                const int len = (int)min((long long)kc, K - k0);
-                const uint32_t base = ring + stage * stage_bytes;
-                for (int j = warp; j * SLAB < len; j += GT_CONSUMERS) {     // warp-uniform
-                    const int koff = j * SLAB + t * WK;
-                    const bool kv = koff < len;            // len is a multiple of WK
-                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 w0 = (kv && w0ok) ? lds128(base + g * wpitch + koff * WSZ) : z;
-                    const uint4 w1 = (kv && w1ok) ? lds128(base + (g + 8) * wpitch + koff * WSZ) : z;
-                    uint4 xv[NT][XL];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int q = 0; q < XL; ++q)
-                            xv[nt][q] = (kv && nt * 8 + g < a.rows_x)
-                                            ? lds128(base + 16 * wpitch + (nt * 8 + g) * xpitch + (koff + 8 * q) * 2)
-                                            : z;
-                    slab_mma<BF16, W8, NT>(acc, w0, w1, xv);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-                if (++stage == (uint32_t)S) {
-                    stage = 0;
-                    ph ^= 1u;
-                }
-            }
-            // the block's sums: warps added in warp order, then (several K
-            // slices) the slices in slice order by the CTA that completes the block
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                red[warp][g][nt * 8 + 2 * t] = acc[nt][0];
-                red[warp][g][nt * 8 + 2 * t + 1] = acc[nt][1];
-                red[warp][g + 8][nt * 8 + 2 * t] = acc[nt][2];
-                red[warp][g + 8][nt * 8 + 2 * t + 1] = acc[nt][3];
-            }
-            named_sync_consumers();
-            const int r = tid & 15, col = tid >> 4;        // W row r, X row col
+        for (int nt = 0; nt < NT; ++nt) {
+            red[warp][g][nt * 8 + 2 * t] = acc[nt][0];
+            red[warp][g][nt * 8 + 2 * t + 1] = acc[nt][1];
+            red[warp][g + 8][nt * 8 + 2 * t] = acc[nt][2];
+            red[warp][g + 8][nt * 8 + 2 * t + 1] = acc[nt][3];
+        }
+        __syncthreads();
+        const int r = threadIdx.x & 15, c = threadIdx.x >> 4;       // W row r, X row c
+        const long long n = r_lo + blk * 16 + r;
+        if (c < COLS && c < a.rows_x && n < r_hi) {
             float v = 0.0f;
-            if (col < COLS) {
 #pragma unroll
-                for (int w = 0; w < GT_CONSUMERS; ++w) v += red[w][r][col];
-            }
-            const long long n = (long long)rb * 16 + r;
-            if (KS == 1) {
-                if (!*abort_flag && col < a.rows_x && n < a.rows_w) gemv_out(a, n, col, v);
-            } else {
-                float *part = a.part + ((long long)rb * KS) * 256;
-                if (col < COLS) part[ks * 256 + r * 16 + col] = v;
-                __threadfence();
-                named_sync_consumers();
-                if (tid == 0) *last_flag = (!*abort_flag && ticket_arrive(a.ticket + rb, a.epoch) == (unsigned)KS) ? 1u : 0u;
-                named_sync_consumers();
-                if (*last_flag) {
-                    __threadfence();
-                    if (col < a.rows_x && n < a.rows_w) {
-                        float s = 0.0f;
-                        for (int q = 0; q < KS; ++q) s += __ldcg(part + q * 256 + r * 16 + col);
-                        gemv_out(a, n, col, s);
-                    }
-                }
-            }
-            named_sync_consumers();            // red and last_flag are free again
+            for (int w = 0; w < GV_WARPS; ++w) v += red[w][r][c];
+            gemv_out(a, n, c, v);
         }
+        __syncthreads();
     }
-    __syncthreads();
+    cp_async_wait<0>();
 }
 
 template <bool BF16, bool W8, int NT>
-cudaError_t launch_tma(const GemvArgs &a, cudaStream_t st)
+cudaError_t launch_rr(const GemvArgs &a, cudaStream_t st)
 {
-    constexpr auto kern = gemv_tma_kernel<BF16, W8, NT>;
-    const int smem = gemv_tma_smem(a.kc, W8 ? 1 : 2, NT * 8, a.stages);
-    if (a.stages < 2 || a.stages > GT_MAX_STAGES || smem > SMEM_LIMIT || a.grid < 1) return cudaErrorInvalidValue;
+    constexpr auto kern = gemv_rr_kernel<BF16, W8, NT>;
+    constexpr int smem = GV_WARPS * GV_RR_RING;
     static std::atomic<bool> configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev].load(std::memory_order_acquire)) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured[dev].store(true, std::memory_order_release);
     }
-    kern<<<a.grid, GT_THREADS, smem, st>>>(a);
+    if (a.grid < 1 || a.grid > a.rows_w) return cudaErrorInvalidValue;
+    kern<<<a.grid, GV_WARPS * 32, smem, st>>>(a);
     return cudaGetLastError();
 }
 
-template <bool BF16, bool W8, int NT, bool PIPE>
+template <bool BF16, bool W8, int NT>
 cudaError_t launch_one(const GemvArgs &a, cudaStream_t st)
 {
-    constexpr auto kern = gemv_kernel<BF16, W8, NT, PIPE>;
-    constexpr int smem = PIPE ? GV_RING : 0;
-    if constexpr (PIPE) {
-        static std::atomic<bool> configured[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!configured[dev].load(std::memory_order_acquire)) {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return e;
-            configured[dev].store(true, std::memory_order_release);
-        }
-    }
+    constexpr auto kern = gemv_kernel<BF16, W8, NT>;
     const long long blocks = ((long long)a.rows_w + 15) / 16 * a.ksplit;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (a.ksplit == 1) {
-        kern<<<(unsigned)blocks, GV_WARPS * 32, smem, st>>>(a);
+        kern<<<(unsigned)blocks, GV_WARPS * 32, 0, st>>>(a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3(GV_WARPS * 32, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -634,41 +488,31 @@ cudaError_t launch_one(const GemvArgs &a, cudaStream_t st)
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t st)
 {
     if (a.rows_x < 1 || a.rows_x > GEMV_MAX_ROWS || a.rows_w < 1 || a.K < 1) return cudaErrorInvalidValue;
-    if (a.ksplit != 1 && a.ksplit != 2 && a.ksplit != 4 && a.ksplit != 8) return cudaErrorInvalidValue;
-    const int nt = a.rows_x > 8 ? 2 : 1;
-    if (a.tma) {
-        const int key = (a.x_bf16 ? 4 : 0) | (a.w_i8 ? 2 : 0) | (nt == 2 ? 1 : 0);
+    const int key = (a.x_bf16 ? 4 : 0) | (a.w_i8 ? 2 : 0) | (a.rows_x > 8 ? 1 : 0);
+    if (a.rowrange) {
+        // 16-byte copies need 16-byte aligned rows of X and W
+        if (!a.x_vec || !a.w_vec) return cudaErrorInvalidValue;
         switch (key) {
-        case 0: return launch_tma<false, false, 1>(a, st);
-        case 1: return launch_tma<false, false, 2>(a, st);
-        case 2: return launch_tma<false, true, 1>(a, st);
-        case 3: return launch_tma<false, true, 2>(a, st);
-        case 4: return launch_tma<true, false, 1>(a, st);
-        case 5: return launch_tma<true, false, 2>(a, st);
-        case 6: return launch_tma<true, true, 1>(a, st);
-        default: return launch_tma<true, true, 2>(a, st);
+        case 0: return launch_rr<false, false, 1>(a, st);
+        case 1: return launch_rr<false, false, 2>(a, st);
+        case 2: return launch_rr<false, true, 1>(a, st);
+        case 3: return launch_rr<false, true, 2>(a, st);
+        case 4: return launch_rr<true, false, 1>(a, st);
+        case 5: return launch_rr<true, false, 2>(a, st);
+        case 6: return launch_rr<true, true, 1>(a, st);
+        default: return launch_rr<true, true, 2>(a, st);
         }
     }
-    // the copy ring wants 16-byte aligned weight rows (base and row stride)
-    const int pipe = a.w_vec ? 1 : 0;
-    const int key = (a.x_bf16 ? 8 : 0) | (a.w_i8 ? 4 : 0) | (nt == 2 ? 2 : 0) | pipe;
+    if (a.ksplit != 1 && a.ksplit != 2 && a.ksplit != 4 && a.ksplit != 8) return cudaErrorInvalidValue;
     switch (key) {
-    case 0: return launch_one<false, false, 1, false>(a, st);
-    case 1: return launch_one<false, false, 1, true>(a, st);
-    case 2: return launch_one<false, false, 2, false>(a, st);
-    case 3: return launch_one<false, false, 2, true>(a, st);
-    case 4: return launch_one<false, true, 1, false>(a, st);
-    case 5: return launch_one<false, true, 1, true>(a, st);
-    case 6: return launch_one<false, true, 2, false>(a, st);
-    case 7: return launch_one<false, true, 2, true>(a, st);
-    case 8: return launch_one<true, false, 1, false>(a, st);
-    case 9: return launch_one<true, false, 1, true>(a, st);
-    case 10: return launch_one<true, false, 2, false>(a, st);
-    case 11: return launch_one<true, false, 2, true>(a, st);
-    case 12: return launch_one<true, true, 1, false>(a, st);
-    case 13: return launch_one<true, true, 1, true>(a, st);
-    case 14: return launch_one<true, true, 2, false>(a, st);
-    default: return launch_one<true, true, 2, true>(a, st);
+    case 0: return launch_one<false, false, 1>(a, st);
+    case 1: return launch_one<false, false, 2>(a, st);
+    case 2: return launch_one<false, true, 1>(a, st);
+    case 3: return launch_one<false, true, 2>(a, st);
+    case 4: return launch_one<true, false, 1>(a, st);
+    case 5: return launch_one<true, false, 2>(a, st);
+    case 6: return launch_one<true, true, 1>(a, st);
+    default: return launch_one<true, true, 2>(a, st);
     }
 }
 

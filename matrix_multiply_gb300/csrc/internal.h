@@ -98,7 +98,6 @@ struct MmaArgs {
     // bytes; the tile's other rows hold stale data, which reaches only
     // output rows beyond M (never stored)
     int a_short_bytes;
-    int pf_dist;           // L2 prefetch of A this many K blocks ahead (0: none)
 };
 
 struct MmaLaunch {
@@ -190,9 +189,9 @@ cudaError_t noalloc_scratch(NoallocScratch *out);
 // beta * Out_old for X with at most GEMV_MAX_ROWS rows.  X is [rows_x, K]
 // (f16 or bf16, row stride ldx elements), W is [rows_w, K] (X's type, or
 // int8 when w_i8; row stride ldw elements); the output element of (X row
-// i, W row j) is at C + i * c_sx + j * c_sw (elements of c_dtype).  K is
-// split across a cluster of ksplit CTAs (1, 2, 4 or 8) whose sums are added
-// in rank order.
+// i, W row j) is at C + i * c_sx + j * c_sw (elements of c_dtype).  The
+// cluster kernel splits K across a cluster of ksplit CTAs (1, 2, 4 or 8)
+// whose sums are added in rank order.
 constexpr int GEMV_MAX_ROWS = 16;
 struct GemvArgs {
     const void *X, *W;
@@ -206,37 +205,12 @@ struct GemvArgs {
     int x_vec, w_vec;      // 16-byte loads allowed: 16-byte aligned base and row stride
     int w_i8, x_bf16;
     int ksplit;
-    // Bulk-copy path (tma = 1; 16-byte aligned rows of X and W and K a
-    // multiple of 16 bytes of W): `grid` persistent CTAs walk `units` =
-    // nrb * kslices units of (16-row block, K slice), copying `kc` K values
-    // per stage into a ring of `stages` slots.  With kslices > 1 the slices'
-    // sums go through part (nrb * kslices * 256 floats) and are added by the
-    // CTA whose arrival completes the block's count in ticket[block] (nrb
-    // words tagged with `epoch`, 1 .. 2^24 - 1, a value no other launch on
-    // the same words uses).
-    int tma;
-    int grid, units, kslices, nrb, stages, kc;
-    float *part;
-    unsigned *ticket;
-    unsigned epoch;
-    unsigned *status;      // device-visible status word (0x200 on an expired wait), or null
-    unsigned long long timeout_ns;
+    // row-range kernel (16-byte aligned rows of X and W): `grid` persistent
+    // CTAs (at most rows_w), CTA c owning W rows [c rows_w / grid,
+    // (c + 1) rows_w / grid); ksplit is then unused
+    int rowrange, grid;
 };
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t st);
-// shared-memory layout of the bulk-copy path: barriers and flags, the warp
-// sums, then the ring; rows 64 bytes past a 128-byte multiple apart
-constexpr int GT_CONSUMERS = 8;
-constexpr int GT_THREADS = (GT_CONSUMERS + 1) * 32;
-constexpr int GT_MAX_STAGES = 8;
-constexpr int GT_HEAD = 256;
-__host__ __device__ constexpr int gt_wpitch(int kc, int wsz) { return kc * wsz + 64; }
-__host__ __device__ constexpr int gt_xpitch(int kc) { return kc * 2 + 64; }
-__host__ __device__ constexpr int gt_ring_off(int cols) { return (GT_HEAD + GT_CONSUMERS * 16 * (cols + 1) * 4 + 127) / 128 * 128; }
-__host__ __device__ constexpr int gemv_tma_smem(int kc, int wsz, int cols, int stages)
-{
-    return gt_ring_off(cols) + stages * (16 * gt_wpitch(kc, wsz) + cols * gt_xpitch(kc));
-}
-
 // fp32 FFMA kernel (exact fp32, ascending-k fused multiply-add chain)
 struct FfmaArgs {
     int M, N, K;

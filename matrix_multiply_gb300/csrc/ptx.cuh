@@ -85,23 +85,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// bring a tensor tile into L2 ahead of its copy to shared memory
-__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, int32_t c1)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int32_t c0, int32_t c1, int32_t c2)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 // 1-D bulk copy global -> this CTA's shared memory, completion counted in
 // bytes on the mbarrier (both addresses and the size multiples of 16 bytes)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)

@@ -699,21 +699,6 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                         else
                             tma_load_3d_pair(dst, tm, fb, 0, k0, mn0 / 64);
                     };
-                    // L2 prefetch of A's block args.pf_dist K blocks ahead (the
-                    // streamed operand), so its DRAM latency is not paid in the ring
-                    if (args.pf_dist > 0 && kb + args.pf_dist < w.kb1) {
-                        const int kp = (kb + args.pf_dist) * BK;
-                        if (a_kmajor) {
-                            if (a_3d) tma_prefetch_3d(mapA, kp, m0, w.b);
-                            else tma_prefetch_2d(mapA, kp, m0);
-                        } else if (a_chunked) {
-                            tma_prefetch_3d(mapA, 0, kp, m0 / 64);
-                        } else if (a_3d) {
-                            tma_prefetch_3d(mapA, m0, kp, w.b);
-                        } else {
-                            tma_prefetch_2d(mapA, m0, kp);
-                        }
-                    }
                     if (a_kmajor) {
                         load(mapA, a_3d, sa, k0, m0);
                     } else if (a_chunked) {

@@ -105,6 +105,26 @@ def test_ffma_parity(ctx, ta, tb, shape):
     assert ctx.last_kernel.startswith("ffma_f32_" + p.layout.lower())
 
 
+@pytest.mark.parametrize("shape", [(1, 4, 4), (16, 32, 64), (17, 35, 129), (255, 257, 300), (100, 60, 1000),
+                                   (256, 256, 256)])
+@pytest.mark.parametrize("beta", [0.0, -0.75])
+def test_ffma_small_nn_pipeline(ctx, force, shape, beta):
+    """The small-problem NN kernel (16-byte aligned rows): K in chunks of 64
+    through a two-buffer cp.async pipeline, zeros past M, N and K; the
+    exact-fp32 bound, and bitwise equality with integer data."""
+    force("ffma=panel")
+    M, N, K = shape
+    r4 = lambda x: (x + 3) // 4 * 4      # noqa: E731
+    p = synthetic.make_problem(M, N, K, "f32", "f32", alpha=1.5, beta=beta, seed=M + N + K, dist="uniform",
+                               c_fill="uniform", lda=r4(K), ldb=r4(N), ldc=N + 1)
+    check_full(ctx, p, f"small nn {shape}", lda=r4(K), ldb=r4(N), ldc=N + 1)
+    q = synthetic.make_problem(M, N, K, "f32", "f32", alpha=1.0, beta=beta, seed=M + 2 * N + K, dist="int", scale=4,
+                               c_fill="int", lda=r4(K), ldb=r4(N))
+    out = run_problem(ctx, q, lda=r4(K), ldb=r4(N))
+    R, _ = oracle.gemm(q)
+    assert np.array_equal(oracle.decode(out)[:, :N], R), ctx.last_kernel
+
+
 @pytest.mark.parametrize("spec", ["ffma=small", "ffma=large", "ffma=panel"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_ffma_tiles(ctx, force, spec, ta, tb):

@@ -173,36 +173,32 @@ def test_gemv_every_row_count(ctx, M, ab):
         assert "_swap" in ctx.last_kernel, ctx.last_kernel
 
 
-@pytest.mark.parametrize("spec", ["gemv_tma=1 gemv_ks=1", "gemv_tma=1 gemv_ks=2", "gemv_tma=1 gemv_ks=3",
-                                  "gemv_tma=1 gemv_ks=4", "gemv_tma=1 gemv_ks=8",
-                                  "gemv_ks=1", "gemv_ks=2", "gemv_ks=8"])
-def test_gemv_k_split_integer_bitwise(ctx, force, spec):
-    """K cut into slices (the bulk-copy form: slices added in slice order by
-    the CTA that completes a block; the register form: a cluster of CTAs
-    added in rank order): integer data give the exact result whatever the
-    cut.  K = 9001 and 17 are not 16-byte multiples, so they take the
-    register form whatever is asked."""
+@pytest.mark.parametrize("spec", ["", "gemv_ks=1", "gemv_ks=2", "gemv_ks=4", "gemv_ks=8"])
+def test_gemv_forms_integer_bitwise(ctx, force, spec):
+    """The row-range form (each CTA an equal share of W's rows, the warps'
+    sums added in warp order) and the cluster form with K cut over 1 to 8
+    CTAs (sums added in rank order): integer data give the exact result
+    whatever the cut.  K = 9001 rows are not 16-byte multiples and 5 rows
+    are fewer than the SMs, so those take the cluster form whatever is asked."""
     force(spec)
-    ks = int(spec.rsplit("=", 1)[1])
     for (M, N, K) in [(4, 1000, 4096), (16, 33, 9001), (1, 5, 17), (9, 300, 2048)]:
-        p = synthetic.make_problem(M, N, K, "f16", "f32", transpose_b=True, beta=1.0, seed=K + ks, dist="int",
-                                   scale=4.0, c_fill="int")
+        p = synthetic.make_problem(M, N, K, "f16", "f32", transpose_b=True, beta=1.0, seed=K + len(spec),
+                                   dist="int", scale=4.0, c_fill="int")
         out = run(ctx, p)
-        tma = "gemv_tma=1" in spec and K % 8 == 0
-        assert ("_tma_" in ctx.last_kernel) == tma, ctx.last_kernel
+        rr = spec == "" and K % 8 == 0 and N >= 152
+        assert ("_rr" in ctx.last_kernel) == rr, ctx.last_kernel
         R, _ = oracle.gemm(p)
         assert np.array_equal(out.numpy().astype(np.float64), R), (M, N, K, ctx.last_kernel)
 
 
 @pytest.mark.parametrize("ab", ["f16", "bf16"])
 def test_gemv_both_forms_agree(ctx, force, ab):
-    """The bulk-copy and register forms on the same problem: both within the
-    bound (their K orders differ), and the bulk-copy form bitwise equal to
-    itself run to run."""
+    """The row-range and cluster forms on the same problem: both within the
+    bound (their K orders differ), each bitwise equal to itself run to run."""
     p = synthetic.make_problem(7, 3000, 5120, ab, "f32", transpose_b=True, alpha=0.5, beta=-1.0, seed=97,
                                dist="normal", c_fill="uniform")
     R, T = oracle.gemm(p)
-    for spec in ["", "gemv_tma=1"]:
+    for spec in ["", "gemv_rr=0"]:
         force(spec)
         outs = [run(ctx, p) for _ in range(3)]
         for o in outs[1:]:
