@@ -5,9 +5,11 @@ accumulation, alpha = 1, beta = 0, inputs normal(0,1) rounded to bf16 from
 seed 1 (the tensorcore gemm.md "Measured perf" 4096^3 shape; the tessl
 architecture.md "Column-Panel Grid Swizzling" bf16 4096^3 figure).
 
-Timing: inputs resident in HBM; before every step the L2 is flushed by
-writing a buffer twice the L2 size; each step's GEMM is bracketed by CUDA
-events on the stream it is launched on (the flush is outside the events);
+Timing: inputs resident in HBM; every step starts from a cold L2 -- by
+default each step reads its own copy of the operands (R >= 2 copies in
+turn, R x step bytes >= 2.5 x L2); ``--l2 flush`` writes a buffer twice the
+L2 size before every step instead; each step's GEMM is bracketed by CUDA
+events on the stream it is launched on (nothing else inside the events);
 W warm-up steps, then exactly K timed steps, with a barrier and a device
 synchronize on both sides.  Under torchrun every rank runs an independent
 replica on its own GPU (the path does not shard), the time is the max over
@@ -337,19 +339,65 @@ def torch_int8():
     return torch.int8
 
 
-class Runner:
-    """Device-resident operands of one workload and its launch."""
+def step_bytes(probs) -> int:
+    """Bytes of the operands one step reads or writes (A, B, C, vectors)."""
+    n = 0
+    for p in probs:
+        n += p.A.numel() * p.A.element_size() + p.B.numel() * p.B.element_size() + p.C.numel() * p.C.element_size()
+    return n
 
-    def __init__(self, tg, ctx, stream, probs):
+
+class Cold:
+    """Cold L2 before every timed step, one of two ways:
+    rotate -- every step reads its own copy of the operands: R >= 2 copies
+              with R x (bytes of a step) >= 2.5 x L2, used in turn, so a
+              step's operands were evicted by the R - 1 steps before it (the
+              rules' "inputs larger than L2"; nothing extra runs between
+              steps);
+    flush  -- one copy, and a write of >= 2 x L2 before every step (outside
+              the timed events); the flush leaves the L2 full of dirty lines,
+              which a read-bound step then pays to write back."""
+
+    def __init__(self, torch, mode: str, l2_bytes: int):
+        self.torch, self.mode, self.l2 = torch, mode, l2_bytes
+        self.buf = (torch.empty(max(2 * l2_bytes, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+                    if mode == "flush" else None)
+
+    def copies(self, probs) -> int:
+        if self.mode != "rotate":
+            return 1
+        nbytes = max(step_bytes(probs), 1)
+        return int(min(4096, max(2, -(-int(2.5 * self.l2) // nbytes))))
+
+    def before_step(self):
+        if self.buf is not None:
+            self.buf.zero_()
+
+    def describe(self) -> str:
+        if self.mode == "flush":
+            return "flushed before every step (write of >= 2x L2); flush outside the timed events"
+        return ("cold L2: each step reads its own copy of the operands, R >= 2 copies in turn with "
+                "R x step bytes >= 2.5x L2 (no flush kernel)")
+
+
+class Runner:
+    """Device-resident operands of one workload (``copies`` copies, used in
+    turn) and its launch."""
+
+    def __init__(self, tg, ctx, stream, probs, copies: int = 1):
         self.tg, self.ctx, self.stream, self.probs = tg, ctx, stream, probs
-        self.A = [p.A.cuda() for p in probs]
-        self.B = [p.B.cuda() for p in probs]
-        self.C = [p.C.cuda() for p in probs]
+        self.copies, self.k = copies, 0
+        self.As = [[p.A.cuda() for p in probs] for _ in range(copies)]
+        self.Bs = [[p.B.cuda() for p in probs] for _ in range(copies)]
+        self.Cs = [[p.C.cuda() for p in probs] for _ in range(copies)]
+        self.A, self.B, self.C = self.As[0], self.Bs[0], self.Cs[0]
         self.d = [tg.make_desc(p.M, p.N, p.K, p.ab_dtype, p.c_dtype, transpose_a=p.transpose_a,
                                transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta,
                                b_dtype="i8" if p.B.dtype == torch_int8() else None) for p in probs]
-        # a group's arguments are marshalled once; each step is one C call
-        self.group = tg.GroupedGemm(self.d, self.A, self.B, self.C) if len(probs) > 1 else None
+        # a group's arguments are marshalled once per copy; each step is one C call
+        self.groups = ([tg.GroupedGemm(self.d, a, b, c) for a, b, c in zip(self.As, self.Bs, self.Cs)]
+                       if len(probs) > 1 else None)
+        self.group = self.groups[0] if self.groups else None
         # the fused-epilogue workloads carry a bias and an activation
         p0 = probs[0]
         self.activation = getattr(p0, "activation", None)
@@ -360,6 +408,11 @@ class Runner:
 
     def step(self):
         tg = self.tg
+        if self.copies > 1:
+            self.k = (self.k + 1) % self.copies
+            self.A, self.B, self.C = self.As[self.k], self.Bs[self.k], self.Cs[self.k]
+            if self.groups:
+                self.group = self.groups[self.k]
         if self.q8_scale is not None:
             tg.tc_gemm_q8_weight_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.q8_scale,
                                        self.stream)
@@ -378,15 +431,15 @@ class Runner:
             self.group.enqueue(self.ctx, self.stream)
 
 
-def time_steps(torch, runner, tstream, flush, steps, warmup):
+def time_steps(torch, runner, tstream, cold, steps, warmup):
     for _ in range(warmup):
-        flush.zero_()
+        cold.before_step()
         runner.step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        cold.before_step()
         starts[i].record(tstream)
         runner.step()
         ends[i].record(tstream)
@@ -414,7 +467,7 @@ def run_ours(args):
     stream = tg.Stream(ctx, torch_stream=tstream)
     props = torch.cuda.get_device_properties(local)
     sms = props.multi_processor_count
-    flush = torch.empty(max(2 * props.L2_cache_size, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    cold = Cold(torch, args.l2, props.L2_cache_size)
     reg = workload_registry()
     name = args.workload
     # Every other named workload is timed first (cold L2 per step, about a
@@ -422,13 +475,13 @@ def run_ours(args):
     # at its running clocks before the headline's warm-up steps begin.
     work = None
     if args.summary and name == HEADLINE and world == 1:
-        work = summary(torch, tg, ctx, stream, tstream, flush, reg, sms)
+        work = summary(torch, tg, ctx, stream, tstream, cold, reg, sms)
     probs = reg[name]()
-    runner = Runner(tg, ctx, stream, probs)
+    runner = Runner(tg, ctx, stream, probs, cold.copies(probs))
     flops = sum(2.0 * p.M * p.N * p.K for p in probs)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        cold.before_step()
         runner.step()
     torch.cuda.synchronize()
     barrier()
@@ -440,7 +493,7 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
+            cold.before_step()
             starts[i].record(tstream)
             runner.step()
             ends[i].record(tstream)
@@ -498,7 +551,7 @@ def run_ours(args):
         "config": {"workload": WORKLOAD if name == HEADLINE else name, "problems": len(probs),
                    "M": p0.M, "N": p0.N, "K": p0.K, "layout": p0.layout, "global_batch": len(probs),
                    "parallelism": f"replicas{world}" if world > 1 else "single", "variant": kernel,
-                   "l2": "flushed before every step (write of >= 2x L2); flush outside the timed events"},
+                   "l2": cold.describe(), "copies": runner.copies},
         "roofline": rl,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -526,7 +579,7 @@ def run_ours(args):
     return 0
 
 
-def summary(torch, tg, ctx, stream, tstream, flush, reg, sms):
+def summary(torch, tg, ctx, stream, tstream, cold, reg, sms):
     """Every other named workload: TFLOP/s and roofline fraction, each timed
     for about a third of a second of device time (cold L2 per step)."""
     out = {}
@@ -534,10 +587,10 @@ def summary(torch, tg, ctx, stream, tstream, flush, reg, sms):
         if name == HEADLINE:
             continue
         probs = factory()
-        runner = Runner(tg, ctx, stream, probs)
-        probe = time_steps(torch, runner, tstream, flush, 3, 2)
+        runner = Runner(tg, ctx, stream, probs, cold.copies(probs))
+        probe = time_steps(torch, runner, tstream, cold, 3, 2)
         steps = int(max(10, min(2000, 0.3e3 / max(statistics.mean(probe), 1e-3))))
-        ms = time_steps(torch, runner, tstream, flush, steps, 3)
+        ms = time_steps(torch, runner, tstream, cold, steps, 3)
         t = statistics.mean(ms) / 1e3
         flops = sum(2.0 * p.M * p.N * p.K for p in probs)
         rl = roofline(probs, t, sms)
@@ -560,6 +613,8 @@ def main():
                     help="which named workload to time (default: the headline bf16 NN 4096^3)")
     ap.add_argument("--no-summary", dest="summary", action="store_false",
                     help="skip the per-workload roofline summary of the other workloads")
+    ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
+                    help="how every timed step starts from a cold L2 (see Cold)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

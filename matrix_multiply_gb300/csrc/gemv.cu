@@ -350,57 +350,103 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_rr_kernel(const GemvArg
     const long long K = a.K;
     const long long r_lo = (long long)blockIdx.x * a.rows_w / gridDim.x;
     const long long r_hi = (long long)(blockIdx.x + 1) * a.rows_w / gridDim.x;
-    const long long nblk = (r_hi - r_lo + 15) / 16;
-    const long long nslab = (K + SLAB - 1) / SLAB;
-    const long long per = warp < nslab ? (nslab - warp + GV_WARPS - 1) / GV_WARPS : 0;   // this warp's steps per block
-    const long long items = nblk * per;
+    const int nblk = (int)((r_hi - r_lo + 15) / 16);
+    const int nslab = (int)((K + SLAB - 1) / SLAB);
+    const int per = warp < nslab ? (nslab - warp + GV_WARPS - 1) / GV_WARPS : 0;   // this warp's steps per block
+    const int items = nblk * per;
     const uint8_t *W = static_cast<const uint8_t *>(a.W);
     const uint8_t *X = static_cast<const uint8_t *>(a.X);
     const uint32_t ring = smem_u32(rr_ring) + (uint32_t)(warp * GV_RR_RING + lane * 16);
-
-    // item i of this warp: block i / per, step warp + 8 (i % per)
-    auto issue = [&](long long i) {
-        const long long blk = i / per;
-        const long long kq = (warp + (long long)GV_WARPS * (i - blk * per)) * SLAB + t * WK;   // this lane's K
-        const long long n0 = r_lo + blk * 16;
-        const uint32_t slot = ring + (uint32_t)((i % S) * SLOT);
-        const long long kb = (K - kq) * WSZ;                       // bytes of the piece inside K
-        const uint32_t wbytes = kb >= 16 ? 16u : kb > 0 ? (uint32_t)kb : 0u;
+    // Per-lane copy state for the next item to issue (block ib, step ij of
+    // this warp, ring slot is): source pointers advanced by additions, byte
+    // counts fixed per block except in the step that reaches past K.
+    const long long wrow = a.ldw * WSZ;                 // bytes between W rows
+    constexpr int WADV = GV_WARPS * SLAB * WSZ;         // bytes between two steps of a warp (W)
+    constexpr int XADV = GV_WARPS * SLAB * 2;           // the same for X
+    const int kbase = warp * SLAB + t * WK;             // this lane's first K
+    const uint8_t *xbase[NT];
+    uint32_t xfull[NT];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const long long n = n0 + g + 8 * h;
-            const bool ok = n < r_hi;
-            cp_async16(slot + h * 512, W + (ok ? (n * a.ldw + kq) * WSZ : 0), ok ? wbytes : 0u);
+    for (int nt = 0; nt < NT; ++nt) {
+        const bool ok = nt * 8 + g < a.rows_x;
+        xfull[nt] = ok ? 16u : 0u;
+        xbase[nt] = ok ? X + ((long long)(nt * 8 + g) * a.ldx + kbase) * 2 : X;
+    }
+    int ib = 0, ij = 0, is = 0, kq = kbase;
+    const uint8_t *wp0 = W, *wp1 = W;
+    const uint8_t *xp[NT];
+    uint32_t w0full = 0, w1full = 0;
+    auto start_block = [&]() {
+        const long long n0 = r_lo + 16LL * ib;
+        const bool ok0 = n0 + g < r_hi, ok1 = n0 + g + 8 < r_hi;
+        w0full = ok0 ? 16u : 0u;
+        w1full = ok1 ? 16u : 0u;
+        wp0 = ok0 ? W + (n0 + g) * wrow + (long long)kbase * WSZ : W;
+        wp1 = ok1 ? W + (n0 + g + 8) * wrow + (long long)kbase * WSZ : W;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) xp[nt] = xbase[nt];
+        kq = kbase;
+    };
+    if (per > 0) start_block();
+    auto issue = [&]() {
+        const uint32_t slot = ring + (uint32_t)(is * SLOT);
+        if ((warp + GV_WARPS * ij + 1) * SLAB <= K) {        // the whole step is inside K (warp-uniform)
+            cp_async16(slot, wp0, w0full);
+            cp_async16(slot + 512, wp1, w1full);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < XL; ++q) cp_async16_l1(slot + (2 + nt * XL + q) * 512, xp[nt] + 16 * q, xfull[nt]);
+        } else {                                              // the step reaching past K
+            const int kw = (int)min(16LL, max(0LL, (K - kq) * WSZ));
+            cp_async16(slot, kw ? wp0 : W, w0full ? (uint32_t)kw : 0u);
+            cp_async16(slot + 512, kw ? wp1 : W, w1full ? (uint32_t)kw : 0u);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < XL; ++q) {
+                    const int kx = (int)min(16LL, max(0LL, (K - (kq + 8 * q)) * 2));
+                    cp_async16_l1(slot + (2 + nt * XL + q) * 512, (kx && xfull[nt]) ? xp[nt] + 16 * q : X,
+                                  xfull[nt] ? (uint32_t)kx : 0u);
+                }
         }
+        if (++is == S) is = 0;
+        if (++ij == per) {
+            ij = 0;
+            ++ib;
+            if (ib < nblk) start_block();
+        } else {
+            wp0 += WADV;
+            wp1 += WADV;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int row = nt * 8 + g;
-#pragma unroll
-            for (int q = 0; q < XL; ++q) {
-                const long long kx = kq + 8 * q;
-                const long long xb = (K - kx) * 2;
-                const uint32_t bytes = row < a.rows_x ? (xb >= 16 ? 16u : xb > 0 ? (uint32_t)xb : 0u) : 0u;
-                cp_async16_l1(slot + (2 + nt * XL + q) * 512, X + (bytes ? ((long long)row * a.ldx + kx) * 2 : 0),
-                              bytes);
-            }
+            for (int nt = 0; nt < NT; ++nt) xp[nt] += XADV;
+            kq += GV_WARPS * SLAB;
         }
     };
 
+    int issued = 0;
 #pragma unroll
     for (int q = 0; q < S - 1; ++q) {
-        if (q < items) issue(q);
+        if (issued < items) {
+            issue();
+            ++issued;
+        }
         cp_async_commit();
     }
-    for (long long blk = 0; blk < nblk; ++blk) {
+    int rs = 0;                                       // ring slot of the item being multiplied
+    for (int blk = 0; blk < nblk; ++blk) {
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-        for (long long j = 0; j < per; ++j) {
-            const long long i = blk * per + j;
-            if (i + S - 1 < items) issue(i + S - 1);
+        for (int j = 0; j < per; ++j) {
+            if (issued < items) {
+                issue();
+                ++issued;
+            }
             cp_async_commit();
-            cp_async_wait<S - 1>();                   // this lane's copies of item i have landed
-            const uint32_t slot = ring + (uint32_t)((i % S) * SLOT);
+            cp_async_wait<S - 1>();                   // this lane's copies of the current item have landed
+            const uint32_t slot = ring + (uint32_t)(rs * SLOT);
+            if (++rs == S) rs = 0;
             uint4 w0, w1;
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w) : "r"(slot));
@@ -427,7 +473,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_rr_kernel(const GemvArg
         }
         __syncthreads();
         const int r = threadIdx.x & 15, c = threadIdx.x >> 4;       // W row r, X row c
-        const long long n = r_lo + blk * 16 + r;
+        const long long n = r_lo + 16LL * blk + r;
         if (c < COLS && c < a.rows_x && n < r_hi) {
             float v = 0.0f;
 #pragma unroll

@@ -13,21 +13,40 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int MMA_K = 16;                       // K of one kind::f16 tcgen05.mma
-constexpr int MMA_THREADS = 192;                // 4 epilogue warps, TMA warp, MMA warp
+constexpr int MMA_THREADS = 192;                // 4 epilogue warps, TMA warp, MMA warp (plain GEMM kernels)
 constexpr int SMEM_LIMIT = 232448;              // max dynamic shared memory per block
 constexpr int EPI_STAGE_BYTES = 4096;           // one 32 x 32 output chunk (fp32 worst case)
 
-// Epilogue staging per warp: two chunk buffers (one TMA store may still be
-// reading the other), except for the one-CTA 192-wide tile, whose 40 KB
-// stages leave room for a fifth stage only with one buffer (its K loop is
-// bound by the latency the ring covers, its single wave drains once).  The
-// plain-store path's 32 x 33-float transpose buffer fits either way.
-__host__ __device__ constexpr int epi_bufs(int bn, int cg) { return (bn == 192 && cg == 1) ? 1 : 2; }
-__host__ __device__ constexpr int epi_warp_bytes(int bn, int cg) { return epi_bufs(bn, cg) == 1 ? 5120 : 8192; }
-__host__ __device__ constexpr int epi_smem(int bn, int cg) { return 4 * epi_warp_bytes(bn, cg); }   // 4 epilogue warps
-__host__ __device__ constexpr int smem_reserve(int bn, int cg)   // alignment slack + barriers + epilogue staging
+// Epilogue warps: four (warp w reads TMEM lanes 32w..32w+31), or, for the
+// fused bias/activation epilogue, eight -- two per TMEM lane quarter, each
+// taking every other 32-column chunk -- so that the CUDA-core epilogue work
+// of a tile that no next tile hides takes half as long.  The one-CTA
+// 192-wide tile keeps four (its fifth pipeline stage needs the space).
+__host__ __device__ constexpr int epi_warps(int bn, int cg, bool epi) { return (epi && !(bn == 192 && cg == 1)) ? 8 : 4; }
+__host__ __device__ constexpr int mma_threads(int bn, int cg, bool epi) { return (epi_warps(bn, cg, epi) + 2) * 32; }
+// Epilogue staging per warp: with four warps two chunk buffers (one TMA
+// store may still be reading the other), except for the one-CTA 192-wide
+// tile, whose 40 KB stages leave room for a fifth stage only with one
+// buffer (its K loop is bound by the latency the ring covers, its single
+// wave drains once); with eight warps one buffer each.  The plain-store
+// path's 32 x 32-float transpose buffer is one such buffer, so a warp's
+// staging never overlaps another warp's (a launch may use both paths: C by
+// plain stores, split-K partial tiles by TMA stores).  Buffers start at
+// multiples of 1024 bytes, the alignment the swizzled TMA layouts assume
+// (the swizzle uses the absolute shared address).
+__host__ __device__ constexpr int epi_bufs(int bn, int cg, bool epi)
 {
-    return 1024 + 256 + epi_smem(bn, cg);
+    return (epi_warps(bn, cg, epi) == 8 || (bn == 192 && cg == 1)) ? 1 : 2;
+}
+__host__ __device__ constexpr int epi_warp_bytes(int bn, int cg, bool epi)
+{
+    return epi_warps(bn, cg, epi) == 8 ? EPI_STAGE_BYTES : epi_bufs(bn, cg, epi) == 1 ? 5120 : 8192;
+}
+__host__ __device__ constexpr int epi_smem(int bn, int cg, bool epi) { return epi_warps(bn, cg, epi) * epi_warp_bytes(bn, cg, epi); }
+
+__host__ __device__ constexpr int smem_reserve(int bn, int cg, bool epi)   // alignment slack + barriers + epilogue staging
+{
+    return 1024 + 256 + epi_smem(bn, cg, epi);
 }
 
 // One pipeline stage of a CTA: its 128 rows of A and its share of B (all BN
@@ -38,15 +57,15 @@ __host__ __device__ constexpr int tmem_cols(int bn)
 {
     return (2 * bn <= 128) ? 128 : (2 * bn <= 256) ? 256 : 512;
 }
-__host__ __device__ constexpr int mma_stages(int bn, int cg)
+__host__ __device__ constexpr int mma_stages(int bn, int cg, bool epi = false)
 {
-    return ((SMEM_LIMIT - smem_reserve(bn, cg)) / stage_bytes(bn, cg)) > 8
+    return ((SMEM_LIMIT - smem_reserve(bn, cg, epi)) / stage_bytes(bn, cg)) > 8
                ? 8
-               : ((SMEM_LIMIT - smem_reserve(bn, cg)) / stage_bytes(bn, cg));
+               : ((SMEM_LIMIT - smem_reserve(bn, cg, epi)) / stage_bytes(bn, cg));
 }
-__host__ __device__ constexpr int mma_smem_bytes(int bn, int cg)
+__host__ __device__ constexpr int mma_smem_bytes(int bn, int cg, bool epi = false)
 {
-    return mma_stages(bn, cg) * stage_bytes(bn, cg) + smem_reserve(bn, cg);
+    return mma_stages(bn, cg, epi) * stage_bytes(bn, cg) + smem_reserve(bn, cg, epi);
 }
 
 // Device-side arguments of the tensor-core kernel (the two TMA descriptors
@@ -108,6 +127,10 @@ struct MmaLaunch {
     // one cluster and add their partial tiles through distributed shared
     // memory (BN 64 or 128, one CTA per unit: grid == args.total_units)
     int csplit;
+    // clusters of two vertically adjacent one-CTA tiles sharing B by TMA
+    // multicast (args.tiles_m counts tile pairs; B descriptors with 64-wide
+    // boxes; whole K per unit)
+    int mcb;
     int grid;    // CTAs (a multiple of cg)
     CUtensorMap tmA, tmB, tmC, tmW;   // A, B, C and the split-K workspace
     MmaArgs args;

@@ -309,11 +309,12 @@ __device__ __forceinline__ void store_direct(const MmaArgs &a, int b, long long 
 }
 
 // C layouts TMA cannot address (rows not 16-byte multiples): the warp's
-// 32 x 32 chunk is transposed through shared memory (32 x 33 floats, so
-// both the row-wise and the column-wise accesses hit 32 distinct banks) and
-// every global access touches one contiguous 32-element row segment per
-// instruction instead of 32 separate rows.
-constexpr int XPOSE_LD = 33;
+// 32 x 32 chunk is transposed through shared memory and every global access
+// touches one contiguous 32-element row segment per instruction instead of
+// 32 separate rows.  Element (r, c) sits at r * 32 + (c ^ r): for a fixed r
+// the 32 columns, and for a fixed c the 32 rows, fall in 32 distinct banks,
+// and the buffer is exactly one 4 KB staging buffer.
+__device__ __forceinline__ int xp(int r, int c) { return r * 32 + (c ^ r); }
 
 // Row r of the chunk in column `lane`: C + ((b * stride_c + (row0 + r) * ldc + col) elements.
 // Every access of the two functions below is unrolled and predicated (no
@@ -351,10 +352,10 @@ __device__ __forceinline__ void apply_alpha_beta_staged(const MmaArgs &a, float 
         }
     }
 #pragma unroll
-    for (int r = 0; r < 32; ++r) buf[r * XPOSE_LD + lane] = c[r];
+    for (int r = 0; r < 32; ++r) buf[xp(r, lane)] = c[r];
     __syncwarp();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = fmaf(a.beta, buf[lane * XPOSE_LD + j], a.alpha * v[j]);
+    for (int j = 0; j < 32; ++j) v[j] = fmaf(a.beta, buf[xp(lane, j)], a.alpha * v[j]);
     __syncwarp();
 }
 
@@ -363,14 +364,14 @@ __device__ __forceinline__ void store_staged(const MmaArgs &a, float *buf, int l
                                              long long col0, const float (&v)[32])
 {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) buf[lane * XPOSE_LD + j] = v[j];
+    for (int j = 0; j < 32; ++j) buf[xp(lane, j)] = v[j];
     __syncwarp();
     const long long col = col0 + lane;
     const long long nrows = (col < a.N) ? min(32LL, a.M - row0) : 0LL;
     const long long first = (long long)b * a.stride_c + row0 * a.ldc + col;
     float w[32];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) w[r] = buf[r * XPOSE_LD + lane];
+    for (int r = 0; r < 32; ++r) w[r] = buf[xp(r, lane)];
     if (a.c_dtype == TC_F32) {
         float *dst = static_cast<float *>(a.C) + first;
 #pragma unroll
@@ -558,13 +559,21 @@ __device__ __forceinline__ void csplit_reduce(const MmaArgs &a, const uint8_t *p
 // adds them in a second kernel instead; the integer sums, their one rounding
 // and everything after are the same.
 //
+// MCB: a cluster of two one-CTA tiles, vertically adjacent (the same B
+// columns): each CTA loads its own A and every other 64-column chunk of B,
+// multicast into both CTAs' shared memory, so L2 serves each B block once
+// for two SMs (narrow N, where every tile row reads all of B).  Each CTA
+// issues its own one-CTA MMAs; a stage is refilled only after both CTAs'
+// MMAs have released it (each MMA commit arrives on both CTAs' "empty"
+// barriers, which count two arrivals).
+//
 // CSPLIT: split-K inside one launch.  The grid holds one unit per CTA and
 // the S K slices of a tile form one cluster (slice = cluster rank); each
 // slice's partial tile stays in its CTA's shared memory and csplit_reduce
 // adds them across the cluster, so no partial tile goes through global
 // memory and no second kernel runs.
-template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false, bool CSPLIT = false>
-__global__ void __launch_bounds__(MMA_THREADS, 1)
+template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false, bool CSPLIT = false, bool MCB = false>
+__global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                const MmaArgs args, const __grid_constant__ TableOf<GROUPED> gt)
@@ -572,7 +581,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     constexpr int BNL = BN / CG;                   // B columns loaded by this CTA
     constexpr int STAGE = stage_bytes(BN, CG);
     constexpr int A_BYTES = BM * BK * 2;
-    constexpr int S = mma_stages(BN, CG);
+    constexpr int S = mma_stages(BN, CG, EPI);
+    constexpr int EW = epi_warps(BN, CG, EPI);     // epilogue warps 0..EW-1, then the TMA and MMA warps
+    constexpr int TMA_WARP = EW, MMA_WARP = EW + 1;
+    constexpr int CSTEP = EW / 4;                  // chunks between two chunks of one epilogue warp
     constexpr int TCOLS = I8ACC ? 512 : tmem_cols(BN);
     constexpr int ACC_STRIDE = I8ACC ? BN : TCOLS / 2;   // TMEM columns between the two accumulators
     constexpr uint32_t RUN_COL = 2 * BN;           // I8ACC: the running int32 sums
@@ -581,14 +593,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     static_assert(!CSPLIT || BM * csplit_ld<BN>() * 4 <= S * STAGE, "the partial tile fits in the idle ring");
     constexpr int CHUNKS = BN / 32;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
+    static_assert(!MCB || (CG == 1 && !GROUPED && !I8ACC && !CSPLIT), "multicast B: one-CTA tiles, whole K");
+    constexpr int CL = (CG == 2 || MCB) ? 2 : 1;  // CTAs per cluster (a pair, or two multicast tiles)
     static_assert(BNL % 64 == 0 && BN <= 256, "each CTA's B share must be whole 64-column boxes");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *cstage = smem + S * STAGE;            // epilogue staging, 2 x 4 KB per warp
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + epi_smem(BN, CG));
+    uint8_t *cstage = smem + S * STAGE;            // epilogue staging
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + epi_smem(BN, CG, EPI));
     uint64_t *full_bar = bars;
     uint64_t *empty_bar = bars + S;
     uint64_t *tfull_bar = bars + 2 * S;
@@ -599,24 +613,24 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const int cluster = blockIdx.x / CG;
-    const int nclusters = gridDim.x / CG;
+    const uint32_t rank = (CL == 2) ? cluster_ctarank() : 0u;
+    const int cluster = blockIdx.x / CL;
+    const int nclusters = gridDim.x / CL;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full_bar[i]), 1);
-            mbar_init(smem_u32(&empty_bar[i]), 1);
+            mbar_init(smem_u32(&empty_bar[i]), MCB ? 2 : 1);    // MCB: both CTAs' MMAs
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull_bar[i]), 1);
-            mbar_init(smem_u32(&tempty_bar[i]), 4 * CG);    // one arrival per epilogue warp
+            mbar_init(smem_u32(&tempty_bar[i]), EW * CG);   // one arrival per epilogue warp
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == TMA_WARP && lane == 0) {
         if constexpr (!GROUPED) {
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
@@ -636,13 +650,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CG == 2) cluster_sync();     // the peer's barriers exist before anyone signals them
+    if (CL == 2) cluster_sync();     // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const Watch watch{abort_flag, args.status, args.timeout_ns};
 
-    if (warp == 4) {
+    if (warp == TMA_WARP) {
         // ------------------------------------------------ TMA producer
         // Its loop per K block is short too (the copies it issues per K block
         // pace it): barrier and stage addresses come from bases computed once.
@@ -668,8 +682,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     a_3d = b_3d = false;
                     a_chunked = b_chunked = false;
                 }
-                const int m0 = w.tm * (BM * CG) + (int)rank * BM;
-                const int n0 = w.tn * BN + (int)rank * BNL;
+                const int m0 = w.tm * (BM * CL) + (int)rank * BM;
+                const int n0 = w.tn * BN + (CG == 2 ? (int)rank * BNL : 0);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bar(empty0 + 8 * stage, ph ^ 1u, watch, W_EMPTY)) {
                         ok = false;
@@ -707,7 +721,20 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                         load(mapA, a_3d, sa, m0, k0);
                         load(mapA, a_3d, sa + 8192, m0 + 64, k0);
                     }
-                    if (b_kmajor) {
+                    if constexpr (MCB) {
+                        // every other 64-wide chunk of B, to both CTAs (64-row
+                        // or one-chunk boxes: chunk j lands 8 KB after chunk j-1)
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j) {
+                            if ((j & 1) != (int)rank) continue;
+                            if (b_kmajor)
+                                tma_load_2d_mc(sb + j * 8192, mapB, fb, k0, n0 + 64 * j, (uint16_t)0x3);
+                            else if (b_chunked)
+                                tma_load_3d_mc(sb + j * 8192, mapB, fb, 0, k0, n0 / 64 + j, (uint16_t)0x3);
+                            else
+                                tma_load_2d_mc(sb + j * 8192, mapB, fb, n0 + 64 * j, k0, (uint16_t)0x3);
+                        }
+                    } else if (b_kmajor) {
                         load(mapB, b_3d, sb, k0, n0);
                     } else if (b_chunked) {
                         load_chunks(mapB, sb, n0);
@@ -722,21 +749,21 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     }
                 }
             }
-            if (!ok && rank == 0) {
+            if (!ok && (CG == 1 || rank == 0)) {
                 // let the copies already issued land before shared memory is released
                 for (uint32_t i = (issued > (uint32_t)S ? issued - S : 0u); i < issued; ++i)
                     drain_wait(smem_u32(&full_bar[i % S]), (i / S) & 1u);
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issuer (even CTA of a pair)
         // One thread feeds the tensor core, and its work between two MMAs
         // paces the K loop: rebuilding both shared-memory descriptors per
         // MMA cost ~3 % of the square bf16 GEMM's time on GB300.  Each
         // descriptor is built once per unit and then advanced by additions,
         // and the ring position is stepped rather than divided out.
-        if (lane == 0 && rank == 0) {
+        if (lane == 0 && (CG == 1 || rank == 0)) {
             uint32_t stage = 0, ph = 0, local = 0;
             bool ok = true;
             int hint = 0;
@@ -788,7 +815,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                             else
                                 mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
                         }
-                        if (CG == 1)
+                        if (MCB)
+                            mma_commit_mc(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
+                        else if (CG == 1)
                             mma_commit(smem_u32(&empty_bar[stage]));
                         else
                             mma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
@@ -818,11 +847,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue warps 0-3
+        // ------------------------------------------------ epilogue warps 0..EW-1
+        // warp w reads TMEM lane quarter w % 4 (tile rows 32 (w % 4) ..) and,
+        // with eight warps, chunks w / 4, w / 4 + 2, ...
         uint32_t local = 0, ebuf = 0;
-        const int row_in_tile = (int)rank * BM + warp * 32 + lane;
-        constexpr int EBUFS = epi_bufs(BN, CG);
-        uint8_t *my_stage = cstage + warp * epi_warp_bytes(BN, CG);
+        const int quarter = warp & 3, chunk0 = warp >> 2;
+        const int row_in_tile = (int)rank * BM + quarter * 32 + lane;
+        constexpr int EBUFS = epi_bufs(BN, CG, EPI);
+        constexpr int LAST_C0 = CHUNKS - CSTEP;        // this warp's last chunk: LAST_C0 + chunk0
+        static_assert(CHUNKS % CSTEP == 0, "chunks split evenly between the warps of a lane quarter");
+        uint8_t *my_stage = cstage + warp * epi_warp_bytes(BN, CG, EPI);
         // The warp's staging is either its TMA chunk buffers (two that
         // alternate over the stores actually issued, a buffer refilled only
         // after one newer store was committed; or one, refilled after its
@@ -904,8 +938,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + acc * ACC_STRIDE;
-                const long long row = (long long)w.tm * (BM * CG) + row_in_tile;
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_STRIDE;
+                const long long row = (long long)w.tm * (BM * CL) + row_in_tile;
                 // accumulator fully read: hand it back to the MMA warp (not after
                 // this CTA's last segment: nothing waits for it then, and the
                 // arrival would sit on the kernel's final critical path)
@@ -928,16 +962,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     // int32 to the running sums in TMEM columns RUN_COL.. of the
                     // same lanes, and after the last slice the exact sum is
                     // rounded once to fp32 and goes through the epilogue.
-                    const uint32_t raddr = tmem_base + ((uint32_t)(warp * 32) << 16) + RUN_COL;
+                    const uint32_t raddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + RUN_COL;
                     const bool first = sg == 0, last = sg + 1 == nseg;
 #pragma unroll 1
-                    for (int c = 0; c < CHUNKS; ++c) {
+                    for (int c = chunk0; c < CHUNKS; c += CSTEP) {
                         uint32_t r[32], q[32];
                         __syncwarp();
                         tmem_ld_32x32b_x32(taddr + c * 32, r);
                         if (!first) tmem_ld_32x32b_x32(raddr + c * 32, q);
                         tmem_ld_wait();
-                        if (c == CHUNKS - 1) release();
+                        if (c == LAST_C0 + chunk0) release();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int x = __float2int_rn(__uint_as_float(r[j]));
@@ -955,12 +989,12 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     if (!last) tmem_st_wait();
                 } else if (w.S == 1) {
 #pragma unroll 1
-                    for (int c = 0; c < CHUNKS; ++c) {
+                    for (int c = chunk0; c < CHUNKS; c += CSTEP) {
                         uint32_t r[32];
                         __syncwarp();
                         tmem_ld_32x32b_x32(taddr + c * 32, r);
                         tmem_ld_wait();
-                        if (c == CHUNKS - 1) release();
+                        if (c == LAST_C0 + chunk0) release();
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -971,14 +1005,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     // CTA's shared memory.  The ring is idle: every copy into it
                     // was consumed by an MMA, and every MMA has completed (this
                     // accumulator's commit).  csplit_reduce adds the slices.
-                    float *red = reinterpret_cast<float *>(smem) + (warp * 32 + lane) * csplit_ld<BN>();
+                    float *red = reinterpret_cast<float *>(smem) + (quarter * 32 + lane) * csplit_ld<BN>();
 #pragma unroll 1
-                    for (int c = 0; c < CHUNKS; ++c) {
+                    for (int c = chunk0; c < CHUNKS; c += CSTEP) {
                         uint32_t r[32];
                         __syncwarp();
                         tmem_ld_32x32b_x32(taddr + c * 32, r);
                         tmem_ld_wait();
-                        if (c == CHUNKS - 1) release();
+                        if (c == LAST_C0 + chunk0) release();
                         float4 *dst = reinterpret_cast<float4 *>(red + c * 32);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -990,14 +1024,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     // slot (row-major, (BM * CG) x BN per unit); the reduction
                     // kernel sums the slices in slice order afterwards
                     const long long wrow0 =
-                        (long long)(w.ufirst + w.s - args.split_base) * (BM * CG) + (int)rank * BM + warp * 32;
+                        (long long)(w.ufirst + w.s - args.split_base) * (BM * CG) + (int)rank * BM + quarter * 32;
 #pragma unroll 1
-                    for (int c = 0; c < CHUNKS; ++c) {
+                    for (int c = chunk0; c < CHUNKS; c += CSTEP) {
                         uint32_t r[32];
                         __syncwarp();
                         tmem_ld_32x32b_x32(taddr + c * 32, r);
                         tmem_ld_wait();
-                        if (c == CHUNKS - 1) release();
+                        if (c == LAST_C0 + chunk0) release();
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -1020,8 +1054,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         cluster_sync();              // every slice's partial tile is in its CTA's shared memory
         csplit_reduce<BN, EPI>(args, smem);
         cluster_sync();              // no CTA releases its shared memory while a peer may read it
-    } else if (CG == 2) {
-        cluster_sync();              // no CTA leaves while its peer may still signal it
+    } else if (CL == 2) {
+        cluster_sync();              // no CTA leaves while its peer may still signal it or copy into it
     }
     tc_fence_after();
     if (warp == 0) {
@@ -1032,11 +1066,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
 }
 
-template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false, bool CSPLIT = false>
+template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false, bool CSPLIT = false,
+          bool MCB = false>
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
-    constexpr auto kern = mma_kernel<BN, CG, GROUPED, EPI, I8ACC, CSPLIT>;
-    constexpr int smem = mma_smem_bytes(BN, CG);
+    constexpr auto kern = mma_kernel<BN, CG, GROUPED, EPI, I8ACC, CSPLIT, MCB>;
+    constexpr int smem = mma_smem_bytes(BN, CG, EPI);
+    constexpr int threads = mma_threads(BN, CG, EPI);
     // per device: the kernel's shared-memory limit is raised once (callers
     // of the context-free entry point may race here from several threads;
     // setting the attribute twice is harmless)
@@ -1054,16 +1090,16 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
         }
         configured[dev].store(true, std::memory_order_release);
     }
-    const int cluster = CSPLIT ? L.args.seg0_split : CG;
+    const int cluster = CSPLIT ? L.args.seg0_split : MCB ? 2 : CG;
     if (CSPLIT && (cluster < 2 || cluster > 16 || L.grid != L.args.total_units || L.grid % cluster != 0))
         return cudaErrorInvalidValue;
     if (cluster == 1) {
-        kern<<<L.grid, MMA_THREADS, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+        kern<<<L.grid, threads, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid, 1, 1);
-    cfg.blockDim = dim3(MMA_THREADS, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1283,6 +1319,18 @@ cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st)
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
     const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE || L.args.col_scale != nullptr;
+    if (L.mcb) {
+        if (L.cg != 1 || L.i8acc || L.csplit || L.grid % 2 != 0) return cudaErrorInvalidValue;
+        switch (L.bn) {
+        case 128: return epi ? launch_kernel<128, 1, false, true, false, false, true>(L, st)
+                             : launch_kernel<128, 1, false, false, false, false, true>(L, st);
+        case 192: return epi ? launch_kernel<192, 1, false, true, false, false, true>(L, st)
+                             : launch_kernel<192, 1, false, false, false, false, true>(L, st);
+        case 256: return epi ? launch_kernel<256, 1, false, true, false, false, true>(L, st)
+                             : launch_kernel<256, 1, false, false, false, false, true>(L, st);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (L.csplit) {
         if (L.cg != 1 || L.i8acc) return cudaErrorInvalidValue;
         switch (L.bn) {
