@@ -167,7 +167,6 @@ struct Plan {
     int bn = 256, cg = 1, split = 1, grid = 1, group_m = 8;
     bool i8acc = false;        // int8: exact K slices summed in TMEM (one unit per tile)
     bool csplit = false;       // split-K as clusters of K slices reduced on chip (seg0_split CTAs per cluster)
-    bool mcb = false;          // clusters of two vertically adjacent one-CTA tiles sharing B by multicast
     // the skinny-product kernel (gemv.cu): X = op(A) and W = B (rows N), or,
     // when swapped, X = B^T (N rows) and W = A (rows M); K split over a
     // cluster of gemv_ks CTAs
@@ -196,9 +195,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // the reduction kernel instead of a cluster reduction on chip) gemv=0 (a
 // product with at most 16 rows on one side stays on the tensor-core kernel)
 // gemv_ks=<1|2|4|8> (the skinny-product kernel's cluster form with this K
-// split) gemv_rr=0 (its cluster form instead of the row-range form) mcb=1
-// (one-CTA tiles in vertically adjacent pairs that share B by TMA multicast;
-// whole K per tile).
+// split) gemv_rr=0 (its cluster form instead of the row-range form).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -212,7 +209,6 @@ struct Force {
     int i8acc = -1;
     int csplit = -1;
     int gemv = -1, gemv_ks = 0, gemv_rr = -1;
-    int mcb = 0;
 };
 
 Force read_force()
@@ -252,7 +248,6 @@ Force read_force()
         else if (k == "gemv") f.gemv = std::atoi(v.c_str());
         else if (k == "gemv_ks") f.gemv_ks = std::atoi(v.c_str());
         else if (k == "gemv_rr") f.gemv_rr = std::atoi(v.c_str());
-        else if (k == "mcb") f.mcb = std::atoi(v.c_str());
     }
     return f;
 }
@@ -472,16 +467,7 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
             }
         }
     }
-    if (f.mcb && n.batch == 1) {
-        // one-CTA tiles, two per cluster along M (the same B columns), whole K
-        if (!(bn == 128 || bn == 192 || bn == 256)) bn = f.bn ? f.bn : 192;
-        cg = 1;
-        p.mcb = true;
-        p.csplit = false;
-        const int64_t units = cdiv(d->M, 2 * BM) * cdiv(d->N, bn);
-        sc = {units, units, 1, 1, 0.0};
-    }
-    const int workers = (cg == 2 || p.mcb) ? std::max(num_sms / 2, 1) : num_sms;   // tiles (clusters) in flight
+    const int workers = cg == 2 ? std::max(num_sms / 2, 1) : num_sms;   // tiles in flight
     if (bn == 0) return TC_ERR_VARIANT;
     p.bn = bn;
     p.cg = cg;
@@ -496,11 +482,11 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
     p.grid = (int)std::min<int64_t>(p.units, workers);
     if (f.grid > 0) p.grid = (int)std::min<int64_t>(f.grid, p.units);
     if (p.csplit) p.grid = (int)p.units;           // one CTA per (tile, slice): clusters of slices
-    p.grid *= (cg == 2 || p.mcb) ? 2 : 1;          // CTAs
+    p.grid *= cg;                                  // CTAs
     p.group_m = f.group_m > 0 ? f.group_m : 4;
     p.tma_store = !f.direct_store;
     std::snprintf(buf, sizeof buf, "tcgen05_%s_%s_%s_%dx%d%s%s%s%s", lay, dt, ct, BM * cg, bn,
-                  cg == 2 ? "_pair" : p.mcb ? "_mcb" : "", sc.seg0_split > 1 ? (p.csplit ? "_csplit" : "_splitk") : "",
+                  cg == 2 ? "_pair" : "", sc.seg0_split > 1 ? (p.csplit ? "_csplit" : "_splitk") : "",
                   p.pack_a ? "_packA" : "",
                   p.pack_b ? "_packB" : "");
     p.name = buf;
@@ -740,7 +726,6 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     L.cg = p.cg;
     L.i8acc = p.i8acc ? 1 : 0;
     L.csplit = p.csplit ? 1 : 0;
-    L.mcb = p.mcb ? 1 : 0;
     L.grid = p.grid;
     if (p.cg == 2) {
         // no more pairs than can be resident at once (a persistent grid)
@@ -754,7 +739,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     a.N = d->N;
     a.K = d->K;
     a.num_kb = (int)cdiv(d->K, BK);
-    a.tiles_m = (int)cdiv(d->M, BM * (p.mcb ? 2 : p.cg));
+    a.tiles_m = (int)cdiv(d->M, BM * p.cg);
     a.tiles_n = (int)cdiv(d->N, p.bn);
     a.tiles_per_batch = a.tiles_m * a.tiles_n;
     a.batch = (int)n.batch;
@@ -806,7 +791,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     bool ok;
     if (a.a_kmajor) {
         // a one-CTA tile taller than A: copy only A's rows (rounded up to 8)
-        const uint32_t rows = (p.cg == 1 && !p.mcb && d->M < BM && !read_force().no_short_a)
+        const uint32_t rows = (p.cg == 1 && d->M < BM && !read_force().no_short_a)
                                   ? (uint32_t)round_up((size_t)d->M, 8)
                                   : (uint32_t)BM;
         a.a_short_bytes = (int)((BM - rows) * BK * 2);
@@ -817,13 +802,12 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     }
     if (ok) {
         if (a.b_kmajor) {
-            // (multicast B: 64-row boxes, one per chunk a CTA sends)
             ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->K, d->N, ldb_use, a.b_3d, n.batch, sb, 64,
-                            (uint32_t)(p.mcb ? 64 : p.bn / p.cg));
+                            (uint32_t)(p.bn / p.cg));
         } else {
             a.b_chunked = chunk_ok && !a.b_3d &&
                           encode_chunked(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use,
-                                         (uint32_t)(p.mcb ? 1 : p.bn / p.cg / 64));
+                                         (uint32_t)(p.bn / p.cg / 64));
             ok = a.b_chunked ||
                  encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, a.b_3d, n.batch, sb, 64, 64);
         }

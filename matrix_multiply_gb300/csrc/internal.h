@@ -127,10 +127,6 @@ struct MmaLaunch {
     // one cluster and add their partial tiles through distributed shared
     // memory (BN 64 or 128, one CTA per unit: grid == args.total_units)
     int csplit;
-    // clusters of two vertically adjacent one-CTA tiles sharing B by TMA
-    // multicast (args.tiles_m counts tile pairs; B descriptors with 64-wide
-    // boxes; whole K per unit)
-    int mcb;
     int grid;    // CTAs (a multiple of cg)
     CUtensorMap tmA, tmB, tmC, tmW;   // A, B, C and the split-K workspace
     MmaArgs args;

@@ -273,40 +273,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
-// TMA load delivered to the same shared offset in every CTA of `mask`
-// (this CTA's own cluster: the data come from this GPU's memory), each copy
-// completing on the mbarrier at the same offset in its CTA
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int32_t c0, int32_t c1,
-                                               uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *tmap, uint32_t bar, int32_t c0, int32_t c1,
-                                               int32_t c2, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-        : "memory");
-}
-
-// one-CTA MMAs: arrive on the mbarrier at the same offset in every CTA of
-// `mask` once the MMAs this thread issued have completed
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(mask)
-        : "memory");
-}
-
 // TMEM allocation shared by the CTA pair: one warp of each CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
 {

@@ -559,20 +559,12 @@ __device__ __forceinline__ void csplit_reduce(const MmaArgs &a, const uint8_t *p
 // adds them in a second kernel instead; the integer sums, their one rounding
 // and everything after are the same.
 //
-// MCB: a cluster of two one-CTA tiles, vertically adjacent (the same B
-// columns): each CTA loads its own A and every other 64-column chunk of B,
-// multicast into both CTAs' shared memory, so L2 serves each B block once
-// for two SMs (narrow N, where every tile row reads all of B).  Each CTA
-// issues its own one-CTA MMAs; a stage is refilled only after both CTAs'
-// MMAs have released it (each MMA commit arrives on both CTAs' "empty"
-// barriers, which count two arrivals).
-//
 // CSPLIT: split-K inside one launch.  The grid holds one unit per CTA and
 // the S K slices of a tile form one cluster (slice = cluster rank); each
 // slice's partial tile stays in its CTA's shared memory and csplit_reduce
 // adds them across the cluster, so no partial tile goes through global
 // memory and no second kernel runs.
-template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false, bool CSPLIT = false, bool MCB = false>
+template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false, bool CSPLIT = false>
 __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -593,8 +585,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     static_assert(!CSPLIT || BM * csplit_ld<BN>() * 4 <= S * STAGE, "the partial tile fits in the idle ring");
     constexpr int CHUNKS = BN / 32;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
-    static_assert(!MCB || (CG == 1 && !GROUPED && !I8ACC && !CSPLIT), "multicast B: one-CTA tiles, whole K");
-    constexpr int CL = (CG == 2 || MCB) ? 2 : 1;  // CTAs per cluster (a pair, or two multicast tiles)
+    constexpr int CL = CG;                        // CTAs per cluster
     static_assert(BNL % 64 == 0 && BN <= 256, "each CTA's B share must be whole 64-column boxes");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 
@@ -620,7 +611,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full_bar[i]), 1);
-            mbar_init(smem_u32(&empty_bar[i]), MCB ? 2 : 1);    // MCB: both CTAs' MMAs
+            mbar_init(smem_u32(&empty_bar[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull_bar[i]), 1);
@@ -721,20 +712,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
                         load(mapA, a_3d, sa, m0, k0);
                         load(mapA, a_3d, sa + 8192, m0 + 64, k0);
                     }
-                    if constexpr (MCB) {
-                        // every other 64-wide chunk of B, to both CTAs (64-row
-                        // or one-chunk boxes: chunk j lands 8 KB after chunk j-1)
-#pragma unroll
-                        for (int j = 0; j < BN / 64; ++j) {
-                            if ((j & 1) != (int)rank) continue;
-                            if (b_kmajor)
-                                tma_load_2d_mc(sb + j * 8192, mapB, fb, k0, n0 + 64 * j, (uint16_t)0x3);
-                            else if (b_chunked)
-                                tma_load_3d_mc(sb + j * 8192, mapB, fb, 0, k0, n0 / 64 + j, (uint16_t)0x3);
-                            else
-                                tma_load_2d_mc(sb + j * 8192, mapB, fb, n0 + 64 * j, k0, (uint16_t)0x3);
-                        }
-                    } else if (b_kmajor) {
+                    if (b_kmajor) {
                         load(mapB, b_3d, sb, k0, n0);
                     } else if (b_chunked) {
                         load_chunks(mapB, sb, n0);
@@ -815,9 +793,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
                             else
                                 mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
                         }
-                        if (MCB)
-                            mma_commit_mc(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
-                        else if (CG == 1)
+                        if (CG == 1)
                             mma_commit(smem_u32(&empty_bar[stage]));
                         else
                             mma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)0x3);
@@ -1066,11 +1042,10 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     }
 }
 
-template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false, bool CSPLIT = false,
-          bool MCB = false>
+template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = false, bool CSPLIT = false>
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
-    constexpr auto kern = mma_kernel<BN, CG, GROUPED, EPI, I8ACC, CSPLIT, MCB>;
+    constexpr auto kern = mma_kernel<BN, CG, GROUPED, EPI, I8ACC, CSPLIT>;
     constexpr int smem = mma_smem_bytes(BN, CG, EPI);
     constexpr int threads = mma_threads(BN, CG, EPI);
     // per device: the kernel's shared-memory limit is raised once (callers
@@ -1090,7 +1065,7 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
         }
         configured[dev].store(true, std::memory_order_release);
     }
-    const int cluster = CSPLIT ? L.args.seg0_split : MCB ? 2 : CG;
+    const int cluster = CSPLIT ? L.args.seg0_split : CG;
     if (CSPLIT && (cluster < 2 || cluster > 16 || L.grid != L.args.total_units || L.grid % cluster != 0))
         return cudaErrorInvalidValue;
     if (cluster == 1) {
@@ -1319,18 +1294,6 @@ cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st)
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
 {
     const bool epi = L.args.bias != nullptr || L.args.act != TC_ACT_NONE || L.args.col_scale != nullptr;
-    if (L.mcb) {
-        if (L.cg != 1 || L.i8acc || L.csplit || L.grid % 2 != 0) return cudaErrorInvalidValue;
-        switch (L.bn) {
-        case 128: return epi ? launch_kernel<128, 1, false, true, false, false, true>(L, st)
-                             : launch_kernel<128, 1, false, false, false, false, true>(L, st);
-        case 192: return epi ? launch_kernel<192, 1, false, true, false, false, true>(L, st)
-                             : launch_kernel<192, 1, false, false, false, false, true>(L, st);
-        case 256: return epi ? launch_kernel<256, 1, false, true, false, false, true>(L, st)
-                             : launch_kernel<256, 1, false, false, false, false, true>(L, st);
-        default: return cudaErrorInvalidValue;
-        }
-    }
     if (L.csplit) {
         if (L.cg != 1 || L.i8acc) return cudaErrorInvalidValue;
         switch (L.bn) {

@@ -149,9 +149,7 @@ def test_alpha_beta(ctx, alpha, beta, c):
                                   "grid=3", "group_m=1", "group_m=3 bn=64", "sms=5 tail=2",
                                   "sms=5 tail=3 bn=64", "sms=7 bn=256 tail=2 pack=1", "cg=2",
                                   "cg=2 bn=128", "cg=2 sms=6 tail=2", "cg=2 grid=1 pack=1",
-                                  "store=direct", "store=direct cg=2 sms=6 tail=2", "store=direct split=3",
-                                  "mcb=1", "mcb=1 bn=128", "mcb=1 bn=256", "mcb=1 pack=1", "mcb=1 grid=2",
-                                  "mcb=1 chunk=0", "mcb=1 store=direct"])
+                                  "store=direct", "store=direct cg=2 sms=6 tail=2", "store=direct split=3"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_forced_variants(ctx, force, spec, ta, tb):
     force(spec)
@@ -221,7 +219,7 @@ def test_padded_leading_dimensions(ctx):
 # ----------------------------------------------------- exactness and edges
 
 @pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "bn=128 split=4 csplit=0",
-                                  "bn=64 split=16", "pack=1 bn=256 split=2", "mcb=1", "mcb=1 bn=128",
+                                  "bn=64 split=16", "pack=1 bn=256 split=2",
                                   "sms=5 tail=3", "cg=2", "cg=2 bn=128 sms=4 tail=2", "store=direct"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
@@ -236,7 +234,7 @@ def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
 
 
 @pytest.mark.parametrize("spec", ["", "cg=2 bn=256", "cg=2 bn=128", "cg=1 bn=256", "cg=1 bn=192", "cg=1 bn=64",
-                                  "bn=128 split=3", "cg=2 sms=8 tail=3", "mcb=1", "mcb=1 bn=256"])
+                                  "bn=128 split=3", "cg=2 sms=8 tail=3"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_chunked_descriptors_bitwise(ctx, force, spec, ta, tb):
     """An MN-major operand whose extent is a multiple of 64 is read with one
@@ -253,13 +251,7 @@ def test_chunked_descriptors_bitwise(ctx, force, spec, ta, tb):
     assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), ctx.last_kernel
     R, T = oracle.gemm(p)
     parity.check(oracle.decode(got), R, T, "f32", what=f"{spec} {ctx.last_kernel}")
-    if spec.startswith("mcb") and "bn=" in spec:
-        # the multicast tiles run the same MMAs as plain one-CTA tiles of the
-        # same width: the same bits
-        force(spec.replace("mcb=1", "cg=1"))
-        plain = run_problem(ctx, p)
-        assert "_mcb" not in ctx.last_kernel
-        assert torch.equal(got.view(torch.int32), plain.view(torch.int32)), ctx.last_kernel
+
 
 
 @pytest.mark.parametrize("spec", ["cg=1 bn=192", "cg=1 bn=192 split=3", "cg=1 bn=192 store=direct"])
