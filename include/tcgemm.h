@@ -125,7 +125,11 @@ tc_status_t tc_stream_create(tc_ctx *ctx, tc_stream **out);
  * library does not destroy the wrapped stream. */
 tc_status_t tc_stream_wrap(tc_ctx *ctx, void *cuda_stream, tc_stream **out);
 /* Wait for the stream's work; returns TC_ERR_DEVICE_TIMEOUT if a kernel
- * reported an expired wait, TC_ERR_CUDA on a CUDA error. */
+ * reported an expired wait, TC_ERR_CUDA on a CUDA error.  After
+ * TC_ERR_DEVICE_TIMEOUT the contents of every C the stream's work wrote
+ * since the previous sync are undefined (a kernel that stopped early may
+ * have written part of a tile, or a sum of incomplete partials); the
+ * stream and the context stay usable. */
 tc_status_t tc_stream_sync(tc_stream *s);
 /* The cudaStream_t behind the stream (for event timing by the caller). */
 void *tc_stream_handle(tc_stream *s);
