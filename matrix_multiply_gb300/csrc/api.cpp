@@ -48,7 +48,7 @@ struct tc_ctx {
     void *dbuf[3] = {nullptr, nullptr, nullptr};  // device copies for tc_gemm_host
     size_t dcap[3] = {0, 0, 0};
     cudaStream_t copy_in = nullptr, copy_out = nullptr;   // tc_gemm_host's copy streams
-    int max_pairs[2] = {-1, -1};                   // resident CTA pairs (BN 128, 256), queried once
+    int max_pairs[3] = {-1, -1, -1};               // resident CTA pairs (BN 128, 192, 256), queried once
     int csplit_clusters[2][17];                    // resident cluster splits (BN 64, 128; S), -1 = not queried
     std::mutex mu;
     tc_ctx()
@@ -257,10 +257,13 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Relative main-loop throughput per SM of each kernel shape (CTAs per tile,
 // tile width), measured on GB300 with bf16 at M = N = 4096 and long K:
 // narrower tiles read more shared memory per MMA flop, and a CTA pair
-// (tcgen05.mma.cta_group::2) loads half of B per SM.
+// (tcgen05.mma.cta_group::2) loads half of B per SM.  The 256 x 192 pair
+// measured the same per SM as the one-CTA 128 x 192 tile (fp16 8192 x 384
+// x 4096: 30.9 us both); on a tie the pair, listed first, is taken (it
+// reads B from L2 half as often).
 double tile_rate(int cg, int bn)
 {
-    if (cg == 2) return bn == 256 ? 1.15 : 0.72;
+    if (cg == 2) return bn == 256 ? 1.15 : bn == 192 ? 0.87 : 0.72;
     return bn == 256 ? 1.0 : bn == 192 ? 0.87 : bn == 128 ? 0.63 : 0.45;
 }
 
@@ -451,7 +454,7 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
         cg = 1;
     } else {
         // the kernel shape (CTAs per tile, tile width) with the least modelled time
-        static const int shapes[][2] = {{2, 256}, {1, 256}, {1, 192}, {2, 128}, {1, 128}, {1, 64}};
+        static const int shapes[][2] = {{2, 256}, {1, 256}, {2, 192}, {1, 192}, {2, 128}, {1, 128}, {1, 64}};
         double best = 1e300;
         for (const auto &sh : shapes) {
             const int c = sh[0], b = sh[1];
@@ -549,19 +552,22 @@ bool encode_map(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, in
 // each as a 64 x 64 swizzled tile 8 KB after the previous one -- the layout
 // that separate 64-wide boxes give.  Only for extents that are multiples of
 // 64: no chunk then reaches past a row's last element.
+// With width 32 the chunks are 32 elements (64 bytes) with the 64-byte
+// swizzle, 4 KB apart: the layout of a B share that is not a multiple of
+// 64 columns.
 bool encode_chunked(tc_ctx *ctx, CUtensorMap *m, tc_dtype_t dt, const void *base, int64_t extent, int64_t k,
-                    int64_t ld_elems, uint32_t chunks)
+                    int64_t ld_elems, uint32_t chunks, uint32_t width = 64)
 {
-    if (extent % 64 != 0) return false;
+    if (extent % width != 0) return false;
     const CUtensorMapDataType t = dt == TC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int64_t es = 2;
-    cuuint64_t dims[3] = {64, (cuuint64_t)k, (cuuint64_t)(extent / 64)};
-    cuuint64_t strides[2] = {(cuuint64_t)(ld_elems * es), (cuuint64_t)(64 * es)};
-    cuuint32_t box[3] = {64, 64, chunks};
+    cuuint64_t dims[3] = {width, (cuuint64_t)k, (cuuint64_t)(extent / width)};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld_elems * es), (cuuint64_t)(width * es)};
+    cuuint32_t box[3] = {width, 64, chunks};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = ctx->encode(m, t, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                             width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -729,7 +735,7 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
     L.grid = p.grid;
     if (p.cg == 2) {
         // no more pairs than can be resident at once (a persistent grid)
-        int &pairs = ctx->max_pairs[p.bn == 256 ? 1 : 0];
+        int &pairs = ctx->max_pairs[p.bn == 256 ? 2 : p.bn == 192 ? 1 : 0];
         if (pairs < 0) pairs = max_active_pairs(p.bn);
         if (pairs < 1) return TC_ERR_VARIANT;
         L.grid = std::min(L.grid, 2 * pairs);
@@ -804,6 +810,13 @@ tc_status_t enqueue(tc_ctx *ctx, const tc_gemm_desc *d, const Norm &n, const Pla
         if (a.b_kmajor) {
             ok = encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->K, d->N, ldb_use, a.b_3d, n.batch, sb, 64,
                             (uint32_t)(p.bn / p.cg));
+        } else if ((p.bn / p.cg) % 64 != 0) {
+            // a share of 32-column chunks (64-byte swizzle), as the kernel expects
+            a.b_chunked = chunk_ok && !a.b_3d &&
+                          encode_chunked(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use,
+                                         (uint32_t)(p.bn / p.cg / 32), 32);
+            ok = a.b_chunked || encode_map(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use, a.b_3d, n.batch,
+                                           sb, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
         } else {
             a.b_chunked = chunk_ok && !a.b_3d &&
                           encode_chunked(ctx, &L.tmB, d->a_dtype, Buse, d->N, d->K, ldb_use,
@@ -971,7 +984,7 @@ tc_status_t enqueue_grouped(tc_ctx *ctx, int n, const tc_gemm_desc *d, const voi
 
     int pairs = 0;
     if (cg == 2) {
-        int &mp = ctx->max_pairs[bn == 256 ? 1 : 0];
+        int &mp = ctx->max_pairs[bn == 256 ? 2 : bn == 192 ? 1 : 0];
         if (mp < 0) mp = max_active_pairs(bn);
         if (mp < 1) return TC_ERR_VARIANT;
         pairs = mp;

@@ -25,10 +25,11 @@ constexpr int EPI_STAGE_BYTES = 4096;           // one 32 x 32 output chunk (fp3
 __host__ __device__ constexpr int epi_warps(int bn, int cg, bool epi) { return (epi && !(bn == 192 && cg == 1)) ? 8 : 4; }
 __host__ __device__ constexpr int mma_threads(int bn, int cg, bool epi) { return (epi_warps(bn, cg, epi) + 2) * 32; }
 // Epilogue staging per warp: with four warps two chunk buffers (one TMA
-// store may still be reading the other), except for the one-CTA 192-wide
-// tile, whose 40 KB stages leave room for a fifth stage only with one
-// buffer (its K loop is bound by the latency the ring covers, its single
-// wave drains once); with eight warps one buffer each.  The plain-store
+// store may still be reading the other), except for the 192-wide tiles,
+// which keep one buffer so that one more pipeline stage fits (the one-CTA
+// tile's 40 KB stages: a fifth; the pair's 28 KB: a seventh; their K loops
+// are bound by the latency the ring covers and their shapes run a single
+// wave, which drains once); with eight warps one buffer each.  The plain-store
 // path's 32 x 32-float transpose buffer is one such buffer, so a warp's
 // staging never overlaps another warp's (a launch may use both paths: C by
 // plain stores, split-K partial tiles by TMA stores).  Buffers start at
@@ -36,7 +37,7 @@ __host__ __device__ constexpr int mma_threads(int bn, int cg, bool epi) { return
 // (the swizzle uses the absolute shared address).
 __host__ __device__ constexpr int epi_bufs(int bn, int cg, bool epi)
 {
-    return (epi_warps(bn, cg, epi) == 8 || (bn == 192 && cg == 1)) ? 1 : 2;
+    return (epi_warps(bn, cg, epi) == 8 || bn == 192) ? 1 : 2;
 }
 __host__ __device__ constexpr int epi_warp_bytes(int bn, int cg, bool epi)
 {

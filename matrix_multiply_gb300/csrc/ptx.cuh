@@ -186,14 +186,19 @@ __device__ __forceinline__ void tmem_st_wait()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle:
-// start address, leading- and stride-dimension byte offsets (all >> 4),
-// the fixed version field (1 at bit 46) and the layout type (2 = 128B
-// swizzle, bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+// Shared-memory matrix descriptor for tcgen05.mma: start address, leading-
+// and stride-dimension byte offsets (all >> 4), the fixed version field (1
+// at bit 46) and the layout type in bits 61-63 (2 = 128-byte swizzle,
+// 4 = 64-byte swizzle).
+constexpr uint64_t SMEM_SW128 = 2, SMEM_SW64 = 4;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t layout)
 {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return smem_desc(saddr, lbo, sbo, SMEM_SW128);
 }
 
 }  // namespace tc

@@ -586,7 +586,15 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     constexpr int CHUNKS = BN / 32;
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
     constexpr int CL = CG;                        // CTAs per cluster
-    static_assert(BNL % 64 == 0 && BN <= 256, "each CTA's B share must be whole 64-column boxes");
+    static_assert(BNL % 32 == 0 && BN <= 256, "each CTA's B share must be whole 32-column boxes");
+    // An MN-major B share that is not a multiple of 64 columns (the 96 of
+    // each CTA of a 256 x 192 pair) is held as 32-column chunks with the
+    // 64-byte swizzle (64 K rows x 64 bytes = 4 KB each), copied by boxes
+    // of 32 columns (or one 3-D copy of 32-element chunks); the host
+    // encodes B's descriptor to match.  A K-major share keeps the 128-byte
+    // swizzle: BNL rows of 128 bytes.
+    constexpr bool B_SW64 = (BNL % 64) != 0;
+    static_assert(!B_SW64 || (!GROUPED && !CSPLIT), "32-column B chunks: plain launches only");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 
     extern __shared__ uint8_t smem_raw[];
@@ -714,6 +722,16 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
                     }
                     if (b_kmajor) {
                         load(mapB, b_3d, sb, k0, n0);
+                    } else if (B_SW64) {
+                        if (b_chunked) {
+                            if (CG == 1)
+                                tma_load_3d(sb, mapB, fb, 0, k0, n0 / 32);
+                            else
+                                tma_load_3d_pair(sb, mapB, fb, 0, k0, n0 / 32);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BNL / 32; ++j) load(mapB, b_3d, sb + j * 4096, n0 + 32 * j, k0);
+                        }
                     } else if (b_chunked) {
                         load_chunks(mapB, sb, n0);
                     } else {
@@ -761,9 +779,12 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
                 // never carry out of the descriptor's 14-bit address field.
                 const uint32_t s0 = smem_u32(smem);
                 const uint64_t ad0 = a_kmajor ? smem_desc_sw128(s0, 16, 1024) : smem_desc_sw128(s0, 8192, 1024);
+                // (32-column B chunks: 4 KB apart, 8 K rows of 64 bytes = 512
+                // bytes per swizzle atom, a K step of 16 rows = 1024 bytes)
                 const uint64_t bd0 = b_kmajor ? smem_desc_sw128(s0 + A_BYTES, 16, 1024)
+                                     : B_SW64 ? smem_desc(s0 + A_BYTES, 4096, 512, SMEM_SW64)
                                               : smem_desc_sw128(s0 + A_BYTES, 8192, 1024);
-                const uint64_t astep = a_kmajor ? 2u : 128u, bstep = b_kmajor ? 2u : 128u;
+                const uint64_t astep = a_kmajor ? 2u : 128u, bstep = b_kmajor ? 2u : B_SW64 ? 64u : 128u;
                 // Segments of the unit, each accumulated in its own TMEM buffer
                 // from zero: the whole K range, or (I8ACC) K slices of
                 // args.slice_kb blocks that the epilogue adds up on chip.
@@ -1311,6 +1332,7 @@ cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
     if (L.cg == 2) {
         switch (L.bn) {
         case 128: return epi ? launch_kernel<128, 2, false, true>(L, st) : launch_kernel<128, 2>(L, st);
+        case 192: return epi ? launch_kernel<192, 2, false, true>(L, st) : launch_kernel<192, 2>(L, st);
         case 256: return epi ? launch_kernel<256, 2, false, true>(L, st) : launch_kernel<256, 2>(L, st);
         default: return cudaErrorInvalidValue;
         }
@@ -1379,6 +1401,7 @@ int max_active_pairs(int bn)
 {
     switch (bn) {
     case 128: return pairs_for<128>();
+    case 192: return pairs_for<192>();
     case 256: return pairs_for<256>();
     default: return 0;
     }

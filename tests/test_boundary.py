@@ -197,7 +197,10 @@ def test_plan_tail_split():
 
 
 def test_plan_narrow_n():
-    assert plan(8192, 384, 4096, "f16", "f16") == "tcgen05_nn_f16_f16_128x192"
+    # a CTA pair on 256 x 192 tiles: each CTA loads 96 columns of B, so the
+    # 64 tile rows read B from L2 half as often as one-CTA 128 x 192 tiles
+    assert plan(8192, 384, 4096, "f16", "f16") == "tcgen05_nn_f16_f16_256x192_pair"
+    assert plan_forced("cg=1", 8192, 384, 4096, "f16", "f16") == "tcgen05_nn_f16_f16_128x192"
 
 
 def test_plan_repacks_unaligned_operands():

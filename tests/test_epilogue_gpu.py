@@ -82,10 +82,10 @@ def test_epilogue_parity(ctx, activation, ab, c, ta, tb, shape):
     assert ctx.last_kernel.endswith(want), ctx.last_kernel
 
 
-@pytest.mark.parametrize("spec", ["", "cg=2", "cg=1 bn=64", "bn=192", "bn=128 split=3", "bn=128 split=3 csplit=0",
+@pytest.mark.parametrize("spec", ["", "cg=2", "cg=1 bn=64", "cg=1 bn=192", "bn=128 split=3", "bn=128 split=3 csplit=0",
                                   "bn=64 split=16", "bn=256 split=5",
                                   "sms=5 tail=2", "cg=2 sms=6 tail=2", "store=direct", "pack=1",
-                                  "pack=1 split=4", "cg=2 bn=128"])
+                                  "pack=1 split=4", "cg=2 bn=128", "cg=2 bn=192", "cg=2 bn=192 sms=4 tail=2"])
 @pytest.mark.parametrize("c", ["bf16", "f32"])
 def test_epilogue_every_variant(ctx, force, spec, c):
     """The epilogue in the tensor-core kernel's own store paths (TMA, plain,

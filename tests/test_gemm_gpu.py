@@ -143,13 +143,15 @@ def test_alpha_beta(ctx, alpha, beta, c):
     check_full(ctx, p, f"alpha={alpha} beta={beta}")
 
 
-@pytest.mark.parametrize("spec", ["bn=64", "bn=128", "bn=192", "bn=256", "bn=128 split=3",
+@pytest.mark.parametrize("spec", ["bn=64", "bn=128", "cg=1 bn=192", "bn=256", "bn=128 split=3",
                                   "bn=128 split=3 csplit=0", "bn=64 split=16 csplit=0",
                                   "bn=256 split=7", "bn=64 split=16", "pack=1", "pack=1 split=5",
                                   "grid=3", "group_m=1", "group_m=3 bn=64", "sms=5 tail=2",
                                   "sms=5 tail=3 bn=64", "sms=7 bn=256 tail=2 pack=1", "cg=2",
                                   "cg=2 bn=128", "cg=2 sms=6 tail=2", "cg=2 grid=1 pack=1",
-                                  "store=direct", "store=direct cg=2 sms=6 tail=2", "store=direct split=3"])
+                                  "store=direct", "store=direct cg=2 sms=6 tail=2", "store=direct split=3",
+                                  "cg=2 bn=192", "cg=2 bn=192 sms=6 tail=2", "cg=2 bn=192 chunk=0",
+                                  "cg=2 bn=192 store=direct", "cg=2 bn=192 pack=1"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_forced_variants(ctx, force, spec, ta, tb):
     force(spec)
@@ -218,9 +220,10 @@ def test_padded_leading_dimensions(ctx):
 
 # ----------------------------------------------------- exactness and edges
 
-@pytest.mark.parametrize("spec", ["", "bn=64", "bn=192", "bn=128 split=4", "bn=128 split=4 csplit=0",
+@pytest.mark.parametrize("spec", ["", "bn=64", "cg=1 bn=192", "bn=128 split=4", "bn=128 split=4 csplit=0",
                                   "bn=64 split=16", "pack=1 bn=256 split=2",
-                                  "sms=5 tail=3", "cg=2", "cg=2 bn=128 sms=4 tail=2", "store=direct"])
+                                  "sms=5 tail=3", "cg=2", "cg=2 bn=128 sms=4 tail=2", "store=direct",
+                                  "cg=2 bn=192", "cg=2 bn=192 sms=4 tail=2", "cg=2 bn=192 chunk=0"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
     """Integer entries in [-4,4], K=2048: every partial sum is an integer
@@ -234,7 +237,7 @@ def test_integer_inputs_bitwise(ctx, force, spec, ta, tb):
 
 
 @pytest.mark.parametrize("spec", ["", "cg=2 bn=256", "cg=2 bn=128", "cg=1 bn=256", "cg=1 bn=192", "cg=1 bn=64",
-                                  "bn=128 split=3", "cg=2 sms=8 tail=3"])
+                                  "bn=128 split=3", "cg=2 sms=8 tail=3", "cg=2 bn=192", "cg=2 bn=192 sms=4 tail=2"])
 @pytest.mark.parametrize("ta,tb", LAYOUTS)
 def test_chunked_descriptors_bitwise(ctx, force, spec, ta, tb):
     """An MN-major operand whose extent is a multiple of 64 is read with one
@@ -254,21 +257,38 @@ def test_chunked_descriptors_bitwise(ctx, force, spec, ta, tb):
 
 
 
-@pytest.mark.parametrize("spec", ["cg=1 bn=192", "cg=1 bn=192 split=3", "cg=1 bn=192 store=direct"])
+@pytest.mark.parametrize("spec", ["cg=1 bn=192", "cg=1 bn=192 split=3", "cg=1 bn=192 store=direct",
+                                  "cg=2 bn=192", "cg=2 bn=192 sms=4 tail=2", "cg=2 bn=192 store=direct"])
 @pytest.mark.parametrize("c", ["f16", "f32"])
 def test_single_buffer_epilogue_192(ctx, force, spec, c):
-    """The 128x192 kernel stages its epilogue in one buffer per warp (for a
-    fifth pipeline stage): TMA-stored C, C through the transpose buffer (an
-    odd ldc, beta != 0 so C_old is read back through it too), plain stores,
-    and split-K partials all go through that one buffer."""
+    """The 192-wide kernels stage their epilogue in one buffer per warp (for
+    one more pipeline stage): TMA-stored C, C through the transpose buffer
+    (an odd ldc, beta != 0 so C_old is read back through it too), plain
+    stores, and split-K partials all go through that one buffer."""
     force(spec)
     for ldc in (0, 389):
         p = synthetic.make_problem(700, 384, 1500, "f16", c, transpose_b=True, alpha=0.75, beta=-0.5, seed=93,
                                    dist="normal", c_fill="uniform", ldc=ldc)
         out = run_problem(ctx, p, ldc=ldc)
-        assert "128x192" in ctx.last_kernel, ctx.last_kernel
+        assert ("256x192_pair" if "cg=2" in spec else "128x192") in ctx.last_kernel, ctx.last_kernel
         R, T = oracle.gemm(p)
         parity.check(oracle.decode(out)[:, :384], R, T, c, what=f"{spec} ldc={ldc} {ctx.last_kernel}")
+
+
+@pytest.mark.parametrize("bn", [128, 192, 256])
+def test_pair_width_first_call_in_fresh_context(force, bn):
+    """Each CTA-pair tile width queries its own residency (pairs that fit
+    at once) on its first use in a context."""
+    c = tg.Context(0)
+    try:
+        force(f"cg=2 bn={bn}")
+        p = synthetic.make_problem(520, 400, 300, "f16", "f32", seed=95, dist="normal")
+        out = run_problem(c, p)
+        assert f"256x{bn}_pair" in c.last_kernel, c.last_kernel
+        R, T = oracle.gemm(p)
+        parity.check(oracle.decode(out), R, T, "f32", what=c.last_kernel)
+    finally:
+        c.close()
 
 
 @pytest.mark.parametrize("M", [1, 4, 7, 9, 100, 127])
@@ -372,7 +392,7 @@ def test_refused_call_launches_nothing(ctx):
 
 # ----------------------------------------------------- batched / grouped / streams
 
-@pytest.mark.parametrize("spec", ["", "pack=1", "bn=128 split=3"])
+@pytest.mark.parametrize("spec", ["", "pack=1", "bn=128 split=3", "cg=2 bn=192"])
 def test_batched(ctx, force, spec):
     force(spec)
     M, N, K, batch = 200, 136, 264, 3
@@ -582,7 +602,7 @@ def test_bf16_tn_splitk_256x16384(ctx, force):
 
 def test_fp16_nn_narrow_8192x384(ctx):
     check_sampled(ctx, synthetic.fp16_nn_narrow_8192x384x4096(), what="fp16 NN 8192x384x4096")
-    assert ctx.last_kernel.endswith("128x192")
+    assert ctx.last_kernel.endswith("256x192_pair")
 
 
 @pytest.mark.parametrize("n", synthetic.SQUARE_SIZES)
