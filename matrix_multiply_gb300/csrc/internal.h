@@ -18,10 +18,13 @@ constexpr int SMEM_LIMIT = 232448;              // max dynamic shared memory per
 constexpr int EPI_STAGE_BYTES = 4096;           // one 32 x 32 output chunk (fp32 worst case)
 
 // Epilogue warps: four (warp w reads TMEM lanes 32w..32w+31), or, for the
-// fused bias/activation epilogue, eight -- two per TMEM lane quarter, each
-// taking every other 32-column chunk -- so that the CUDA-core epilogue work
-// of a tile that no next tile hides takes half as long.  The one-CTA
-// 192-wide tile keeps four (its fifth pipeline stage needs the space).
+// fused bias/activation epilogue and for grouped launches (`epi` true),
+// eight -- two per TMEM lane quarter, each taking every other 32-column
+// chunk -- so that CUDA-core epilogue work takes half as long: the tail
+// tile's, which no next tile hides, and the plain-store epilogue of ragged
+// problems, which otherwise holds the accumulator longer than the next
+// tile's K loop runs.  The one-CTA 192-wide tile keeps four (its fifth
+// pipeline stage needs the space).
 __host__ __device__ constexpr int epi_warps(int bn, int cg, bool epi) { return (epi && !(bn == 192 && cg == 1)) ? 8 : 4; }
 __host__ __device__ constexpr int mma_threads(int bn, int cg, bool epi) { return (epi_warps(bn, cg, epi) + 2) * 32; }
 // Epilogue staging per warp: with four warps two chunk buffers (one TMA

@@ -565,7 +565,7 @@ __device__ __forceinline__ void csplit_reduce(const MmaArgs &a, const uint8_t *p
 // adds them across the cluster, so no partial tile goes through global
 // memory and no second kernel runs.
 template <int BN, int CG, bool GROUPED, bool EPI, bool I8ACC = false, bool CSPLIT = false>
-__global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
+__global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
     mma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                const MmaArgs args, const __grid_constant__ TableOf<GROUPED> gt)
@@ -573,8 +573,12 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     constexpr int BNL = BN / CG;                   // B columns loaded by this CTA
     constexpr int STAGE = stage_bytes(BN, CG);
     constexpr int A_BYTES = BM * BK * 2;
-    constexpr int S = mma_stages(BN, CG, EPI);
-    constexpr int EW = epi_warps(BN, CG, EPI);     // epilogue warps 0..EW-1, then the TMA and MMA warps
+    // eight epilogue warps where the epilogue has CUDA-core work to hide:
+    // the fused bias/activation, and grouped launches (whose ragged problems
+    // often store C by plain stores, row-coalesced through shared memory)
+    constexpr bool WIDE = EPI || GROUPED;
+    constexpr int S = mma_stages(BN, CG, WIDE);
+    constexpr int EW = epi_warps(BN, CG, WIDE);    // epilogue warps 0..EW-1, then the TMA and MMA warps
     constexpr int TMA_WARP = EW, MMA_WARP = EW + 1;
     constexpr int CSTEP = EW / 4;                  // chunks between two chunks of one epilogue warp
     constexpr int TCOLS = I8ACC ? 512 : tmem_cols(BN);
@@ -601,7 +605,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *cstage = smem + S * STAGE;            // epilogue staging
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + epi_smem(BN, CG, EPI));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cstage + epi_smem(BN, CG, WIDE));
     uint64_t *full_bar = bars;
     uint64_t *empty_bar = bars + S;
     uint64_t *tfull_bar = bars + 2 * S;
@@ -850,10 +854,10 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI), 1)
         uint32_t local = 0, ebuf = 0;
         const int quarter = warp & 3, chunk0 = warp >> 2;
         const int row_in_tile = (int)rank * BM + quarter * 32 + lane;
-        constexpr int EBUFS = epi_bufs(BN, CG, EPI);
+        constexpr int EBUFS = epi_bufs(BN, CG, WIDE);
         constexpr int LAST_C0 = CHUNKS - CSTEP;        // this warp's last chunk: LAST_C0 + chunk0
         static_assert(CHUNKS % CSTEP == 0, "chunks split evenly between the warps of a lane quarter");
-        uint8_t *my_stage = cstage + warp * epi_warp_bytes(BN, CG, EPI);
+        uint8_t *my_stage = cstage + warp * epi_warp_bytes(BN, CG, WIDE);
         // The warp's staging is either its TMA chunk buffers (two that
         // alternate over the stores actually issued, a buffer refilled only
         // after one newer store was committed; or one, refilled after its
@@ -1067,8 +1071,8 @@ template <int BN, int CG, bool GROUPED = false, bool EPI = false, bool I8ACC = f
 cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GROUPED> &gt = TableOf<GROUPED>{})
 {
     constexpr auto kern = mma_kernel<BN, CG, GROUPED, EPI, I8ACC, CSPLIT>;
-    constexpr int smem = mma_smem_bytes(BN, CG, EPI);
-    constexpr int threads = mma_threads(BN, CG, EPI);
+    constexpr int smem = mma_smem_bytes(BN, CG, EPI || GROUPED);
+    constexpr int threads = mma_threads(BN, CG, EPI || GROUPED);
     // per device: the kernel's shared-memory limit is raised once (callers
     // of the context-free entry point may race here from several threads;
     // setting the attribute twice is harmless)
