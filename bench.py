@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 M = N = K = 4096
 HEADLINE = "bf16_nn_4096"
 SETTLE_MS = 30.0           # default of --settle-ms (see run_ours)
+HOST_AHEAD_CYCLES = 400000  # device spin (~0.2 ms) before the timed region's first event
 WORKLOAD = "bf16 NN GEMM M=N=K=4096, bf16 out, fp32 accumulate, alpha=1 beta=0, normal(0,1) from seed 1"
 METRIC = "GEMM TFLOP/s (2MNK/t) bf16 4096^3 NN"
 PAGES_BASELINE = 29.0     # TFLOP/s, bf16 4096^3 NN, Apple M5 Pro (tessl architecture.md, column-panel swizzle)
@@ -444,6 +445,7 @@ def time_steps(torch, runner, tstream, cold, steps, warmup):
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda._sleep(HOST_AHEAD_CYCLES)      # the host queues ahead of the first event (see run_ours)
     for i in range(steps):
         cold.before_step()
         starts[i].record(tstream)
@@ -504,6 +506,11 @@ def run_ours(args):
     launches0 = ctx.launch_count
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
+        # Untimed: a short device-side spin ahead of the first start event,
+        # so that the host has queued the first steps by the time the GPU
+        # reaches it.  Without it the first step, launched onto an idle GPU,
+        # also times the host's launch latency (~20 us).
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
         for i in range(args.steps):
             cold.before_step()
             starts[i].record(tstream)
