@@ -290,12 +290,13 @@ __global__ void __launch_bounds__(256, 2) ffma128_kernel(const FfmaArgs a)
 
 // Small NN problems with 16-byte aligned rows (the pages' fp32 256^3 shape):
 // 16 x 32 tiles, 128 threads, one row and four columns per thread.  A and B
-// arrive in K chunks of 64 through a double-buffered cp.async pipeline (bytes
-// past M, N or K read as zeros), so the first multiply-adds start after one
-// chunk rather than after the whole K panel; every shared read is 16 bytes
-// (four k of the thread's A row, four columns of a B row).  Per output one
-// fmaf chain in ascending k.
-constexpr int SBM = 16, SBN = 32, SKC = 64, SLDA = SKC + 4;
+// arrive in K chunks of 64 through a cp.async ring of SNBUF buffers (bytes
+// past M, N or K read as zeros): SNBUF - 1 chunks are in flight before the
+// first multiply-add, so a short K pays the load latency about once, and the
+// first multiply-adds start after one chunk rather than after the whole K
+// panel; every shared read is 16 bytes (four k of the thread's A row, four
+// columns of a B row).  Per output one fmaf chain in ascending k.
+constexpr int SBM = 16, SBN = 32, SKC = 64, SLDA = SKC + 4, SNBUF = 3;
 
 __device__ __forceinline__ void cp_async16_f(uint32_t dst, const void *src, uint32_t src_bytes)
 {
@@ -304,8 +305,8 @@ __device__ __forceinline__ void cp_async16_f(uint32_t dst, const void *src, uint
 
 __global__ void __launch_bounds__(128) ffma_small_nn_kernel(const FfmaArgs a)
 {
-    __shared__ __align__(16) float As[2][SBM][SLDA];
-    __shared__ __align__(16) float Bs[2][SKC][SBN];
+    __shared__ __align__(16) float As[SNBUF][SBM][SLDA];
+    __shared__ __align__(16) float Bs[SNBUF][SKC][SBN];
     const int tid = threadIdx.x;
     const int tx = tid & 7, ty = tid >> 3;
     const long long n0 = (long long)blockIdx.x * SBN;
@@ -317,11 +318,11 @@ __global__ void __launch_bounds__(128) ffma_small_nn_kernel(const FfmaArgs a)
         const float *A = a.A + (long long)b * a.stride_a;
         const float *B = a.B + (long long)b * a.stride_b;
         float *C = a.C + (long long)b * a.stride_c;
-        // chunk c into buffer c & 1: A 16 x 64 (2 pieces of 16 bytes a
+        // chunk c into buffer c % SNBUF: A 16 x 64 (2 pieces of 16 bytes a
         // thread), B 64 x 32 (4 pieces a thread)
         auto issue = [&](long long c) {
             const long long k0 = c * SKC;
-            const int buf = (int)(c & 1);
+            const int buf = (int)(c % SNBUF);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int e = tid + 128 * i;
@@ -344,14 +345,19 @@ __global__ void __launch_bounds__(128) ffma_small_nn_kernel(const FfmaArgs a)
             }
         };
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        issue(0);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (nchunk > 1) issue(1);
-        asm volatile("cp.async.commit_group;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < SNBUF - 1; ++i) {
+            if (i < nchunk) issue(i);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
         for (long long c = 0; c < nchunk; ++c) {
-            asm volatile("cp.async.wait_group 1;" ::: "memory");      // chunk c has landed
+            // chunk c + SNBUF - 1 into the buffer chunk c - 1 used (free since
+            // the previous iteration's closing barrier), then wait for chunk c
+            if (c + SNBUF - 1 < nchunk) issue(c + SNBUF - 1);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            asm volatile("cp.async.wait_group %0;" ::"n"(SNBUF - 1) : "memory");   // chunk c has landed
             __syncthreads();
-            const int buf = (int)(c & 1);
+            const int buf = (int)(c % SNBUF);
 #pragma unroll
             for (int kk = 0; kk < SKC; kk += 4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(&As[buf][ty][kk]);
@@ -366,8 +372,6 @@ __global__ void __launch_bounds__(128) ffma_small_nn_kernel(const FfmaArgs a)
                 }
             }
             __syncthreads();                                           // buffer free again
-            if (c + 2 < nchunk) issue(c + 2);
-            asm volatile("cp.async.commit_group;" ::: "memory");
         }
         const long long gm = m0 + ty, gn = n0 + tx * 4;
         if (gm < a.M) {
