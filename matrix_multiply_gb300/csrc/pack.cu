@@ -115,48 +115,101 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const __grid_constan
 }
 
 // Relaxed fp32 (split into bf16 parts): x = hi + lo + e with hi = bf16(x),
-// lo = bf16(x - hi) (x - hi is exact in fp32), |e| <= 2^-16 |x|.  One thread
-// per element; consecutive threads take consecutive columns, so the fp32
-// loads and the three bf16 stores are contiguous across a warp.
+// lo = bf16(x - hi) (x - hi is exact in fp32), |e| <= 2^-16 |x|.  Each thread
+// takes four consecutive columns of a row: one 16-byte load and three 8-byte
+// stores when the row's addresses allow, element by element otherwise.
+// Consecutive threads take consecutive groups, so loads and stores are
+// contiguous across a warp.  Index = 32-bit unsigned when the group count
+// allows (the division per group dominates the index arithmetic).
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <typename Index>
 __global__ void __launch_bounds__(256) split_kernel(const SplitArgs a)
 {
-    const long long total = a.rows * a.cols;
-    for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
-        const long long r = i / a.cols, c = i - r * a.cols;
-        const float x = __ldg(a.src + r * a.ld_src + c);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-        const uint16_t part[2] = {__bfloat16_as_ushort(hi), __bfloat16_as_ushort(lo)};
+    const Index gpr = (Index)((a.cols + 3) / 4), total = (Index)a.rows * gpr;
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.src) & 15u) == 0) && (a.ld_src % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(a.dst) & 7u) == 0) && (a.ld_dst % 4 == 0) &&
+                     (!a.k_along_cols || a.cols % 4 == 0);
+    for (Index i = (Index)blockIdx.x * 256 + threadIdx.x; i < total; i += (Index)gridDim.x * 256) {
+        const Index r = i / gpr;
+        const long long c = (long long)(i - r * gpr) * 4;
+        const float *src = a.src + (long long)r * a.ld_src + c;
+        const int n = (int)min(4LL, a.cols - c);
+        float x[4];
+        if (vec && n == 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+            x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = j < n ? __ldg(src + j) : 0.0f;
+        }
+        float hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            hi[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
+            lo[j] = x[j] - hi[j];
+        }
+        const uint2 part[2] = {make_uint2(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3])),
+                               make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]))};
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
-            const long long off = a.k_along_cols ? r * a.ld_dst + j * a.cols + c : (j * a.rows + r) * a.ld_dst + c;
-            a.dst[off] = part[a.parts[j]];
+            const long long off = a.k_along_cols ? (long long)r * a.ld_dst + j * a.cols + c
+                                                 : (j * a.rows + (long long)r) * a.ld_dst + c;
+            const uint2 v = part[a.parts[j]];
+            if (vec && n == 4) {
+                *reinterpret_cast<uint2 *>(a.dst + off) = v;
+            } else {
+                const uint16_t e[4] = {(uint16_t)(v.x & 0xffffu), (uint16_t)(v.x >> 16), (uint16_t)(v.y & 0xffffu),
+                                       (uint16_t)(v.y >> 16)};
+                for (int q = 0; q < n; ++q) a.dst[off + q] = e[q];
+            }
         }
     }
 }
 
-// int8 -> bf16 (every int8 value is exact in bf16), four consecutive
-// columns per thread: four byte loads, one 8-byte store when the row has
-// all four.
+// int8 -> bf16 or f16 (every int8 value is exact in both).  Each thread takes
+// 16 consecutive columns of a row: one 16-byte load and two 16-byte stores
+// when the row's addresses allow (the destination rows are 64-element
+// padded and 256-byte aligned), element by element otherwise.
+template <typename Index>
 __global__ void __launch_bounds__(256) widen_kernel(const WidenArgs a)
 {
-    const long long groups = (a.cols + 3) / 4, total = a.rows * groups;
-    for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
-        const long long r = i / groups, c = (i - r * groups) * 4;
-        const int8_t *src = a.src + r * a.ld_src + c;
-        uint16_t *dst = a.dst + r * a.ld_dst + c;
-        const int n = (int)min(4LL, a.cols - c);
-        uint16_t h[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float x = j < n ? (float)__ldg(src + j) : 0.0f;
-            h[j] = a.to_f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
-        }
-        if (n == 4) {
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16);
+    const Index gpr = (Index)((a.cols + 15) / 16), total = (Index)a.rows * gpr;
+    const bool vec_src = ((reinterpret_cast<uintptr_t>(a.src) & 15u) == 0) && (a.ld_src % 16 == 0);
+    for (Index i = (Index)blockIdx.x * 256 + threadIdx.x; i < total; i += (Index)gridDim.x * 256) {
+        const Index r = i / gpr;
+        const long long c = (long long)(i - r * gpr) * 16;
+        const int8_t *src = a.src + (long long)r * a.ld_src + c;
+        uint16_t *dst = a.dst + (long long)r * a.ld_dst + c;
+        const int n = (int)min(16LL, a.cols - c);
+        int8_t b[16];
+        if (vec_src && n == 16) {
+            const int4 v = __ldg(reinterpret_cast<const int4 *>(src));
+            *reinterpret_cast<int4 *>(b) = v;
         } else {
-            for (int j = 0; j < n; ++j) dst[j] = h[j];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) b[j] = j < n ? __ldg(src + j) : (int8_t)0;
         }
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float x0 = (float)b[2 * j], x1 = (float)b[2 * j + 1];
+            if (a.to_f16) {
+                const __half2 h = __floats2half2_rn(x0, x1);
+                w[j] = *reinterpret_cast<const uint32_t *>(&h);
+            } else {
+                w[j] = pack_bf16x2(x0, x1);
+            }
+        }
+        // the destination row is padded to a multiple of 64 elements: a
+        // 16-column group never straddles its end, so whole stores are safe
+        // (columns past `cols` land in the padding, which nothing reads)
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
     }
 }
 
@@ -166,18 +219,24 @@ cudaError_t launch_widen(const WidenArgs &a, cudaStream_t st)
 {
     if (a.rows < 1 || a.cols < 1 || (a.ld_dst % 64) || (reinterpret_cast<uintptr_t>(a.dst) & 255u))
         return cudaErrorInvalidValue;
-    const long long total = a.rows * ((a.cols + 3) / 4);
+    const long long total = a.rows * ((a.cols + 15) / 16);
     const long long grid = std::min<long long>((total + 255) / 256, 152LL * 16);
-    widen_kernel<<<(unsigned)grid, 256, 0, st>>>(a);
+    if (total + (long long)grid * 256 < (1LL << 31))
+        widen_kernel<uint32_t><<<(unsigned)grid, 256, 0, st>>>(a);
+    else
+        widen_kernel<unsigned long long><<<(unsigned)grid, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t st)
 {
     if (a.rows < 1 || a.cols < 1) return cudaErrorInvalidValue;
-    const long long total = a.rows * a.cols;
+    const long long total = a.rows * ((a.cols + 3) / 4);
     const long long grid = std::min<long long>((total + 255) / 256, 152LL * 16);
-    split_kernel<<<(unsigned)grid, 256, 0, st>>>(a);
+    if (total + (long long)grid * 256 < (1LL << 31))
+        split_kernel<uint32_t><<<(unsigned)grid, 256, 0, st>>>(a);
+    else
+        split_kernel<unsigned long long><<<(unsigned)grid, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
