@@ -195,7 +195,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // the reduction kernel instead of a cluster reduction on chip) gemv=0 (a
 // product with at most 16 rows on one side stays on the tensor-core kernel)
 // gemv_ks=<1|2|4|8> (the skinny-product kernel's cluster form with this K
-// split) gemv_rr=0 (its cluster form instead of the row-range form).
+// split) gemv_rr=0 (its cluster form instead of the row-range form)
+// hband=<rows> (tc_gemm_host moves A and C in bands of this many rows).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
 // debug_timeout_ms=<ms> (the bound on every device wait).
@@ -206,6 +207,7 @@ struct Force {
     int debug_drop = 0, debug_timeout_ms = 0;
     int no_chunk = 0;
     int no_short_a = 0;
+    int host_band = 0;
     int i8acc = -1;
     int csplit = -1;
     int gemv = -1, gemv_ks = 0, gemv_rr = -1;
@@ -243,6 +245,7 @@ Force read_force()
         else if (k == "debug_timeout_ms") f.debug_timeout_ms = std::atoi(v.c_str());
         else if (k == "chunk") f.no_chunk = std::atoi(v.c_str()) == 0;
         else if (k == "shorta") f.no_short_a = std::atoi(v.c_str()) == 0;
+        else if (k == "hband") f.host_band = std::atoi(v.c_str());
         else if (k == "i8acc") f.i8acc = std::atoi(v.c_str());
         else if (k == "csplit") f.csplit = std::atoi(v.c_str());
         else if (k == "gemv") f.gemv = std::atoi(v.c_str());
@@ -1643,7 +1646,9 @@ tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
     // (Host-device copies run at one rate per direction whatever the number
     // of streams; the two directions overlap.)
     const int64_t es_a = (int64_t)elem_size(d->a_dtype), es_c = (int64_t)elem_size(d->c_dtype);
-    const int64_t band = d->M <= 1536 ? d->M : std::max<int64_t>(1024, (int64_t)round_up((size_t)cdiv(d->M, 4), 256));
+    const int64_t hb = read_force().host_band;
+    const int64_t band = hb > 0 ? std::min<int64_t>(hb, d->M)
+                         : d->M <= 1536 ? d->M : std::max<int64_t>(1024, (int64_t)round_up((size_t)cdiv(d->M, 4), 256));
     const int nb = (int)cdiv(d->M, band);
     uint8_t *dA = static_cast<uint8_t *>(ctx->dbuf[0]), *dB = static_cast<uint8_t *>(ctx->dbuf[1]);
     uint8_t *dC = static_cast<uint8_t *>(ctx->dbuf[2]);
