@@ -438,21 +438,39 @@ class Runner:
             self.group.enqueue(self.ctx, self.stream)
 
 
-def time_steps(torch, runner, tstream, cold, steps, warmup):
+def timed_loop(torch, runner, tstream, cold, steps, per_step):
+    """Device time (ms) of `steps` steps issued back to back on the launching
+    stream, as a list with one entry per step.  per_step: an event pair
+    around every step (each step then also pays the gap between kernels
+    that an event in the stream imposes); else one pair around all of them
+    (the throughput of back-to-back steps), each entry the mean."""
+    torch.cuda._sleep(HOST_AHEAD_CYCLES)      # the host queues ahead of the first event (see run_ours)
+    if per_step:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            cold.before_step()
+            starts[i].record(tstream)
+            runner.step()
+            ends[i].record(tstream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(tstream)
+    for i in range(steps):
+        cold.before_step()
+        runner.step()
+    end.record(tstream)
+    torch.cuda.synchronize()
+    return [start.elapsed_time(end) / steps] * steps
+
+
+def time_steps(torch, runner, tstream, cold, steps, warmup, per_step=False):
     for _ in range(warmup):
         cold.before_step()
         runner.step()
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    torch.cuda._sleep(HOST_AHEAD_CYCLES)      # the host queues ahead of the first event (see run_ours)
-    for i in range(steps):
-        cold.before_step()
-        starts[i].record(tstream)
-        runner.step()
-        ends[i].record(tstream)
-    torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return timed_loop(torch, runner, tstream, cold, steps, per_step)
 
 
 def run_ours(args):
@@ -501,29 +519,20 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     launches0 = ctx.launch_count
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
-        # Untimed: a short device-side spin ahead of the first start event,
-        # so that the host has queued the first steps by the time the GPU
-        # reaches it.  Without it the first step, launched onto an idle GPU,
-        # also times the host's launch latency (~20 us).
-        torch.cuda._sleep(HOST_AHEAD_CYCLES)
-        for i in range(args.steps):
-            cold.before_step()
-            starts[i].record(tstream)
-            runner.step()
-            ends[i].record(tstream)
-        torch.cuda.synchronize()
+        # (timed_loop first queues a short device-side spin ahead of the
+        # first event, so that the host has queued the first steps by the
+        # time the GPU reaches it: without it the first step, launched onto
+        # an idle GPU, also times the host's launch latency, ~20 us)
+        ms = timed_loop(torch, runner, tstream, cold, args.steps, args.timing == "step")
         t_wall = time.perf_counter() - t_wall
     barrier()
     torch.cuda.synchronize()
     stream.sync()
     launches = ctx.launch_count - launches0
     kernel = ctx.last_kernel
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(sum(ms), world)
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, flops, args.steps, total_ms)
@@ -563,7 +572,7 @@ def run_ours(args):
     if args.summary and name == HEADLINE and world == 1:
         del runner
         torch.cuda.empty_cache()
-        work = summary(torch, tg, ctx, stream, tstream, cold, reg, sms)
+        work = summary(torch, tg, ctx, stream, tstream, cold, reg, sms, args.timing == "step")
 
     rl = roofline(probs, statistics.mean(ms) / 1e3, sms)
     rl["traffic"] = profile_traffic(name, kernel_source_hash())
@@ -578,7 +587,9 @@ def run_ours(args):
         "config": {"workload": WORKLOAD if name == HEADLINE else name, "problems": len(probs),
                    "M": p0.M, "N": p0.N, "K": p0.K, "layout": p0.layout, "global_batch": len(probs),
                    "parallelism": f"replicas{world}" if world > 1 else "single", "variant": kernel,
-                   "l2": cold.describe(), "copies": n_copies, "settle_ms": args.settle_ms},
+                   "l2": cold.describe(), "copies": n_copies, "settle_ms": args.settle_ms,
+                   "timing": ("one CUDA event pair around each step" if args.timing == "step" else
+                              "one CUDA event pair around the back-to-back timed steps")},
         "roofline": rl,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -606,7 +617,7 @@ def run_ours(args):
     return 0
 
 
-def summary(torch, tg, ctx, stream, tstream, cold, reg, sms):
+def summary(torch, tg, ctx, stream, tstream, cold, reg, sms, per_step=False):
     """Every other named workload: TFLOP/s and roofline fraction, each timed
     for about a third of a second of device time (cold L2 per step)."""
     out = {}
@@ -617,7 +628,7 @@ def summary(torch, tg, ctx, stream, tstream, cold, reg, sms):
         runner = Runner(tg, ctx, stream, probs, cold.copies(probs))
         probe = time_steps(torch, runner, tstream, cold, 3, 2)
         steps = int(max(10, min(2000, 0.3e3 / max(statistics.mean(probe), 1e-3))))
-        ms = time_steps(torch, runner, tstream, cold, steps, 3)
+        ms = time_steps(torch, runner, tstream, cold, steps, 3, per_step)
         t = statistics.mean(ms) / 1e3
         flops = sum(2.0 * p.M * p.N * p.K for p in probs)
         rl = roofline(probs, t, sms)
@@ -643,6 +654,8 @@ def main():
     ap.add_argument("--settle-ms", type=float, default=SETTLE_MS,
                     help="untimed repetitions of the step (wall ms) before the warm-up steps; 0 for "
                          "profiler runs that list every launch")
+    ap.add_argument("--timing", choices=["stream", "step"], default="stream",
+                    help="one event pair around the back-to-back timed steps (stream), or one per step")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="how every timed step starts from a cold L2 (see Cold)")
     args = ap.parse_args()
