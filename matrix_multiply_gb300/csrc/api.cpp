@@ -196,6 +196,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // product with at most 16 rows on one side stays on the tensor-core kernel)
 // gemv_ks=<1|2|4|8> (the skinny-product kernel's cluster form with this K
 // split) gemv_rr=0 (its cluster form instead of the row-range form)
+// gemv_blocks=0|1 (the row-range form on 2 CTAs per SM, sharing rows or
+// whole 16-row blocks) gemv_grid=<G> (the row-range form on G CTAs)
 // hband=<rows> (tc_gemm_host moves A and C in bands of this many rows).
 // Test hooks: debug_drop=1 (the MMA warp withholds the first tile's
 // "accumulator ready" signal, so the epilogue's wait expires) and
@@ -210,7 +212,7 @@ struct Force {
     int host_band = 0;
     int i8acc = -1;
     int csplit = -1;
-    int gemv = -1, gemv_ks = 0, gemv_rr = -1;
+    int gemv = -1, gemv_ks = 0, gemv_rr = -1, gemv_blocks = -1, gemv_grid = 0;
 };
 
 Force read_force()
@@ -251,6 +253,8 @@ Force read_force()
         else if (k == "gemv") f.gemv = std::atoi(v.c_str());
         else if (k == "gemv_ks") f.gemv_ks = std::atoi(v.c_str());
         else if (k == "gemv_rr") f.gemv_rr = std::atoi(v.c_str());
+        else if (k == "gemv_blocks") f.gemv_blocks = std::atoi(v.c_str());
+        else if (k == "gemv_grid") f.gemv_grid = std::atoi(v.c_str());
     }
     return f;
 }
@@ -329,12 +333,17 @@ int gemv_ksplit(int64_t rows_w, int64_t K, bool w_i8, int num_sms)
 // The row-range form of the skinny-product kernel applies when every row of
 // X and W starts on a 16-byte boundary and there are at least as many W rows
 // as SMs: two persistent CTAs per SM (fewer when rows are few), each owning
-// an equal share of the rows.
+// an equal share of the rows. Where W has more 16-row blocks than CTAs, the shares are whole blocks on
+// as few CTAs as keep the passes per CTA at their least (x[4,4096]
+// W[11008,4096]: 688 blocks, 230 CTAs of 3 blocks, 20.1 us, against 304 CTAs
+// of 36.2 rows each -- three passes, the last a quarter full -- 21.8 us).
 bool plan_gemv_rr(GemvArgs &g, int num_sms)
 {
     if (!g.x_vec || !g.w_vec || g.rows_w < num_sms) return false;
     g.rowrange = 1;
-    g.grid = (int)std::min<int64_t>(2LL * num_sms, g.rows_w);
+    const int64_t nb = cdiv(g.rows_w, 16), ctas = 2LL * num_sms;
+    g.block_rows = nb > ctas;
+    g.grid = (int)(g.block_rows ? cdiv(nb, cdiv(nb, ctas)) : std::min<int64_t>(ctas, g.rows_w));
     return true;
 }
 
@@ -594,7 +603,12 @@ tc_status_t enqueue_gemv(tc_ctx *ctx, tc_stream *s, GemvArgs &g, const Force &f,
 {
     char buf[48];
     if (f.gemv_rr != 0 && f.gemv_ks == 0 && plan_gemv_rr(g, ctx->num_sms)) {
-        std::snprintf(buf, sizeof buf, "_rr%d", g.grid);
+        if (f.gemv_blocks >= 0 && f.gemv_blocks != g.block_rows) {
+            g.block_rows = f.gemv_blocks != 0;
+            g.grid = (int)std::min<int64_t>(2LL * ctx->num_sms, g.rows_w);
+        }
+        if (f.gemv_grid > 0) g.grid = (int)std::min<int64_t>(f.gemv_grid, g.rows_w);
+        std::snprintf(buf, sizeof buf, "_rr%d%s", g.grid, g.block_rows ? "b" : "");
     } else {
         g.rowrange = 0;
         std::snprintf(buf, sizeof buf, "_ks%d", g.ksplit);

@@ -348,8 +348,15 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_rr_kernel(const GemvArg
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const long long K = a.K;
-    const long long r_lo = (long long)blockIdx.x * a.rows_w / gridDim.x;
-    const long long r_hi = (long long)(blockIdx.x + 1) * a.rows_w / gridDim.x;
+    long long r_lo, r_hi;
+    if (a.block_rows) {
+        const long long nb = ((long long)a.rows_w + 15) / 16;
+        r_lo = 16 * ((long long)blockIdx.x * nb / gridDim.x);
+        r_hi = min((long long)a.rows_w, 16 * ((long long)(blockIdx.x + 1) * nb / gridDim.x));
+    } else {
+        r_lo = (long long)blockIdx.x * a.rows_w / gridDim.x;
+        r_hi = (long long)(blockIdx.x + 1) * a.rows_w / gridDim.x;
+    }
     const int nblk = (int)((r_hi - r_lo + 15) / 16);
     const int nslab = (int)((K + SLAB - 1) / SLAB);
     const int per = warp < nslab ? (nslab - warp + GV_WARPS - 1) / GV_WARPS : 0;   // this warp's steps per block

@@ -230,8 +230,10 @@ struct GemvArgs {
     int ksplit;
     // row-range kernel (16-byte aligned rows of X and W): `grid` persistent
     // CTAs (at most rows_w), CTA c owning W rows [c rows_w / grid,
-    // (c + 1) rows_w / grid); ksplit is then unused
-    int rowrange, grid;
+    // (c + 1) rows_w / grid) -- or, with block_rows, whole 16-row blocks
+    // [16 (c nb / grid), 16 ((c + 1) nb / grid)) of the nb = ceil(rows_w / 16)
+    // blocks; ksplit is then unused
+    int rowrange, grid, block_rows;
 };
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t st);
 // fp32 FFMA kernel (exact fp32, ascending-k fused multiply-add chain)

@@ -80,13 +80,16 @@ def test_q8_parity(ctx, shape, x, c):
     assert ctx.last_kernel.startswith(want), ctx.last_kernel
 
 
-@pytest.mark.parametrize("spec", ["", "gemv_ks=1", "gemv_ks=2", "gemv_ks=4", "gemv_ks=8"])
+@pytest.mark.parametrize("spec", ["", "gemv_ks=1", "gemv_ks=2", "gemv_ks=4", "gemv_ks=8", "gemv_blocks=0",
+                                  "gemv_blocks=1"])
 @pytest.mark.parametrize("x", ["f16", "bf16"])
 def test_q8_integer_bitwise(ctx, force, spec, x):
     """Integer activations in [-4, 4] and unit scales: every partial sum is an
-    integer below 2^24, so the fp32 result is exact whatever the K split."""
+    integer below 2^24, so the fp32 result is exact whatever the K split or
+    the share of W's rows (or 16-row blocks, 313 of them for 5003 rows) that
+    each CTA of the row-range form takes."""
     force(spec)
-    for (M, N, K) in [(4, 1100, 4096), (13, 200, 9000), (1, 64, 33)]:
+    for (M, N, K) in [(4, 1100, 4096), (13, 200, 9000), (1, 64, 33), (4, 5003, 1024)]:
         p, _ = synthetic.q8_weight_problem(M, N, K, x, "f32", seed=K + M, x_dist="int")
         out = run(ctx, p, torch.ones(N))
         _, _, ACC = oracle.gemm_q8_weight(p, torch.ones(N))

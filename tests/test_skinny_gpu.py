@@ -173,20 +173,25 @@ def test_gemv_every_row_count(ctx, M, ab):
         assert "_swap" in ctx.last_kernel, ctx.last_kernel
 
 
-@pytest.mark.parametrize("spec", ["", "gemv_ks=1", "gemv_ks=2", "gemv_ks=4", "gemv_ks=8"])
+@pytest.mark.parametrize("spec", ["", "gemv_ks=1", "gemv_ks=2", "gemv_ks=4", "gemv_ks=8", "gemv_blocks=0",
+                                  "gemv_blocks=1", "gemv_grid=230", "gemv_grid=1000", "gemv_blocks=1 gemv_grid=1000"])
 def test_gemv_forms_integer_bitwise(ctx, force, spec):
     """The row-range form (each CTA an equal share of W's rows, the warps'
     sums added in warp order) and the cluster form with K cut over 1 to 8
     CTAs (sums added in rank order): integer data give the exact result
     whatever the cut.  K = 9001 rows are not 16-byte multiples and 5 rows
-    are fewer than the SMs, so those take the cluster form whatever is asked."""
+    are fewer than the SMs, so those take the cluster form whatever is asked.
+    5003 rows are 313 16-row blocks, more than two per SM, so by default
+    they go out in whole blocks (157 CTAs of 2, the last ragged)."""
     force(spec)
-    for (M, N, K) in [(4, 1000, 4096), (16, 33, 9001), (1, 5, 17), (9, 300, 2048)]:
+    for (M, N, K) in [(4, 1000, 4096), (16, 33, 9001), (1, 5, 17), (9, 300, 2048), (4, 5003, 1024)]:
         p = synthetic.make_problem(M, N, K, "f16", "f32", transpose_b=True, beta=1.0, seed=K + len(spec),
                                    dist="int", scale=4.0, c_fill="int")
         out = run(ctx, p)
-        rr = spec == "" and K % 8 == 0 and N >= 152
+        rr = "gemv_ks" not in spec and K % 8 == 0 and N >= 152
         assert ("_rr" in ctx.last_kernel) == rr, ctx.last_kernel
+        if spec == "" and N == 5003:
+            assert ctx.last_kernel.endswith("_rr157b"), ctx.last_kernel
         R, _ = oracle.gemm(p)
         assert np.array_equal(out.numpy().astype(np.float64), R), (M, N, K, ctx.last_kernel)
 
