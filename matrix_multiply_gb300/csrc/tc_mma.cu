@@ -250,14 +250,31 @@ __device__ __forceinline__ void apply_alpha_beta(const MmaArgs &a, int b, long l
     }
 }
 
+// Column col0 + lane's bias (0 past N or without a bias), which the lane
+// loads for bias_act.
+__device__ __forceinline__ float bias_of(const MmaArgs &a, int lane, long long col0)
+{
+    const long long col = col0 + lane;
+    return (a.bias && col < a.N) ? load_c(a.bias, col, a.c_dtype) : 0.0f;
+}
+
+// x[i] for a run-time i < N, from registers (the unrolled selects keep the
+// array out of local memory).
+template <int N>
+__device__ __forceinline__ float pick(const float (&x)[N], int i)
+{
+    float r = x[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k) r = (i == k) ? x[k] : r;
+    return r;
+}
+
 // The warp's chunk, lane = row, v[j] = column col0 + j: add the column's
-// bias (each lane loads one column's value, shared by shuffles) and apply
-// the activation.  Every lane of the warp calls it.
-__device__ __forceinline__ void bias_act(const MmaArgs &a, int lane, long long col0, float (&v)[32])
+// bias (bl: lane j holds column col0 + j's value, from bias_of, shared by
+// shuffles) and apply the activation.  Every lane of the warp calls it.
+__device__ __forceinline__ void bias_act(const MmaArgs &a, float bl, float (&v)[32])
 {
     if (a.bias) {
-        const long long col = col0 + lane;
-        const float bl = (col < a.N) ? load_c(a.bias, col, a.c_dtype) : 0.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, bl, j);
     }
@@ -883,21 +900,22 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
         const CUtensorMap *mapC = &tmC;
         int cur_p = -1, hint = 0;
         const MmaArgs &ea = GROUPED ? ga : args;
-        // alpha/beta, then the chunk to C (TMA store when C allows it)
-        auto emit = [&](int b, long long row, long long col0, float (&v)[32]) {
+        // alpha/beta, then the chunk to C (TMA store when C allows it); bl:
+        // the chunk's bias, lane j holding column col0 + j's
+        auto emit = [&](int b, long long row, long long col0, float (&v)[32], float bl) {
             if (!ea.c_tma) {
                 float *xbuf = reinterpret_cast<float *>(staging(STG_XPOSE));
                 if constexpr (EPI)
                     if (ea.col_scale) col_scale_apply(ea, lane, col0, v);
                 apply_alpha_beta_staged(ea, xbuf, lane, b, row - lane, col0, v);
-                if constexpr (EPI) bias_act(ea, lane, col0, v);
+                if constexpr (EPI) bias_act(ea, bl, v);
                 store_staged(ea, xbuf, lane, b, row - lane, col0, v);
                 return;
             }
             if constexpr (EPI)
                 if (ea.col_scale) col_scale_apply(ea, lane, col0, v);
             apply_alpha_beta(ea, b, row, col0, v);
-            if constexpr (EPI) bias_act(ea, lane, col0, v);
+            if constexpr (EPI) bias_act(ea, bl, v);
             if (ea.c_tma) {
                 // buffers rotate over the stores actually issued
                 const long long row0 = row - lane;
@@ -929,6 +947,13 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
                     cur_p = w.p;
                 }
             }
+            // the bias of this warp's chunks of the tile, loaded before the
+            // wait for the accumulator so that its latency hides behind the MMAs
+            constexpr int NCH = CHUNKS / CSTEP;
+            float bpre[NCH];
+#pragma unroll
+            for (int i = 0; i < NCH; ++i)
+                bpre[i] = EPI ? bias_of(ea, lane, (long long)w.tn * BN + (chunk0 + i * CSTEP) * 32) : 0.0f;
             // segments of the unit (see the MMA warp): one, or the K slices
             // that I8ACC adds up in TMEM
             const int nseg = I8ACC ? (w.kb1 - w.kb0 + args.slice_kb - 1) / args.slice_kb : 1;
@@ -984,7 +1009,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
                             float v[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = __int2float_rn((int)q[j]);
-                            emit(w.b, row, (long long)w.tn * BN + c * 32, v);
+                            emit(w.b, row, (long long)w.tn * BN + c * 32, v, pick(bpre, (c - chunk0) / CSTEP));
                         }
                     }
                     if (!last) tmem_st_wait();
@@ -999,7 +1024,7 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                        emit(w.b, row, (long long)w.tn * BN + c * 32, v);
+                        emit(w.b, row, (long long)w.tn * BN + c * 32, v, pick(bpre, (c - chunk0) / CSTEP));
                     }
                 } else if constexpr (CSPLIT) {
                     // K slice of a cluster split: the partial tile goes to this

@@ -48,10 +48,10 @@ def bound_epilogue(R, T, Y, bias_abs, c_dtype: str, activation: str) -> np.ndarr
     """Bound for C = act(alpha*acc + beta*C_old + bias) against the oracle's
     R = act(Y): the GEMM's 1e-4*T plus the fp32 roundings of the bias add
     (2^-20 of |Y| + |bias|), carried through the activation's slope, plus
-    the fp32 evaluation of GELU (2e-6 |Y|: the device forms x / (1 +
-    exp(-2z)) with a fast exp of relative error below ~1.5e-6 for the
-    arguments that matter, plus a few ulp in z and the division) and one
-    output ulp for f16/bf16."""
+    the fp32 evaluation of GELU (2e-6 |Y|: the device forms x / (1 + 2^u),
+    u = -2 z log2(e), with approximate ex2 and reciprocal instructions whose
+    relative error stays below ~1.5e-6 for the arguments that matter, plus a
+    few ulp in u) and one output ulp for f16/bf16."""
     Y = np.abs(np.asarray(Y, dtype=np.float64))
     pre = 1e-4 * T + 2.0 ** -20 * (Y + bias_abs)
     if activation == "gelu_tanh":
