@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_kernel(const GemvArgs a
     const long long K = a.K;
     const long long nslab = (K + SLAB - 1) / SLAB;
     const long long s0 = (long long)kr * nslab / KS, s1 = (long long)(kr + 1) * nslab / KS;
+    griddep_launch_dependents();     // a dependent launched next may start its set-up
+    griddep_wait();                  // (no-op: this kernel is launched in the ordinary way)
 
     const uint8_t *W = static_cast<const uint8_t *>(a.W);
     const uint8_t *X = static_cast<const uint8_t *>(a.X);
@@ -348,6 +350,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 2) gemv_rr_kernel(const GemvArg
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const long long K = a.K;
+    griddep_launch_dependents();     // launched as a programmatic dependent (see launch_dependent)
+    griddep_wait();
     long long r_lo, r_hi;
     if (a.block_rows) {
         const long long nb = ((long long)a.rows_w + 15) / 16;
@@ -507,8 +511,7 @@ cudaError_t launch_rr(const GemvArgs &a, cudaStream_t st)
         configured[dev].store(true, std::memory_order_release);
     }
     if (a.grid < 1 || a.grid > a.rows_w) return cudaErrorInvalidValue;
-    kern<<<a.grid, GV_WARPS * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)a.grid), dim3(GV_WARPS * 32), smem, st, 1u, a);
 }
 
 template <bool BF16, bool W8, int NT>
@@ -517,6 +520,8 @@ cudaError_t launch_one(const GemvArgs &a, cudaStream_t st)
     constexpr auto kern = gemv_kernel<BF16, W8, NT>;
     const long long blocks = ((long long)a.rows_w + 15) / 16 * a.ksplit;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // an ordinary launch (one small CTA per block and slice: as a dependent,
+    // its CTAs would be placed early, crowding the SMs that are idle then)
     if (a.ksplit == 1) {
         kern<<<(unsigned)blocks, GV_WARPS * 32, 0, st>>>(a);
         return cudaGetLastError();

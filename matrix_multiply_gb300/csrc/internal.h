@@ -4,8 +4,39 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace tc {
+
+// Launch `kern` as a programmatic dependent of the stream's previous kernel
+// (clusters of `cluster` CTAs when above 1).  Its CTAs may be scheduled as
+// soon as every CTA of that kernel has executed
+// griddepcontrol.launch_dependents or exited, so the launch and the
+// kernel's set-up overlap the previous kernel's last CTAs; every kernel
+// launched this way runs griddepcontrol.wait -- which returns once the
+// previous grid has completed and its memory operations are visible --
+// before its first global memory access.  Behind anything but a kernel
+// (a copy, an event, another stream's work) the launch is ordered as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             unsigned cluster, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Tile geometry of the tensor-core kernel.  Every output tile is BM rows by
 // BN columns; the K loop steps BK elements (one 128-byte swizzle row of a

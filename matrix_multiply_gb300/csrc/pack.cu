@@ -14,6 +14,7 @@
 // One launch repacks every operand of a call (a whole group of problems):
 // the CTAs are split between the operands by a prefix table.
 #include "internal.h"
+#include "ptx.cuh"
 
 #include <cuda_bf16.h>
 
@@ -52,6 +53,8 @@ __device__ __forceinline__ uint4 window16(const uint4 &a, const uint4 &b, uint32
 template <typename Index>
 __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const __grid_constant__ PackBatch pb)
 {
+    griddep_launch_dependents();     // the GEMM launched next may start its set-up
+    griddep_wait();                  // (no-op: this kernel is launched in the ordinary way)
     // the copy this CTA works on: the last e with block_begin[e] <= blockIdx.x
     int lo = 0, hi = pb.count - 1;
     while (lo < hi) {
@@ -130,6 +133,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 template <typename Index>
 __global__ void __launch_bounds__(256) split_kernel(const SplitArgs a)
 {
+    griddep_launch_dependents();     // the GEMM launched next may start its set-up
+    griddep_wait();                  // (no-op: this kernel is launched in the ordinary way)
     const Index gpr = (Index)((a.cols + 3) / 4), total = (Index)a.rows * gpr;
     const bool vec = ((reinterpret_cast<uintptr_t>(a.src) & 15u) == 0) && (a.ld_src % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(a.dst) & 7u) == 0) && (a.ld_dst % 4 == 0) &&
@@ -178,6 +183,8 @@ __global__ void __launch_bounds__(256) split_kernel(const SplitArgs a)
 template <typename Index>
 __global__ void __launch_bounds__(256) widen_kernel(const WidenArgs a)
 {
+    griddep_launch_dependents();     // launched as a programmatic dependent (see launch_dependent)
+    griddep_wait();
     const Index gpr = (Index)((a.cols + 15) / 16), total = (Index)a.rows * gpr;
     const bool vec_src = ((reinterpret_cast<uintptr_t>(a.src) & 15u) == 0) && (a.ld_src % 16 == 0);
     for (Index i = (Index)blockIdx.x * 256 + threadIdx.x; i < total; i += (Index)gridDim.x * 256) {
@@ -222,10 +229,8 @@ cudaError_t launch_widen(const WidenArgs &a, cudaStream_t st)
     const long long total = a.rows * ((a.cols + 15) / 16);
     const long long grid = std::min<long long>((total + 255) / 256, 152LL * 16);
     if (total + (long long)grid * 256 < (1LL << 31))
-        widen_kernel<uint32_t><<<(unsigned)grid, 256, 0, st>>>(a);
-    else
-        widen_kernel<unsigned long long><<<(unsigned)grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+        return launch_dependent(widen_kernel<uint32_t>, dim3((unsigned)grid), dim3(256), 0, st, 1u, a);
+    return launch_dependent(widen_kernel<unsigned long long>, dim3((unsigned)grid), dim3(256), 0, st, 1u, a);
 }
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t st)
@@ -233,6 +238,9 @@ cudaError_t launch_split(const SplitArgs &a, cudaStream_t st)
     if (a.rows < 1 || a.cols < 1) return cudaErrorInvalidValue;
     const long long total = a.rows * ((a.cols + 3) / 4);
     const long long grid = std::min<long long>((total + 255) / 256, 152LL * 16);
+    // an ordinary launch (as a dependent: relaxed fp32 4096^3 ~2 us slower a
+    // step, its CTAs placed beside the previous GEMM's); the widening pass
+    // gains from one (int8 4096^3: 164.2 against 166.3 us)
     if (total + (long long)grid * 256 < (1LL << 31))
         split_kernel<uint32_t><<<(unsigned)grid, 256, 0, st>>>(a);
     else
@@ -257,6 +265,9 @@ cudaError_t launch_pack(PackBatch &pb, cudaStream_t st)
     }
     pb.block_begin[pb.count] = blocks;
     if (blocks < 1 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // an ordinary launch: as a dependent of the GEMM before it, its many
+    // small CTAs would be placed beside that GEMM's and crowd the SMs (the
+    // 64-problem ragged batch: 720.8 us a step against 710)
     if (narrow)
         pack_kernel<uint32_t><<<(unsigned)blocks, PACK_THREADS, 0, st>>>(pb);
     else

@@ -657,8 +657,9 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
             if (args.c_tma) prefetch_tmap(&tmC);
             if (args.ws) prefetch_tmap(&tmW);
         }
-        // let the split-K reduction kernel (if any) launch early; it waits
-        // for this grid to finish before it reads the partial tiles
+        // let the next kernel in the stream (the split-K reduction, or the
+        // next GEMM) launch early; it waits for this grid to finish before
+        // it touches global memory
         griddep_launch_dependents();
     }
     __syncwarp();
@@ -673,6 +674,10 @@ __global__ void __launch_bounds__(mma_threads(BN, CG, EPI || GROUPED), 1)
     if (CL == 2) cluster_sync();     // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // launched as a programmatic dependent: everything above (barriers,
+    // TMEM, descriptor prefetch) overlapped the previous kernel; the
+    // operands, C and the status word are touched only once it has finished
+    griddep_wait();
 
     const Watch watch{abort_flag, args.status, args.timeout_ns};
 
@@ -1118,23 +1123,8 @@ cudaError_t launch_kernel(const MmaLaunch &L, cudaStream_t st, const TableOf<GRO
     const int cluster = CSPLIT ? L.args.seg0_split : CG;
     if (CSPLIT && (cluster < 2 || cluster > 16 || L.grid != L.args.total_units || L.grid % cluster != 0))
         return cudaErrorInvalidValue;
-    if (cluster == 1) {
-        kern<<<L.grid, threads, smem, st>>>(L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.grid, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmC, L.tmW, L.args, gt);
+    return launch_dependent(kern, dim3(L.grid), dim3(threads), smem, st, (unsigned)cluster, L.tmA, L.tmB, L.tmC,
+                            L.tmW, L.args, gt);
 }
 
 // Clusters of S CTAs of the BN-wide cluster-split kernel that can be
@@ -1212,6 +1202,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ReduceArgs r)
 {
     static_assert(COLS == 4 || COLS == 8, "whole 16-byte loads");
     griddep_wait();
+    griddep_launch_dependents();     // the next GEMM may start its set-up
     // a GEMM wait that expired left partial tiles unwritten: do not sum them
     if (r.status && *reinterpret_cast<const volatile unsigned *>(r.status) != 0u) return;
     const int groups = r.bn / COLS;                    // threads per row
@@ -1324,21 +1315,12 @@ cudaError_t launch_reduce(const ReduceArgs &r, cudaStream_t st)
     // 256-thread CTA per SM of a GB300
     const long long threads8 = (long long)r.ntiles * r.rows_per_tile * (r.bn / 8);
     const int cols = threads8 < 152LL * 256 ? 4 : 8;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)r.ntiles * (unsigned)(r.rows_per_tile / cols), 1, 1);
-    cfg.blockDim = dim3((unsigned)r.bn, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 grid((unsigned)r.ntiles * (unsigned)(r.rows_per_tile / cols)), block((unsigned)r.bn);
     if (r.int_sum)
-        return cols == 4 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true, 4>, r)
-                         : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true, 8>, r);
-    return cols == 4 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false, 4>, r)
-                     : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false, 8>, r);
+        return cols == 4 ? launch_dependent(splitk_reduce_kernel<true, 4>, grid, block, 0, st, 1u, r)
+                         : launch_dependent(splitk_reduce_kernel<true, 8>, grid, block, 0, st, 1u, r);
+    return cols == 4 ? launch_dependent(splitk_reduce_kernel<false, 4>, grid, block, 0, st, 1u, r)
+                     : launch_dependent(splitk_reduce_kernel<false, 8>, grid, block, 0, st, 1u, r);
 }
 
 cudaError_t launch_mma(const MmaLaunch &L, cudaStream_t st)
