@@ -235,3 +235,17 @@ def q8_weight_problem(M, N, K, x_dtype="f16", c_dtype="f16", *, alpha=1.0, beta=
 def q8_decode(M: int, N: int, K: int, seed: int = 10):
     """fp16 x[M, K] @ (W_q8[N, K] * scale[n])^T, fp16 out (the decode shapes)."""
     return q8_weight_problem(M, N, K, "f16", "f16", seed=seed)
+
+
+def signed_permutation(n: int, seed: int, dtype=torch.float32):
+    """A signed permutation matrix P[n, n] (column j holds s_j = +-1 at row
+    perm[j], zeros elsewhere; in ``dtype``) from a fresh generator, with perm
+    and s as integer arrays.  X @ P is then a signed permutation of X's columns:
+    exact in every dtype, so a chain of such products can be checked value
+    for value however long it is."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    perm = torch.randperm(n, generator=g)
+    s = torch.randint(0, 2, (n,), generator=g) * 2 - 1
+    P = torch.zeros(n, n, dtype=dtype)
+    P[perm, torch.arange(n)] = s.to(dtype)
+    return P, perm.numpy(), s.numpy()
