@@ -397,14 +397,12 @@ class Runner:
         self.As = [[p.A.cuda() for p in probs] for _ in range(copies)]
         self.Bs = [[p.B.cuda() for p in probs] for _ in range(copies)]
         self.Cs = [[p.C.cuda() for p in probs] for _ in range(copies)]
-        self.A, self.B, self.C = self.As[0], self.Bs[0], self.Cs[0]
         self.d = [tg.make_desc(p.M, p.N, p.K, p.ab_dtype, p.c_dtype, transpose_a=p.transpose_a,
                                transpose_b=p.transpose_b, alpha=p.alpha, beta=p.beta,
                                b_dtype="i8" if p.B.dtype == torch_int8() else None) for p in probs]
         # a group's arguments are marshalled once per copy; each step is one C call
         self.groups = ([tg.GroupedGemm(self.d, a, b, c) for a, b, c in zip(self.As, self.Bs, self.Cs)]
                        if len(probs) > 1 else None)
-        self.group = self.groups[0] if self.groups else None
         # the fused-epilogue workloads carry a bias and an activation
         p0 = probs[0]
         self.activation = getattr(p0, "activation", None)
@@ -412,30 +410,19 @@ class Runner:
         self.relaxed = getattr(p0, "precision", None) == "relaxed"
         self.col_scale = p0.col_scale.cuda() if getattr(p0, "col_scale", None) is not None else None
         self.q8_scale = p0.q8_scale.cuda() if getattr(p0, "q8_scale", None) is not None else None
+        # a single product's arguments are marshalled once per copy as well
+        self.calls = ([tg.PreparedGemm(ctx, self.d[0], a[0], b[0], c[0], stream, bias=self.bias,
+                                       activation=self.activation, relaxed=self.relaxed, col_scale=self.col_scale,
+                                       q8_scale=self.q8_scale) for a, b, c in zip(self.As, self.Bs, self.Cs)]
+                      if len(probs) == 1 else None)
 
     def step(self):
-        tg = self.tg
-        if self.copies > 1:
-            self.k = (self.k + 1) % self.copies
-            self.A, self.B, self.C = self.As[self.k], self.Bs[self.k], self.Cs[self.k]
-            if self.groups:
-                self.group = self.groups[self.k]
-        if self.q8_scale is not None:
-            tg.tc_gemm_q8_weight_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.q8_scale,
-                                       self.stream)
-        elif self.col_scale is not None:
-            tg.tc_gemm_i8_dequant_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.col_scale,
-                                        self.stream)
-        elif self.relaxed:
-            tg.tc_gemm_f32_relaxed_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.stream,
-                                         bias=self.bias, activation=self.activation)
-        elif self.activation is not None:
-            tg.tc_gemm_epilogue_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.stream,
-                                      bias=self.bias, activation=self.activation)
-        elif len(self.probs) == 1:
-            tg.tc_gemm_async(self.ctx, self.d[0], self.A[0], self.B[0], self.C[0], self.stream)
+        """One step: the next copy's product (or group), one C call."""
+        self.k = (self.k + 1) % self.copies
+        if self.calls:
+            self.calls[self.k].enqueue()
         else:
-            self.group.enqueue(self.ctx, self.stream)
+            self.groups[self.k].enqueue(self.ctx, self.stream)
 
 
 def timed_loop(torch, runner, tstream, cold, steps, per_step):

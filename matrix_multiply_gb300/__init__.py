@@ -322,6 +322,47 @@ def tc_gemm_grouped_async(ctx: Context, descs, As, Bs, Cs, stream: Stream):
     GroupedGemm(descs, As, Bs, Cs).enqueue(ctx, stream)
 
 
+class PreparedGemm:
+    """One asynchronous product with its arguments checked and marshalled
+    once: tc_gemm_async; with ``bias``/``activation`` tc_gemm_epilogue_async;
+    with ``relaxed`` tc_gemm_f32_relaxed_async; with ``col_scale``
+    tc_gemm_i8_dequant_async; with ``q8_scale`` tc_gemm_q8_weight_async.
+    enqueue() is then one C call -- the library still plans the product and
+    launches its kernels every time -- for a caller that issues the same
+    product on the same buffers many times (the Python checks otherwise
+    cost about as much host time per call as the library itself).  The
+    tensors stay referenced as long as this object."""
+
+    def __init__(self, ctx: Context, d: tc_gemm_desc, A, B, C, stream: Stream, *, bias=None, activation=None,
+                 relaxed: bool = False, col_scale=None, q8_scale=None):
+        _check_capacity(d, A, B, C)
+        vp = ctypes.c_void_p
+        head = (vp(ctx.ptr), ctypes.byref(d))
+        abc = (vp(_addr(A)), vp(_addr(B)), vp(_addr(C)), vp(stream.ptr))
+        self._e = None
+        if q8_scale is not None:
+            _require(q8_scale, d.N, "scale")
+            self._fn, self._name = _lib.tc_gemm_q8_weight_async, "tc_gemm_q8_weight_async"
+            self._args = head + (vp(_addr(q8_scale)),) + abc
+        elif col_scale is not None:
+            _require(col_scale, d.N, "col_scale")
+            self._fn, self._name = _lib.tc_gemm_i8_dequant_async, "tc_gemm_i8_dequant_async"
+            self._args = head + (vp(_addr(col_scale)),) + abc
+        elif relaxed or bias is not None or activation is not None:
+            _check_bias(d, bias)
+            self._e = make_epilogue(bias, activation)
+            self._name = "tc_gemm_f32_relaxed_async" if relaxed else "tc_gemm_epilogue_async"
+            self._fn = getattr(_lib, self._name)
+            self._args = head + (ctypes.byref(self._e),) + abc
+        else:
+            self._fn, self._name = _lib.tc_gemm_async, "tc_gemm_async"
+            self._args = head + abc
+        self._keep = (ctx, d, A, B, C, stream, bias, col_scale, q8_scale)
+
+    def enqueue(self):
+        _check(self._fn(*self._args), self._name)
+
+
 def make_epilogue(bias=None, activation=None) -> tc_epilogue:
     """bias: a CUDA tensor of N values in C's dtype (or an address, or
     None); activation: None/"none" or "gelu_tanh" (or a TC_ACT_* code)."""

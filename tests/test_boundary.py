@@ -266,3 +266,13 @@ def test_q8_weight_validation():
     assert v(q8(), W=1 << 30, C=(1 << 30) + 32 * 64 - 1) == tg.TC_ERR_OVERLAP
     # the scale must not overlap C (4 x 32 f16 at 3 << 40)
     assert v(q8(), scale=(3 << 40) + 16) == tg.TC_ERR_OVERLAP
+
+
+def test_prepared_call_checks_its_arguments_once_up_front():
+    """PreparedGemm runs the same argument checks as the per-call wrappers,
+    when it is built: host tensors and short buffers are refused before any
+    context or stream is touched."""
+    d = tg.make_desc(64, 64, 64, "bf16", "bf16")
+    host = torch.zeros(64 * 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tg.PreparedGemm(None, d, host, host, host, None)
