@@ -3,7 +3,6 @@ enqueue) against the per-call wrappers: the same entry point on the same
 buffers, so every output is bitwise equal, and within the oracle's bound."""
 from __future__ import annotations
 
-import numpy as np
 import pytest
 import torch
 
