@@ -119,7 +119,12 @@ void tc_ctx_destroy(tc_ctx *ctx);
 /* tensorcore gemm.md, "Async, batched, and streams": a stream on which
  * tc_gemm_async enqueues work; only tc_stream_sync waits for it.  Each
  * stream owns its own workspace (split-K partials, repacked operands), so
- * work on different streams never shares scratch memory. */
+ * work on different streams never shares scratch memory.  Stream order is
+ * kept: most of the library's kernels are launched as programmatic
+ * dependents of the kernel before them on the stream, so their set-up may
+ * overlap its last blocks, but each waits for that kernel to complete
+ * before it reads or writes any operand (build addition: the pages do not
+ * describe launches). */
 tc_status_t tc_stream_create(tc_ctx *ctx, tc_stream **out);
 /* Wrap an existing cudaStream_t (e.g. PyTorch's current stream); the
  * library does not destroy the wrapped stream. */
