@@ -481,6 +481,26 @@ tc_status_t make_plan(const tc_gemm_desc *d, const Norm &n, const void *A, const
                 sc = t;
             }
         }
+        // A short K loop (under 16 blocks) on one wave of tiles: a tile's
+        // fixed costs -- set-up, the first loads' latency, the epilogue of
+        // its 128 x BN/CG outputs -- outweigh the rates above, and a tile of
+        // any width up to 256 takes the same MMA time (the ~128-cycle
+        // tcgen05.mma floor).  So 128 x 64 one-CTA tiles when they fit in
+        // one wave (fp16 512^3: 6.7 us against 8.3 with 256 x 128 pairs;
+        // 256^3: 5.8 against 7.1), else one-CTA tiles of the chosen width
+        // when those do (bf16 2048 x 2048 x 512: 9.9 against 10.2 us).
+        if (!f.cg && !f.bn && num_kb < 16) {
+            const int64_t tiles64 = cdiv(d->M, BM) * cdiv(d->N, 64) * n.batch;
+            const int64_t tiles1 = cdiv(d->M, BM) * cdiv(d->N, bn) * n.batch;
+            if (tiles64 <= num_sms) {
+                bn = 64;
+                cg = 1;
+                sc = schedule(tiles64, num_kb, num_sms, 1, 64, f.tail);
+            } else if (cg == 2 && tiles1 <= num_sms) {
+                cg = 1;
+                sc = schedule(tiles1, num_kb, num_sms, 1, bn, f.tail);
+            }
+        }
     }
     const int workers = cg == 2 ? std::max(num_sms / 2, 1) : num_sms;   // tiles in flight
     if (bn == 0) return TC_ERR_VARIANT;

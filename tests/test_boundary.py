@@ -153,6 +153,17 @@ def test_plan_tensor_core_shapes():
     assert plan(4096, 4096, 8192, "bf16", "f32", tb=True).startswith("tcgen05_nt_bf16_f32")
 
 
+def test_plan_short_k_single_wave_takes_one_cta_tiles():
+    """Under 16 K blocks on one wave of tiles: 128 x 64 one-CTA tiles when
+    they fit in one wave, else one-CTA tiles of the modelled width; a long K
+    loop keeps the CTA pair."""
+    assert plan(256, 256, 256, "f16", "f16") == "tcgen05_nn_f16_f16_128x64"
+    assert plan(512, 512, 512, "bf16", "bf16") == "tcgen05_nn_bf16_bf16_128x64"
+    assert plan(2048, 2048, 512, "bf16", "bf16") == "tcgen05_nn_bf16_bf16_128x256"
+    assert plan(2048, 2048, 2048, "f16", "f16") == "tcgen05_nn_f16_f16_256x256_pair"
+    assert plan_forced("cg=2", 2048, 2048, 512, "bf16", "bf16") == "tcgen05_nn_bf16_bf16_256x256_pair"
+
+
 def test_plan_split_k_for_tall_k():
     # the slices of a tile form one cluster (at most 16 CTAs) and are reduced
     # on chip; 64-wide tiles give 8 tiles x 16 slices = 128 CTAs, each with
