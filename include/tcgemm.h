@@ -240,7 +240,8 @@ tc_status_t tc_gemm_q8_weight_validate(const tc_gemm_desc *d, const float *scale
 
 /* Same GEMM with HOST operands: copies A and B (and C when beta != 0) to the
  * device, runs, copies C back and waits.  Device buffers are cached in the
- * context.  Pinned host memory gives full copy bandwidth. */
+ * context, so concurrent calls on one context run one after the other.
+ * Pinned host memory gives full copy bandwidth. */
 tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
                          const void *B_host, void *C_host);
 

@@ -48,6 +48,8 @@ struct tc_ctx {
     void *dbuf[3] = {nullptr, nullptr, nullptr};  // device copies for tc_gemm_host
     size_t dcap[3] = {0, 0, 0};
     cudaStream_t copy_in = nullptr, copy_out = nullptr;   // tc_gemm_host's copy streams
+    std::vector<cudaEvent_t> host_ev;              // tc_gemm_host's events, created once and reused
+    std::mutex host_mu;                            // one tc_gemm_host at a time (it owns dbuf, host_ev)
     int max_pairs[3] = {-1, -1, -1};               // resident CTA pairs (BN 128, 192, 256), queried once
     int csplit_clusters[2][17];                    // resident cluster splits (BN 64, 128; S), -1 = not queried
     std::mutex mu;
@@ -1470,6 +1472,7 @@ void tc_ctx_destroy(tc_ctx *ctx)
         if (ctx->dbuf[i]) cudaFree(ctx->dbuf[i]);
     if (ctx->copy_in) cudaStreamDestroy(ctx->copy_in);
     if (ctx->copy_out) cudaStreamDestroy(ctx->copy_out);
+    for (cudaEvent_t e : ctx->host_ev) cudaEventDestroy(e);
     delete ctx;
 }
 
@@ -1650,6 +1653,7 @@ tc_status_t tc_gemm_grouped_async(tc_ctx *ctx, int n, const tc_gemm_desc *d, con
 tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host, const void *B_host, void *C_host)
 {
     if (!ctx) return TC_ERR_NULL;
+    std::lock_guard<std::mutex> host_lock(ctx->host_mu);
     Norm n;
     // validate on the host buffers (overlap between host ranges, dims, ...)
     tc_status_t st = validate(d, A_host, B_host, C_host, 1, 0, 0, 0, &n);
@@ -1689,17 +1693,23 @@ tc_status_t tc_gemm_host(tc_ctx *ctx, const tc_gemm_desc *d, const void *A_host,
     const uint8_t *hA = static_cast<const uint8_t *>(A_host);
     uint8_t *hC = static_cast<uint8_t *>(C_host);
     cudaStream_t comp = ctx->def->st;
-    std::vector<cudaEvent_t> ev;
+    // events from the context's pool, created on first use and re-recorded
+    // by later calls (each call has synchronised all three streams before it
+    // returns, so no earlier record is still pending)
+    size_t next_ev = 0;
     auto event = [&](cudaEvent_t *e) {
-        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
-        ev.push_back(*e);
+        if (next_ev == ctx->host_ev.size()) {
+            cudaEvent_t fresh;
+            if (cudaEventCreateWithFlags(&fresh, cudaEventDisableTiming) != cudaSuccess) return false;
+            ctx->host_ev.push_back(fresh);
+        }
+        *e = ctx->host_ev[next_ev++];
         return true;
     };
     auto finish = [&](tc_status_t result) {
         cudaStreamSynchronize(ctx->copy_in);
         cudaStreamSynchronize(ctx->copy_out);
         tc_status_t s2 = tc_stream_sync(ctx->def);
-        for (cudaEvent_t e : ev) cudaEventDestroy(e);
         return result != TC_OK ? result : s2;
     };
     // one band of op(A) rows [m0, m1): rows of A, or columns of A stored [K, M]
