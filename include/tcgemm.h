@@ -123,8 +123,12 @@ void tc_ctx_destroy(tc_ctx *ctx);
  * kept: most of the library's kernels are launched as programmatic
  * dependents of the kernel before them on the stream, so their set-up may
  * overlap its last blocks, but each waits for that kernel to complete
- * before it reads or writes any operand (build addition: the pages do not
- * describe launches). */
+ * before it reads or writes any operand.  They also signal
+ * griddepcontrol.launch_dependents early, so a caller's own kernel launched
+ * after them with programmatic stream serialisation must wait
+ * (cudaGridDependencySynchronize) before it reads their results; ordinary
+ * launches, copies and events are ordered as usual (build addition: the
+ * pages do not describe launches). */
 tc_status_t tc_stream_create(tc_ctx *ctx, tc_stream **out);
 /* Wrap an existing cudaStream_t (e.g. PyTorch's current stream); the
  * library does not destroy the wrapped stream. */
