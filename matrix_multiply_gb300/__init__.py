@@ -11,7 +11,9 @@ the CUDA kernels of ``_lib/libtcgemm.so``.  The functions keep the C names
 device addresses or torch tensors (PyTorch provides device memory and
 streams only).  Where a tensor is given, its capacity is checked in
 elements before the call (the tessl architecture.md "nn Boundary" rule: a
-view of too few elements is refused, nothing is launched).
+view of too few elements is refused, nothing is launched).  ``GroupedGemm``
+and ``PreparedGemm`` run those checks once for a group or a single product
+that is issued many times; each ``enqueue()`` is then one C call.
 
 There is no fallback: if the library is missing, importing this package
 raises.  Build it with ``python -c "import __graft_entry__ as g; g.build()"``.
